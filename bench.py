@@ -1,0 +1,454 @@
+"""Benchmark of the HiSparse top-k sparse decode hot path on GB300.
+
+One step = one decode step of the fully-resident workload (32 requests x 8192
+context, anchor + 3 drafts = 128 query rows, 128 heads, top-k 2048, 576-dim
+bf16 latent rows): hs_resolve_topk + hs_sparse_attn_decode, inputs resident in
+HBM, L2 flushed (256 MiB write) before every timed step. The headline value is
+query rows per second; the JSON line also carries
+
+  roofline      the attention kernel's algorithmic bytes / its CUDA-event time
+                against the measured HBM copy bandwidth,
+  e2e           the same step through the C ABI with page-locked host buffers:
+                host->device copies of q / top-k / row descriptors and the
+                device->host copy of the output inside the timed region,
+  swap_in       host-backed workload (64 x 32768 context, 4096 hot slots, 80 %
+                reuse, 16 steps): swap-in GB/s against the measured
+                host->device link bandwidth,
+  cpu_baseline  the CPU oracle timed on a bounded sample on this host.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs the same per-GPU workload (weak scaling, no
+data-path collective); rank 0 prints the line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "sparse-attn decode query-rows/sec and swap-in GB/s at 1 GB300 (% of roofline)"
+L2_FLUSH_BYTES = 256 << 20
+ROW_BYTES = 576 * 2
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def _attn_bytes(valid_counts: np.ndarray, H: int, K: int) -> int:
+    """Algorithmic bytes of one attention launch: the gathered latent rows,
+    q, the output and the index table."""
+    R = valid_counts.shape[0]
+    return int(valid_counts.sum()) * ROW_BYTES + R * H * (576 * 2 + 512 * 2) + R * K * 4
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _source_sha() -> str:
+    p = os.path.join(ROOT, "hisparse_top_sparse_gb300", "csrc", "hs_attn.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def _traffic():
+    """dram bytes per attention launch from the committed ncu summary, when
+    it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("source_sha") != _source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- ours ---
+
+def run_ours(args):
+    import hisparse_top_sparse_gb300 as hs
+    from hisparse_top_sparse_gb300 import _build
+    _build.build()
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    cfg = W.get_config(2)
+    cfg.seed = cfg.seed + 1000 * rank          # each rank its own batch, same shape
+    rc = W.resident_case(cfg, 0, device=dev)
+    R, H, K = cfg.R, cfg.H, cfg.K
+    idx = torch.empty_like(rc["topk"])
+    valid = torch.empty_like(rc["req"])
+    out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((R, H), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        hs.hs_resolve_topk(rc["req"], rc["clen"], rc["bt"], rc["topk"], cfg.block_size,
+                           cfg.block_size, idx, valid)
+        ev_a0.record(stream)
+        hs.hs_sparse_attn_decode(rc["q"], rc["kv"], idx, cfg.scale, out, lse)
+        ev_a1.record(stream)
+
+    ev_a0, ev_a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    valid_np = valid.cpu().numpy()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    step_ms, attn_ms = [], []
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        for _ in range(args.steps):
+            flush.fill_(1)
+            s0.record(stream)
+            step()
+            s1.record(stream)
+            s1.synchronize()
+            step_ms.append(s0.elapsed_time(s1))
+            attn_ms.append(ev_a0.elapsed_time(ev_a1))
+    torch.cuda.synchronize()
+    barrier()
+    t_step = sum(step_ms) / len(step_ms)
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([t_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step = float(t.item())
+    rows_per_s = ws * R / (t_step * 1e-3)
+
+    # roofline of the attention kernel
+    peaks, peak_kind = _peaks()
+    t_attn = sum(attn_ms) / len(attn_ms) * 1e-3
+    alg_bytes = _attn_bytes(valid_np, H, K)
+    achieved = alg_bytes / t_attn / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": _traffic(), "peak_kind": peak_kind,
+                "kernel": "k_attn_mma", "algorithmic_bytes_per_launch": alg_bytes,
+                "attn_ms": round(t_attn * 1e3, 4),
+                "tensor_floor_ms": round(R * H * K * 2 * (576 + 512) / (peaks["bf16_tflops"] * 1e12)
+                                         * 1e3, 4)}
+
+    e2e = run_e2e(hs, cfg, rc, dev, args)
+    swap = run_swap_bench(hs, dev, args) if (rank == 0 and not args.skip_swap) else None
+    cpu = cpu_baseline(cfg, rc) if (rank == 0 and ws == 1 and not args.skip_cpu) else None
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(rows_per_s, 1), "unit": "query-rows/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "requests": cfg.B, "context": cfg.L[0],
+                       "query_rows": R, "heads": H, "top_k": K, "latent_dim": 576,
+                       "value_dim": 512, "block_size": cfg.block_size,
+                       "step": "hs_resolve_topk + hs_sparse_attn_decode",
+                       "l2": "flushed before every timed step (256 MiB write)",
+                       "parallelism": f"replicas x{ws}, requests sharded, no collective"},
+            "gpu_launches": 2 * args.steps,
+            "roofline": roofline, "e2e": e2e, "clocks": clk.summary(),
+            "swap_in": swap, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(hs, cfg, rc, dev, args):
+    """The same step through the C ABI from page-locked host buffers."""
+    R, H, K = cfg.R, cfg.H, cfg.K
+    h_q = rc["q"].cpu().pin_memory()
+    h_topk = rc["topk"].cpu().pin_memory()
+    h_req = rc["req"].cpu().pin_memory()
+    h_clen = rc["clen"].cpu().pin_memory()
+    h_out = torch.empty((R, H, 512), dtype=torch.bfloat16).pin_memory()
+    d_q, d_topk = torch.empty_like(rc["q"]), torch.empty_like(rc["topk"])
+    d_req, d_clen = torch.empty_like(rc["req"]), torch.empty_like(rc["clen"])
+    idx = torch.empty_like(rc["topk"])
+    out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_topk, h_req, h_clen))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_topk.copy_(h_topk, non_blocking=True)
+        d_req.copy_(h_req, non_blocking=True)
+        d_clen.copy_(h_clen, non_blocking=True)
+        hs.hs_resolve_topk(d_req, d_clen, rc["bt"], d_topk, cfg.block_size, cfg.block_size, idx)
+        hs.hs_sparse_attn_decode(d_q, rc["kv"], idx, cfg.scale, out)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    b.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    return {"value": round(R / (ms * 1e-3), 1), "unit": "query-rows/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def measure_link(hs, dev):
+    """Host->device bandwidth: best of a 1 GiB pinned cudaMemcpyAsync and the
+    zero-copy read probe over the same pinned buffer."""
+    n = 1 << 30
+    host = torch.empty(n, dtype=torch.uint8).pin_memory()
+    host.fill_(3)
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best_copy = 0.0
+    for _ in range(3):
+        a.record()
+        d.copy_(host, non_blocking=True)
+        b.record()
+        b.synchronize()
+        best_copy = max(best_copy, n / (a.elapsed_time(b) * 1e-3) / 1e9)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    best_zc = 0.0
+    for blocks in (sms * 4, sms * 8, sms * 16):
+        sink = torch.empty(blocks, dtype=torch.int64, device=dev)
+        for _ in range(2):
+            a.record()
+            hs.hs_read_probe(host, sink, blocks)
+            b.record()
+            b.synchronize()
+            best_zc = max(best_zc, n / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del host, d
+    return {"copy_engine_gbs": round(best_copy, 1), "zero_copy_gbs": round(best_zc, 1),
+            "peak_gbs": round(max(best_copy, best_zc), 1)}
+
+
+def run_swap_bench(hs, dev, args):
+    """Workload 3: swap-in GB/s over 16 steps (step 0 cold, reported apart)."""
+    cfg = W.get_config(3)
+    req, ri = W.rows_of(cfg)
+    clen = W.causal_lengths(cfg.L, req, ri)
+    hb = W.host_backed_case(cfg, device=dev)
+    buf = hs.HsBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hb["hot"],
+                      hb["pool"], hb["hbt"])
+    sets = [W.locality_sets(cfg, cfg.L[b], b, cfg.steps) for b in range(cfg.B)]
+    topks = [torch.as_tensor(W.topk_shared_sets(cfg, sets, s), device=dev)
+             for s in range(cfg.steps)]
+    t_req, t_clen = torch.as_tensor(req, device=dev), torch.as_tensor(clen, device=dev)
+    out = torch.empty((cfg.R, cfg.K), dtype=torch.int32, device=dev)
+    stats = torch.zeros(2, dtype=torch.int64, device=dev)
+    q = W.step_q(cfg, 0, device=dev)
+    o = torch.empty((cfg.R, cfg.H, 512), dtype=torch.bfloat16, device=dev)
+    a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    swap_ms, attn_ms, miss = [], [], []
+    for s in range(cfg.steps):
+        stats.zero_()
+        a.record()
+        hs.hs_swap_in(buf, t_req, t_clen, hb["kv_len"], topks[s], out, None, stats)
+        b.record()
+        hs.hs_sparse_attn_decode(q, hb["hot"], out, cfg.scale, o)
+        c.record()
+        c.synchronize()
+        swap_ms.append(a.elapsed_time(b))
+        attn_ms.append(b.elapsed_time(c))
+        miss.append(int(stats[1].item()))
+    st = hs.hs_get_status(buf)
+    buf.close()
+    del hb
+    link = measure_link(hs, dev)
+    steady = range(1, cfg.steps)
+    bytes_ss = sum(miss[s] for s in steady) * ROW_BYTES
+    t_ss = sum(swap_ms[s] for s in steady) * 1e-3
+    gbs = bytes_ss / t_ss / 1e9
+    return {"workload": cfg.name, "gbs": round(gbs, 2), "link": link,
+            "frac_of_link": round(gbs / link["peak_gbs"], 4),
+            "misses_per_step": miss, "swap_ms_per_step": [round(x, 4) for x in swap_ms],
+            "cold_step_gbs": round(miss[0] * ROW_BYTES / (swap_ms[0] * 1e-3) / 1e9, 2),
+            "attn_ms_per_step_mean": round(statistics.mean(attn_ms[1:]), 4),
+            "query_rows_per_s_attention": round(cfg.R / (statistics.mean(attn_ms[1:]) * 1e-3), 1),
+            "status": st, "gpu_launches_per_step": 6}
+
+
+def cpu_baseline(cfg, rc, budget_s: float = 12.0):
+    """The CPU oracle on this host: resolve + float64 attention, row by row,
+    until the time budget is spent. Returns query rows per second."""
+    from oracle import hs_oracle as O
+    q = rc["q"].cpu()
+    kv = rc["kv"]
+    topk, req, clen, bt = rc["topk_np"], rc["req_np"], rc["clen_np"], rc["bt_np"]
+    rows_done = 0
+    t0 = time.perf_counter()
+    r = 0
+    while time.perf_counter() - t0 < budget_s and r < cfg.R:
+        idx, _, _ = O.resolve_topk(req[r:r + 1], clen[r:r + 1], bt, topk[r:r + 1],
+                                   cfg.block_size, cfg.block_size)
+        rows = torch.as_tensor(idx[0][idx[0] >= 0], device=kv.device)
+        kv_rows = kv[rows].cpu()
+        O.sparse_attn_decode(q[r:r + 1], kv_rows, np.arange(len(rows))[None, :], cfg.scale)
+        rows_done += 1
+        r += 1
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(rows_done / dt, 3), "unit": "query-rows/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{rows_done} query rows of {cfg.name} (resolve + float64 attention, "
+                      f"{dt:.1f} s; numpy BLAS threads over the process's cores)"}
+
+
+# ------------------------------------------------------------ reference ---
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, timed on this host's cores, on the
+    same workload and metric, each step a bounded sample of query rows."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    cfg = W.get_config(2)
+    rc = W.resident_case(cfg, 0, device=dev)
+    rows_per_step = 2
+    times = []
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        cb = cpu_baseline_rows(cfg, rc, s * rows_per_step % cfg.R, rows_per_step)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+    per_row = sum(times) / (len(times) * rows_per_step)
+    v = 1.0 / per_row
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "query-rows/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sum(times) / len(times) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "requests": cfg.B, "context": cfg.L[0],
+                       "query_rows": cfg.R, "heads": cfg.H, "top_k": cfg.K,
+                       "sample_rows_per_step": rows_per_step},
+            "cpu_baseline": {"value": round(v, 3), "unit": "query-rows/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"{rows_per_step} query rows per step (resolve + "
+                                       "float64 attention)"},
+            "e2e": {"value": round(v, 3), "unit": "query-rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line))
+
+
+def cpu_baseline_rows(cfg, rc, r0, n):
+    from oracle import hs_oracle as O
+    kv = rc["kv"]
+    for r in range(r0, r0 + n):
+        idx, _, _ = O.resolve_topk(rc["req_np"][r:r + 1], rc["clen_np"][r:r + 1], rc["bt_np"],
+                                   rc["topk_np"][r:r + 1], cfg.block_size, cfg.block_size)
+        rows = torch.as_tensor(idx[0][idx[0] >= 0], device=kv.device)
+        O.sparse_attn_decode(rc["q"][r:r + 1].cpu(), kv[rows].cpu(),
+                             np.arange(len(rows))[None, :], cfg.scale)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-swap", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,272 @@
+"""Thin Python binding of libhisparse (the C ABI in include/hisparse.h).
+
+Argument marshalling only: every function checks tensor devices, dtypes,
+shapes and contiguity, passes raw pointers and the CUDA stream to the C call
+of the same name, and raises ``HisparseError`` on a non-zero status. All
+computation runs in the library's CUDA kernels; there is no other path. If
+the library is not built, every call raises.
+
+PyTorch provides device memory and streams only.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB as _LIB_PATH, build  # noqa: F401
+
+HS_OK = 0
+HS_ERR_INVALID_ARG = -1
+HS_ERR_CAPACITY = -2
+HS_ERR_INDEX = -3
+HS_ERR_CUDA = -4
+HS_ERR_TIMEOUT = -5
+HS_ERR_UNSUPPORTED = -6
+HS_STATUS_INDEX = 1
+HS_STATUS_CAPACITY = 2
+HS_LOGITS_F32 = 0
+HS_LOGITS_BF16 = 1
+LATENT_DIM = 576
+VALUE_DIM = 512
+
+EXPORTS = (
+    "hs_buffer_create", "hs_buffer_destroy", "hs_request_reset", "hs_get_status",
+    "hs_buffer_dump", "hs_buffer_clock", "hs_last_error_string", "hs_resolve_topk",
+    "hs_swap_in", "hs_sparse_attn_decode", "hs_verify_finalize", "hs_read_probe",
+)
+
+
+class HisparseError(RuntimeError):
+    def __init__(self, code: int, what: str, msg: str):
+        super().__init__(f"{what} failed with status {code}: {msg}")
+        self.code = code
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [
+        ("max_reqs", ctypes.c_int32), ("slots_per_req", ctypes.c_int32),
+        ("step_slots", ctypes.c_int32), ("max_ctx", ctypes.c_int32),
+        ("block_size", ctypes.c_int32), ("hbt_stride", ctypes.c_int32),
+        ("hot_kv", ctypes.c_void_p), ("host_pool", ctypes.c_void_p),
+        ("host_pool_rows", ctypes.c_int64), ("host_block_table", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_I64 = ctypes.c_int64
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with __graft_entry__.build() "
+                "(there is no fallback implementation)")
+        L = ctypes.CDLL(_LIB_PATH)
+        sig = {
+            "hs_buffer_create": (_I, [ctypes.POINTER(_Desc), ctypes.POINTER(_P)]),
+            "hs_buffer_destroy": (_I, [_P]),
+            "hs_request_reset": (_I, [_P, _I, _P]),
+            "hs_get_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
+            "hs_buffer_dump": (_I, [_P, _P, _P, _P, _P]),
+            "hs_buffer_clock": (_I64, [_P]),
+            "hs_last_error_string": (ctypes.c_char_p, []),
+            "hs_resolve_topk": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
+            "hs_swap_in": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P]),
+            "hs_sparse_attn_decode": (_I, [_P, _P, _I64, _P, _I, _I, _I, ctypes.c_float,
+                                           _P, _P, _P]),
+            "hs_verify_finalize": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+            "hs_read_probe": (_I, [_P, ctypes.c_size_t, _P, _I, _P]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != HS_OK:
+        raise HisparseError(rc, what, lib().hs_last_error_string().decode(errors="replace"))
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t, name, dtype=None, shape=None, allow_none=False, device=True):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+# ------------------------------------------------------------------ buffer --
+
+class HsBuffer:
+    """Owner of an hs_buffer handle (the per-request hot buffer's metadata).
+    The tensors passed in stay owned by the caller and must outlive it."""
+
+    def __init__(self, max_reqs, slots_per_req, step_slots, max_ctx, block_size,
+                 hot_kv: torch.Tensor, host_pool: torch.Tensor,
+                 host_block_table: torch.Tensor):
+        S_tot = slots_per_req + step_slots
+        _ptr(hot_kv, "hot_kv", torch.bfloat16, (max_reqs * S_tot, LATENT_DIM))
+        if host_pool.dtype != torch.bfloat16 or host_pool.dim() != 2 or \
+                host_pool.shape[1] != LATENT_DIM or not host_pool.is_contiguous():
+            raise ValueError("host_pool must be a contiguous bf16 [rows][576] tensor")
+        if not host_pool.is_cuda and not host_pool.is_pinned():
+            raise ValueError("host_pool must be pinned host memory or a CUDA tensor")
+        _ptr(host_block_table, "host_block_table", torch.int32)
+        if host_block_table.dim() != 2 or host_block_table.shape[0] < max_reqs:
+            raise ValueError("host_block_table must be int32 [max_reqs][hbt_stride]")
+        d = _Desc(max_reqs, slots_per_req, step_slots, max_ctx, block_size,
+                  host_block_table.shape[1], hot_kv.data_ptr(), host_pool.data_ptr(),
+                  host_pool.shape[0], host_block_table.data_ptr())
+        h = ctypes.c_void_p()
+        _check(lib().hs_buffer_create(ctypes.byref(d), ctypes.byref(h)), "hs_buffer_create")
+        self.handle = h
+        self.max_reqs, self.S, self.n_step = max_reqs, slots_per_req, step_slots
+        self.S_tot, self.max_ctx, self.block_size = S_tot, max_ctx, block_size
+        self.hot_kv, self.host_pool, self.hbt = hot_kv, host_pool, host_block_table
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().hs_buffer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def clock(self) -> int:
+        return int(lib().hs_buffer_clock(self.handle))
+
+    def dump(self, stream=None):
+        """(token_slot [max_reqs][max_ctx], slot_token [max_reqs][S],
+        slot_ts [max_reqs][S]) as CPU tensors."""
+        ts = torch.empty((self.max_reqs, self.max_ctx), dtype=torch.int32)
+        st = torch.empty((self.max_reqs, self.S), dtype=torch.int32)
+        tt = torch.empty((self.max_reqs, self.S), dtype=torch.int64)
+        _check(lib().hs_buffer_dump(self.handle, _stream(stream), ts.data_ptr(),
+                                    st.data_ptr(), tt.data_ptr()), "hs_buffer_dump")
+        return ts, st, tt
+
+
+def hs_buffer_create(**kw) -> HsBuffer:
+    return HsBuffer(**kw)
+
+
+def hs_buffer_destroy(buf: HsBuffer) -> None:
+    buf.close()
+
+
+def hs_request_reset(buf: HsBuffer, req: int, stream=None) -> None:
+    _check(lib().hs_request_reset(buf.handle, int(req), _stream(stream)), "hs_request_reset")
+
+
+def hs_get_status(buf: HsBuffer, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check(lib().hs_get_status(buf.handle, _stream(stream), ctypes.byref(v)), "hs_get_status")
+    return int(v.value)
+
+
+# ----------------------------------------------------------------- calls --
+
+def hs_resolve_topk(req_id_per_row, row_causal_len, block_table, topk, block_size: int,
+                    phys_block_stride: int, out_idx, out_valid=None, status=None,
+                    stream=None) -> None:
+    R, K = topk.shape
+    _check(lib().hs_resolve_topk(
+        _ptr(req_id_per_row, "req_id_per_row", torch.int32, (R,)),
+        _ptr(row_causal_len, "row_causal_len", torch.int32, (R,)),
+        _ptr(block_table, "block_table", torch.int32), block_table.shape[1],
+        _ptr(topk, "topk", torch.int32), R, K, block_size, phys_block_stride,
+        _ptr(out_idx, "out_idx", torch.int32, (R, K)),
+        _ptr(out_valid, "out_valid", torch.int32, (R,), allow_none=True),
+        _ptr(status, "status", torch.int32, (1,), allow_none=True),
+        _stream(stream)), "hs_resolve_topk")
+
+
+def hs_swap_in(buf: HsBuffer, req_id_per_row, row_causal_len, kv_len, topk, out_slot_idx,
+               out_valid=None, stats=None, stream=None) -> None:
+    R, K = topk.shape
+    _check(lib().hs_swap_in(
+        buf.handle,
+        _ptr(req_id_per_row, "req_id_per_row", torch.int32, (R,)),
+        _ptr(row_causal_len, "row_causal_len", torch.int32, (R,)),
+        _ptr(kv_len, "kv_len", torch.int32, (buf.max_reqs,)),
+        _ptr(topk, "topk", torch.int32), R, K,
+        _ptr(out_slot_idx, "out_slot_idx", torch.int32, (R, K)),
+        _ptr(out_valid, "out_valid", torch.int32, (R,), allow_none=True),
+        _ptr(stats, "stats", torch.int64, (2,), allow_none=True),
+        _stream(stream)), "hs_swap_in")
+
+
+def hs_sparse_attn_decode(q, kv, idx, scale: float, out, lse=None, stream=None) -> None:
+    R, H, D = q.shape
+    if D != LATENT_DIM:
+        raise ValueError("q must be [R][H][576]")
+    K = idx.shape[1]
+    _check(lib().hs_sparse_attn_decode(
+        _ptr(q, "q", torch.bfloat16), _ptr(kv, "kv", torch.bfloat16), kv.shape[0],
+        _ptr(idx, "idx", torch.int32, (R, K)), R, H, K, float(scale),
+        _ptr(out, "out", torch.bfloat16, (R, H, VALUE_DIM)),
+        _ptr(lse, "lse", torch.float32, (R, H), allow_none=True),
+        _stream(stream)), "hs_sparse_attn_decode")
+
+
+def hs_verify_finalize(buf: HsBuffer, logits, draft_tokens, step_kv, kv_len, accept_len,
+                       next_token, req_ids=None, stream=None) -> None:
+    B, d1, V = logits.shape
+    d = d1 - 1
+    if logits.dtype == torch.float32:
+        dt = HS_LOGITS_F32
+    elif logits.dtype == torch.bfloat16:
+        dt = HS_LOGITS_BF16
+    else:
+        raise TypeError("logits must be float32 or bfloat16")
+    _check(lib().hs_verify_finalize(
+        buf.handle, _ptr(logits, "logits"), dt, B, d, V,
+        _ptr(draft_tokens, "draft_tokens", torch.int32, (B, d), allow_none=(d == 0)),
+        _ptr(step_kv, "step_kv", torch.bfloat16, (B, d1, LATENT_DIM)),
+        _ptr(req_ids, "req_ids", torch.int32, (B,), allow_none=True),
+        _ptr(kv_len, "kv_len", torch.int32, (buf.max_reqs,)),
+        _ptr(accept_len, "accept_len", torch.int32, (B,)),
+        _ptr(next_token, "next_token", torch.int32, (B,)),
+        _stream(stream)), "hs_verify_finalize")
+
+
+def hs_read_probe(src: torch.Tensor, sink: torch.Tensor, blocks: int, stream=None) -> None:
+    nbytes = src.numel() * src.element_size()
+    if not (src.is_cuda or src.is_pinned()):
+        raise ValueError("src must be pinned host memory or a CUDA tensor")
+    _check(lib().hs_read_probe(src.data_ptr(), nbytes,
+                               _ptr(sink, "sink", torch.int64, (blocks,)), blocks,
+                               _stream(stream)), "hs_read_probe")

@@ -1,0 +1,221 @@
+// a7-a8: greedy verify of [anchor, drafts] and commit of the accepted prefix.
+//
+// "投机解码的 KV 流转：prefill 阶段 DFlash 也要吃下整个 prompt", section ④: the
+// target runs once over the anchor and the d drafts; the logits at input i
+// check draft i+1, the first mismatch yields the correction token, and when
+// every draft passes the last input's logits yield one more token. Only the
+// KV of the agreeing prefix (anchor + accepted drafts) is kept; the token
+// picked last has no KV until the next round, where it is the anchor at
+// position L (section ⑥ and the closing table).
+//
+// Two launches:
+//   k_verify_argmax  block per (request, input) row: streaming argmax over the
+//                    vocabulary with 16-byte loads, ties to the lowest index
+//   k_verify_commit  block per request: accepted length, next token, host-pool
+//                    write of the kept rows through the mapped pool, LRU slot
+//                    choice (m+1 rounds of a block-wide min over (ts, slot)),
+//                    hot-slot write and the kv_len update
+
+#include <float.h>
+
+#include "hs_internal.cuh"
+
+namespace {
+
+struct Best {
+  float v;
+  int32_t i;
+};
+
+__device__ __forceinline__ void take(Best &b, float v, int32_t i) {
+  if (v > b.v || (v == b.v && i < b.i)) { b.v = v; b.i = i; }
+}
+
+__device__ __forceinline__ Best warp_best(Best b) {
+  for (int off = 16; off; off >>= 1) {
+    const float v = __shfl_xor_sync(0xffffffffu, b.v, off);
+    const int32_t i = __shfl_xor_sync(0xffffffffu, b.i, off);
+    take(b, v, i);
+  }
+  return b;
+}
+
+template <int DTYPE>
+__global__ void __launch_bounds__(512) k_verify_argmax(const void *__restrict__ logits,
+                                                       int32_t V, int32_t rows_per_req,
+                                                       int32_t n_step, int32_t *__restrict__ pred) {
+  const int64_t row = blockIdx.x;
+  Best best{-INFINITY, INT32_MAX};
+  const int64_t elem = (DTYPE == HS_LOGITS_F32) ? 4 : 2;
+  const char *base = reinterpret_cast<const char *>(logits) + row * (int64_t)V * elem;
+  const int per16 = 16 / (int)elem;
+  // 16-byte path over the aligned body, scalar head and tail
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(base);
+  int head = (int)(((16 - (addr & 15)) & 15) / elem);
+  if ((addr & (elem - 1)) != 0) head = V;  // misaligned element: all scalar
+  if (head > V) head = V;
+  const int nvec = (V - head) / per16;
+  auto load = [&](int32_t i) -> float {
+    if (DTYPE == HS_LOGITS_F32) return reinterpret_cast<const float *>(base)[i];
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[i]);
+  };
+  for (int i = threadIdx.x; i < head; i += blockDim.x) take(best, load(i), i);
+  const uint4 *body = reinterpret_cast<const uint4 *>(base + (int64_t)head * elem);
+  for (int k = threadIdx.x; k < nvec; k += blockDim.x) {
+    const uint4 w = __ldcs(body + k);
+    const int32_t i0 = head + k * per16;
+    if (DTYPE == HS_LOGITS_F32) {
+      take(best, __uint_as_float(w.x), i0);
+      take(best, __uint_as_float(w.y), i0 + 1);
+      take(best, __uint_as_float(w.z), i0 + 2);
+      take(best, __uint_as_float(w.w), i0 + 3);
+    } else {
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        take(best, __uint_as_float(ws[q] << 16), i0 + 2 * q);
+        take(best, __uint_as_float(ws[q] & 0xFFFF0000u), i0 + 2 * q + 1);
+      }
+    }
+  }
+  for (int i = head + nvec * per16 + threadIdx.x; i < V; i += blockDim.x) take(best, load(i), i);
+
+  best = warp_best(best);
+  __shared__ Best wb[16];
+  if ((threadIdx.x & 31) == 0) wb[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    Best b = (threadIdx.x < (blockDim.x >> 5)) ? wb[threadIdx.x] : Best{-INFINITY, INT32_MAX};
+    b = warp_best(b);
+    if (threadIdx.x == 0) {
+      const int64_t req = row / rows_per_req, i = row % rows_per_req;
+      pred[req * n_step + i] = b.i;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) k_verify_commit(
+    int32_t d, const int32_t *__restrict__ drafts, const int32_t *__restrict__ pred,
+    const uint4 *__restrict__ step_kv, const int32_t *__restrict__ req_ids,
+    int32_t *kv_len, int32_t *accept_len, int32_t *next_token, int32_t max_reqs, int32_t S,
+    int32_t S_tot, int32_t n_step, int32_t max_ctx, int32_t block_size, int32_t hbt_stride,
+    const int32_t *__restrict__ hbt, int64_t pool_rows, uint4 *pool, uint4 *hot,
+    int32_t *token_slot, int32_t *slot_token, int64_t *slot_ts, uint32_t *status, int64_t now) {
+  const int b = blockIdx.x;
+  __shared__ int sm_m, sm_L, sm_ok;
+  __shared__ int32_t chosen[HS_MAX_STEP];
+  __shared__ uint64_t wmin[8];
+  const int32_t req = req_ids ? req_ids[b] : b;
+  if (threadIdx.x == 0) {
+    const int32_t *p = pred + (int64_t)b * n_step;
+    int m = 0;
+    while (m < d && drafts[(int64_t)b * d + m] == p[m]) ++m;
+    accept_len[b] = m;
+    next_token[b] = p[m];
+    int ok = 1;
+    int L = 0;
+    if (req < 0 || req >= max_reqs) {
+      ok = 0;
+      atomicOr(status, HS_STATUS_INDEX);
+    } else {
+      L = kv_len[req];
+      if ((int64_t)L + m + 1 > max_ctx || m + 1 > S) {
+        ok = 0;
+        atomicOr(status, HS_STATUS_CAPACITY);
+      }
+    }
+    sm_m = m; sm_L = L; sm_ok = ok;
+  }
+  __syncthreads();
+  if (!sm_ok) return;
+  const int n = sm_m + 1, L = sm_L;
+  const int64_t sbase = (int64_t)req * S;
+
+  // n rounds of a block-wide minimum over (ts + 1, slot): the LRU order with
+  // no protected slot. Keys of slots already chosen are skipped.
+  for (int k = 0; k < n; ++k) {
+    uint64_t best = ~0ull;
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {
+      bool used = false;
+      for (int q = 0; q < k; ++q) used |= (chosen[q] == s);
+      if (!used) {
+        const uint64_t key = ((uint64_t)(slot_ts[sbase + s] + 1) << 16) | (uint64_t)s;
+        best = key < best ? key : best;
+      }
+    }
+    for (int off = 16; off; off >>= 1) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+      best = o < best ? o : best;
+    }
+    if ((threadIdx.x & 31) == 0) wmin[threadIdx.x >> 5] = best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint64_t m = wmin[0];
+      for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = wmin[w] < m ? wmin[w] : m;
+      chosen[k] = (int32_t)(m & 0xFFFF);
+    }
+    __syncthreads();
+  }
+
+  // map updates (one thread per kept position)
+  const int64_t cbase = (int64_t)req * max_ctx;
+  if (threadIdx.x < n) {
+    const int k = threadIdx.x;
+    const int32_t s = chosen[k], t = L + k;
+    const int32_t old = slot_token[sbase + s];
+    if (old >= 0 && old < max_ctx) token_slot[cbase + old] = -1;
+    slot_token[sbase + s] = t;
+    token_slot[cbase + t] = s;
+    slot_ts[sbase + s] = now;
+  }
+  // row copies: kept step rows -> host pool rows and hot slots
+  const int32_t *hbt_row = hbt + (int64_t)req * hbt_stride;
+  for (int e = threadIdx.x; e < n * HS_ROW_VEC16; e += blockDim.x) {
+    const int k = e / HS_ROW_VEC16, c = e % HS_ROW_VEC16;
+    const int32_t t = L + k;
+    const uint4 v = step_kv[((int64_t)b * (d + 1) + k) * HS_ROW_VEC16 + c];
+    const int32_t hb = hbt_row[t / block_size];
+    const int64_t hr = (int64_t)hb * block_size + t % block_size;
+    if (hb >= 0 && hr < pool_rows) pool[hr * HS_ROW_VEC16 + c] = v;
+    else if (c == 0) atomicOr(status, HS_STATUS_INDEX);
+    hot[((int64_t)req * S_tot + chosen[k]) * HS_ROW_VEC16 + c] = v;
+  }
+  if (threadIdx.x == 0) kv_len[req] = L + n;
+}
+
+}  // namespace
+
+extern "C" int hs_verify_finalize(hs_buffer *buf, const void *logits, int32_t logits_dtype,
+                                  int32_t B, int32_t d, int32_t V, const int32_t *draft_tokens,
+                                  const void *step_kv, const int32_t *req_ids, int32_t *kv_len,
+                                  int32_t *accept_len, int32_t *next_token, hs_stream_t stream) {
+  int rc = hs_check_buffer(buf);
+  if (rc) return rc;
+  if (B < 1 || B > buf->max_reqs || d < 0 || d + 1 > buf->n_step || V < 1)
+    return hs_set_error(HS_ERR_INVALID_ARG, "bad sizes B=%d (1..%d) d=%d (d+1<=%d) V=%d", B,
+                        buf->max_reqs, d, buf->n_step, V);
+  if (logits_dtype != HS_LOGITS_F32 && logits_dtype != HS_LOGITS_BF16)
+    return hs_set_error(HS_ERR_INVALID_ARG, "logits_dtype %d", logits_dtype);
+  if (!logits || (d > 0 && !draft_tokens) || !step_kv || !kv_len || !accept_len || !next_token)
+    return hs_set_error(HS_ERR_INVALID_ARG, "NULL argument");
+  if ((uintptr_t)step_kv & 15)
+    return hs_set_error(HS_ERR_INVALID_ARG, "step_kv must be 16-byte aligned");
+  buf->clock += 1;
+  const int rows = B * (d + 1);
+  if (logits_dtype == HS_LOGITS_F32)
+    k_verify_argmax<HS_LOGITS_F32><<<rows, 512, 0, stream>>>(logits, V, d + 1, buf->n_step,
+                                                             buf->pred);
+  else
+    k_verify_argmax<HS_LOGITS_BF16><<<rows, 512, 0, stream>>>(logits, V, d + 1, buf->n_step,
+                                                              buf->pred);
+  HS_LAUNCH_CHECK("k_verify_argmax");
+  k_verify_commit<<<B, 256, 0, stream>>>(
+      d, draft_tokens, buf->pred, reinterpret_cast<const uint4 *>(step_kv), req_ids, kv_len,
+      accept_len, next_token, buf->max_reqs, buf->S, buf->S_tot, buf->n_step, buf->max_ctx,
+      buf->block_size, buf->hbt_stride, buf->hbt, buf->host_pool_rows,
+      reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(buf->host_pool)),
+      reinterpret_cast<uint4 *>(buf->hot_kv), buf->token_slot, buf->slot_token, buf->slot_ts,
+      buf->status, buf->clock);
+  HS_LAUNCH_CHECK("k_verify_commit");
+  return HS_OK;
+}

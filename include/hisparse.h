@@ -1,0 +1,287 @@
+/*
+ * hisparse.h -- C ABI of libhisparse: the decode-step hot path of HiSparse-style
+ * hierarchical top-k sparse attention with MTP speculative decoding, for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Sources (pages of the hisparse_top_sparse material):
+ *   [MTP]  "hiSparse-MTP" (Notion): section 1 (HiSparseCoordinator holds the
+ *          device buffer, the host pool, LRU slots, token metadata and an async
+ *          stream) and the core state maps (request -> slots, slot -> token
+ *          position, position -> host KV location, logical position -> slot).
+ *   [KVF]  "投机解码的 KV 流转：prefill 阶段 DFlash 也要吃下整个 prompt"
+ *          (shenshijiu.com): sections ④-⑥ and the closing table (greedy verify,
+ *          which positions keep target KV, where the next anchor sits).
+ *   [VLLM] "vllm 分析(十二) HiSparse 下篇" (devpress.csdn.net): sections
+ *          HiSparseCacheHandle.resolve_topk (fully-resident index conversion
+ *          versus swap-in) and "数据 back up" (paged host-row arithmetic).
+ *
+ * Conventions shared by every call
+ *   - Every call returns an int status: HS_OK (0) or a negative HS_ERR_* code.
+ *     Argument errors are detected on the host and returned at once, with
+ *     nothing enqueued; hs_last_error_string() then describes them.
+ *   - Every call that takes a stream is asynchronous on that stream (a
+ *     cudaStream_t; NULL is the legacy default stream) and only enqueues
+ *     kernels. Data errors found on the device (a position beyond a row's
+ *     causal length, a request that needs more positions than it has slots)
+ *     set bits of a device status word: the buffer's, read with
+ *     hs_get_status(), or the caller's word for hs_resolve_topk.
+ *   - Pointers named "device" must be device memory (or memory the device can
+ *     address) of the current CUDA device. The caller owns every tensor: q,
+ *     KV caches, index tables, outputs, logits, the hot KV storage, the pinned
+ *     host pool and the block tables. The library owns only the hs_buffer's
+ *     metadata (slot maps, timestamps, scratch) which hs_buffer_create
+ *     allocates and hs_buffer_destroy frees. No other call allocates.
+ *   - bf16 tensors are raw IEEE bfloat16 (uint16) arrays.
+ *   - Calls on one hs_buffer must be ordered (one stream, or streams joined
+ *     by events): they read and update its slot maps.
+ */
+#ifndef HISPARSE_H_
+#define HISPARSE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st *hs_stream_t;
+
+/* Opaque hot-buffer object. */
+typedef struct hs_buffer hs_buffer;
+
+enum hs_status_code {
+  HS_OK = 0,
+  HS_ERR_INVALID_ARG = -1, /* bad pointer, size, alignment or device        */
+  HS_ERR_CAPACITY = -2,    /* hs_get_status: a request overflowed its slots */
+  HS_ERR_INDEX = -3,       /* hs_get_status: a position was out of range    */
+  HS_ERR_CUDA = -4,        /* a CUDA runtime call or a launch failed        */
+  HS_ERR_TIMEOUT = -5,     /* reserved: a bounded device wait gave up       */
+  HS_ERR_UNSUPPORTED = -6  /* a shape the kernels do not handle             */
+};
+
+/* Bits of the device status word. */
+#define HS_STATUS_INDEX 1u    /* a top-k position >= the row's causal length,
+                                 a negative block-table entry, or a request id
+                                 outside the buffer                          */
+#define HS_STATUS_CAPACITY 2u /* a request needed more than S positions in one
+                                 swap-in, or a commit would pass max_ctx      */
+
+#define HS_LATENT_DIM 576 /* q and latent KV row: 512 value dims + 64 rope */
+#define HS_VALUE_DIM 512  /* attention values are dims 0..511 of a row     */
+
+#define HS_LOGITS_F32 0
+#define HS_LOGITS_BF16 1
+
+/* ------------------------------------------------------------------------ */
+/* Hot buffer ([MTP] section 1 and core state maps; [VLLM] HiSparseHotSpec)  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Description of a hot buffer. Request b owns hot rows
+ *   b * (slots_per_req + step_slots) + s,
+ * where s < slots_per_req are LRU slots and the next step_slots rows hold the
+ * KV of the step's own positions kv_len[b] .. kv_len[b] + step_slots - 1
+ * (anchor + drafts), which the caller writes before hs_swap_in (they are
+ * always hits and never evicted).
+ *
+ *   max_reqs          number of requests the buffer serves (ids 0..max_reqs-1)
+ *   slots_per_req     S, LRU slots per request, 1 .. 8192
+ *   step_slots        rows per request per decode step (1 anchor + d drafts),
+ *                     1 .. 16; a verify with d drafts needs d + 1 <= step_slots
+ *                     (the draft count may not pass this "extra page" space)
+ *   max_ctx           positions per request covered by the maps and by the
+ *                     host block table (committed KV length never passes it)
+ *   block_size        positions per host block (>= 1)
+ *   hbt_stride        int32 entries per row of host_block_table
+ *                     (>= ceil(max_ctx / block_size))
+ *   hot_kv            device bf16 [max_reqs * (S + step_slots)][576]; caller-owned
+ *   host_pool         bf16 [host_pool_rows][576] in page-locked host memory the
+ *                     device can map (cudaHostAlloc / cudaHostRegister), or in
+ *                     device memory; caller-owned
+ *   host_pool_rows    rows of host_pool
+ *   host_block_table  device int32 [max_reqs][hbt_stride]: the host block that
+ *                     holds positions [k*block_size, (k+1)*block_size) of a
+ *                     request; the row of position t is
+ *                     hbt[b][t / block_size] * block_size + t % block_size
+ *                     ([VLLM] 数据 back up, one host page per block)
+ */
+typedef struct hs_buffer_desc {
+  int32_t max_reqs;
+  int32_t slots_per_req;
+  int32_t step_slots;
+  int32_t max_ctx;
+  int32_t block_size;
+  int32_t hbt_stride;
+  void *hot_kv;
+  void *host_pool;
+  int64_t host_pool_rows;
+  const int32_t *host_block_table;
+} hs_buffer_desc;
+
+/* Validates desc and allocates the buffer's metadata on the current device:
+ * token->slot map [max_reqs][max_ctx], slot->token map and timestamps
+ * [max_reqs][S], and per-call scratch; all slots start empty. On success
+ * *out receives the buffer. The call synchronises the device. */
+int hs_buffer_create(const hs_buffer_desc *desc, hs_buffer **out);
+
+/* Frees the metadata (not the caller's tensors). NULL is accepted. */
+int hs_buffer_destroy(hs_buffer *buf);
+
+/* Empties every LRU slot of request req (the state a request has when it is
+ * admitted to the decode batch, [MTP] section 3 collect_ready_reqs). */
+int hs_request_reset(hs_buffer *buf, int32_t req, hs_stream_t stream);
+
+/* Synchronises stream, returns the buffer's device status bits in *out_bits
+ * (HS_STATUS_*) and clears them. */
+int hs_get_status(hs_buffer *buf, hs_stream_t stream, uint32_t *out_bits);
+
+/* Copies the buffer's maps to host memory after synchronising stream, for
+ * tests and debugging: token_slot int32 [max_reqs][max_ctx], slot_token int32
+ * [max_reqs][S], slot_ts int64 [max_reqs][S]; any pointer may be NULL. */
+int hs_buffer_dump(hs_buffer *buf, hs_stream_t stream, int32_t *token_slot,
+                   int32_t *slot_token, int64_t *slot_ts);
+
+/* Number of swap-in and commit calls made so far (the LRU clock). */
+int64_t hs_buffer_clock(const hs_buffer *buf);
+
+/* Text of the last error returned on this thread. */
+const char *hs_last_error_string(void);
+
+/* ------------------------------------------------------------------------ */
+/* a1: fully-resident index conversion ([VLLM] resolve_topk, fully_resident  */
+/*     branch: request of the row + block table + top-k -> physical rows)     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ *   req_id_per_row   device int32 [R]: request (block-table row) of each query row
+ *   row_causal_len   device int32 [R]: positions a row may attend (L_b + i + 1
+ *                    for row i of request b)
+ *   block_table      device int32 [*][bt_stride]: physical block of each
+ *                    logical block of a request
+ *   topk             device int32 [R][K]: logical positions; < 0 is padding
+ *   block_size       positions per logical block
+ *   phys_block_stride rows between consecutive physical blocks of the cache
+ *   out_idx          device int32 [R][K]:
+ *                    block_table[b][t / block_size] * phys_block_stride
+ *                    + t % block_size, or -1 for padding and invalid entries
+ *   out_valid        device int32 [R] or NULL: non-negative entries per row
+ *                    (entries keep their places; no compaction)
+ *   status           device uint32 or NULL: HS_STATUS_INDEX is OR-ed in when
+ *                    t >= row_causal_len or the block-table entry is negative
+ * Requirements: R >= 0, K >= 0, block_size >= 1, phys_block_stride >= 1.
+ * The caller guarantees t / block_size < bt_stride for t < row_causal_len.
+ */
+int hs_resolve_topk(const int32_t *req_id_per_row, const int32_t *row_causal_len,
+                    const int32_t *block_table, int32_t bt_stride,
+                    const int32_t *topk, int32_t R, int32_t K, int32_t block_size,
+                    int32_t phys_block_stride, int32_t *out_idx,
+                    int32_t *out_valid, uint32_t *status, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* a2-a5: swap-in for host-backed KV ([VLLM] resolve_topk -> runtime.swap_in; */
+/*        [MTP] LRU slots and the position <-> slot maps)                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For each query row r (request b = req_id_per_row[r], causal length
+ * n = row_causal_len[r], committed length L = kv_len[b]) and entry t:
+ *   t < 0                 padding                 -> -1
+ *   t >= n                index error (status)    -> -1
+ *   L <= t < n            step position           -> hot row b*(S+step)+S+(t-L)
+ *   t < L                 committed position: made resident, then
+ *                                                 -> hot row b*(S+step)+slot
+ * Residency, per request over all its rows in the call: hits get timestamp
+ * ts := clock (the clock advances by one per call); the distinct missing
+ * positions, in ascending order, take the victim slots -- slots holding no
+ * position needed in this call -- in ascending (ts, slot) order (empty slots
+ * have ts = -1 and come first); the host row of each miss is copied into its
+ * slot. A request needing more than S distinct committed positions gets
+ * HS_STATUS_CAPACITY, its committed entries come out -1 and its maps are left
+ * unchanged.
+ *   kv_len        device int32 [max_reqs]: committed length per request
+ *                 (0 <= kv_len <= max_ctx)
+ *   topk          device int32 [R][K]
+ *   out_slot_idx  device int32 [R][K]: rows of hot_kv, for hs_sparse_attn_decode
+ *   out_valid     device int32 [R] or NULL
+ *   stats         device int64 [2] or NULL: hits and misses of this call are
+ *                 ADDED to stats[0] and stats[1]
+ * Requirements: R >= 0, K >= 0.
+ */
+int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
+               const int32_t *row_causal_len, const int32_t *kv_len,
+               const int32_t *topk, int32_t R, int32_t K, int32_t *out_slot_idx,
+               int32_t *out_valid, int64_t *stats, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* a6: sparse attention over the selected latent rows (the DSA attention that */
+/*     consumes resolve_topk / swap_in indices; MLA latent of 576 dims whose  */
+/*     first 512 dims are the values)                                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For each row r, head h:  s_j = scale * <q[r,h,:], kv[idx[r,j],:]> over 576
+ * dims;  out[r,h,:] = sum_j softmax(s)_j * kv[idx[r,j], 0:512];
+ * lse[r,h] = ln(sum_j exp(s_j)). Entries of idx outside [0, n_kv_rows) are
+ * skipped; repeated entries count each time; a row with no valid entry gives
+ * out = 0 and lse = -inf. bf16 inputs, fp32 accumulation, bf16 output.
+ *   q      device bf16 [R][H][576], 16-byte aligned
+ *   kv     device bf16 [n_kv_rows][576], 16-byte aligned (the paged cache for
+ *          resolve indices, hot_kv for swap-in indices)
+ *   idx    device int32 [R][K]
+ *   out    device bf16 [R][H][512]
+ *   lse    device float [R][H] or NULL
+ * Requirements: R >= 0, 1 <= H <= 1024, K >= 0.
+ */
+int hs_sparse_attn_decode(const void *q, const void *kv, int64_t n_kv_rows,
+                          const int32_t *idx, int32_t R, int32_t H, int32_t K,
+                          float scale, void *out, float *lse, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* a7-a8: greedy verify and commit of the accepted prefix ([KVF] ④-⑥)       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For batch entry b (request req = req_ids ? req_ids[b] : b, L = kv_len[req]):
+ *   pred[i] = argmax_v logits[b][i][v] for i = 0..d (lowest index on ties);
+ *     input 0 is the anchor, input i >= 1 is draft i;
+ *   m = length of the longest prefix with draft_tokens[b][i] == pred[i];
+ *   accept_len[b] = m; next_token[b] = pred[m] (the correction token, or the
+ *     bonus token when all d drafts pass);
+ *   the KV of inputs 0..m (step_kv[b][0..m], positions L..L+m) is committed:
+ *     written to the host pool rows of those positions and placed in LRU
+ *     slots taken in ascending (ts, slot) order with nothing protected;
+ *     kv_len[req] = L + m + 1. The next token has no KV yet.
+ * A request with L + m + 1 > max_ctx gets HS_STATUS_CAPACITY and no commit.
+ *   logits        device [B][d+1][V], fp32 (HS_LOGITS_F32) or bf16
+ *                 (HS_LOGITS_BF16); finite values
+ *   draft_tokens  device int32 [B][d]
+ *   step_kv       device bf16 [B][d+1][576]
+ *   kv_len        device int32 [max_reqs], updated in place
+ *   accept_len, next_token  device int32 [B]
+ *   req_ids       device int32 [B] or NULL (identity)
+ * Requirements: 1 <= B <= max_reqs, 0 <= d, d + 1 <= step_slots, V >= 1.
+ */
+int hs_verify_finalize(hs_buffer *buf, const void *logits, int32_t logits_dtype,
+                       int32_t B, int32_t d, int32_t V,
+                       const int32_t *draft_tokens, const void *step_kv,
+                       const int32_t *req_ids, int32_t *kv_len,
+                       int32_t *accept_len, int32_t *next_token,
+                       hs_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Measurement helper (no counterpart on the pages)                           */
+/* ------------------------------------------------------------------------ */
+
+/* Reads `bytes` (a multiple of 16) from `src` -- e.g. mapped page-locked host
+ * memory -- with 16-byte loads on `blocks` x 256 threads and writes one
+ * checksum word per block to device uint64 sink[blocks]. Used to measure the
+ * host-to-device link bandwidth a zero-copy gather can reach. */
+int hs_read_probe(const void *src, size_t bytes, uint64_t *sink, int32_t blocks,
+                  hs_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HISPARSE_H_ */

@@ -389,11 +389,8 @@ def argmax_lowest(row) -> int:
     """Index of the largest logit, the lowest index among equals (R6)."""
     v = np.asarray(row)
     assert np.all(np.isfinite(v)), "logits must be finite"
-    best = 0
-    for i in range(1, v.shape[0]):
-        if v[i] > v[best]:
-            best = i
-    return best
+    # numpy documents that argmax returns the first occurrence of the maximum
+    return int(np.argmax(v))
 
 
 def greedy_accept(preds, drafts):

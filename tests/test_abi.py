@@ -1,0 +1,42 @@
+"""The C ABI library builds, loads without a GPU, and exports every function
+that include/hisparse.h declares; the binding declares the same names."""
+import os
+import re
+
+import __graft_entry__ as G
+
+HDR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                   "include", "hisparse.h")
+
+
+def _declared():
+    src = open(HDR).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hs_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    G.build()
+    import hisparse_top_sparse_gb300 as hs
+    L = hs.lib()
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in hisparse.h but not exported"
+    assert sorted(hs.EXPORTS) == names
+
+
+def test_argument_errors_return_without_a_gpu():
+    G.build()
+    import ctypes
+    import hisparse_top_sparse_gb300 as hs
+    L = hs.lib()
+    # invalid sizes are rejected on the host before anything touches a device
+    assert L.hs_resolve_topk(None, None, None, 0, None, -1, 4, 64, 64, None, None, None,
+                             None) == hs.HS_ERR_INVALID_ARG
+    assert b"bad sizes" in L.hs_last_error_string()
+    assert L.hs_sparse_attn_decode(None, None, 0, None, 1, 0, 1, ctypes.c_float(1.0), None,
+                                   None, None) == hs.HS_ERR_INVALID_ARG
+    assert L.hs_buffer_create(None, None) == hs.HS_ERR_INVALID_ARG
+    assert L.hs_swap_in(None, None, None, None, None, 0, 0, None, None, None,
+                        None) == hs.HS_ERR_INVALID_ARG

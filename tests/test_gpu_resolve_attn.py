@@ -1,0 +1,134 @@
+"""GPU parity: a1 (fully-resident index conversion) bit-exact, a6 (sparse
+attention) within max abs 1e-2 and per-vector relative 2e-2 of the float64
+oracle, on small ragged cases, special cases and workload 2 at full size."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import hs_oracle as O
+from gpu_util import check_attn, lib, np_
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _bf16(x):
+    return torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("K", [1, 5, 64, 130, 2048])
+def test_resolve_small_and_ragged(K):
+    hs = lib()
+    g = np.random.default_rng(K)
+    B, bs, nblk, R = 5, 16, 12, 9
+    bt = g.permutation(B * nblk).reshape(B, nblk).astype(np.int32)
+    bt[2, 7] = -1                              # an unallocated block
+    req = g.integers(0, B, size=R).astype(np.int32)
+    clen = g.integers(1, nblk * bs + 1, size=R).astype(np.int32)
+    topk = g.integers(-3, nblk * bs, size=(R, K)).astype(np.int32)
+    for stride in (bs, 3 * bs):
+        e_idx, e_valid, e_st = O.resolve_topk(req, clen, bt, topk, bs, stride)
+        out = torch.full((R, K), 7, dtype=torch.int32, device=DEV)
+        valid = torch.full((R,), 7, dtype=torch.int32, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        t = lambda a: torch.as_tensor(a, device=DEV)
+        hs.hs_resolve_topk(t(req), t(clen), t(bt), t(topk), bs, stride, out, valid, st)
+        torch.cuda.synchronize()
+        assert np.array_equal(np_(out), e_idx)
+        assert np.array_equal(np_(valid), e_valid)
+        assert int(st.item()) == e_st
+
+
+def _attn_case(seed, R, H, K, N, sharp=False):
+    g = np.random.default_rng(seed)
+    s = 1.0 if sharp else 1.0 / 24
+    q = _bf16(g.standard_normal((R, H, 576)) * s)
+    kv = _bf16(g.standard_normal((N, 576)) * s)
+    idx = g.integers(0, N, size=(R, K)).astype(np.int32)
+    if K > 3:
+        idx[0, 1] = -1
+        idx[0, 2] = N + 5                       # out of range: skipped
+        idx[min(1, R - 1), 0] = idx[min(1, R - 1), K - 1]   # a duplicate entry
+    idx[R - 1, :] = -1                          # an empty row
+    return q, kv, idx
+
+
+@pytest.mark.parametrize("H,K", [(16, 1), (16, 64), (64, 37), (128, 200), (80, 130),
+                                 (128, 2048), (1, 65)])
+@pytest.mark.parametrize("sharp", [False, True])
+def test_attention_small(H, K, sharp):
+    hs = lib()
+    R, N = 4, 3000
+    q, kv, idx = _attn_case(H * 1000 + K, R, H, K, N, sharp)
+    scale = 1.0 / 24
+    ref, ref_lse = O.sparse_attn_decode(q, kv, idx, scale)
+    out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((R, H), dtype=torch.float32, device=DEV)
+    hs.hs_sparse_attn_decode(q.to(DEV), kv.to(DEV), torch.as_tensor(idx, device=DEV), scale,
+                             out, lse)
+    torch.cuda.synchronize()
+    check_attn(out, ref, lse, ref_lse)
+
+
+def test_attention_single_valid_key_is_exact():
+    hs = lib()
+    g = np.random.default_rng(3)
+    q = _bf16(g.standard_normal((2, 128, 576)))
+    kv = _bf16(g.standard_normal((50, 576)))
+    idx = np.full((2, 96), -1, np.int32)
+    idx[0, 40] = 17
+    idx[1, 95] = 3
+    out = torch.empty((2, 128, 512), dtype=torch.bfloat16, device=DEV)
+    hs.hs_sparse_attn_decode(q.to(DEV), kv.to(DEV), torch.as_tensor(idx, device=DEV), 0.1, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out[0].cpu(), kv[17, :512].expand(128, 512))
+    assert torch.equal(out[1].cpu(), kv[3, :512].expand(128, 512))
+
+
+def test_attention_planted_dominant_key():
+    hs = lib()
+    g = np.random.default_rng(4)
+    H, K, N = 128, 300, 400
+    q = g.standard_normal((1, H, 576)) / 24
+    kv = g.standard_normal((N, 576)) / 24
+    q[0, :, 0] = 1.0
+    kv[:, 0] = 0.0
+    kv[123, 0] = 60.0                           # logit >= 50 above all others (scale 1)
+    idx = g.permutation(N)[:K].astype(np.int32)
+    idx[17] = 123
+    q, kv = _bf16(q), _bf16(kv)
+    out = torch.empty((1, H, 512), dtype=torch.bfloat16, device=DEV)
+    hs.hs_sparse_attn_decode(q.to(DEV), kv.to(DEV), torch.as_tensor(idx[None], device=DEV),
+                             1.0, out)
+    torch.cuda.synchronize()
+    got = out[0].float().cpu()
+    want = kv[123, :512].float().expand(H, 512)
+    ulp = torch.abs(want) * 2.0 ** -7 + 1e-30
+    assert ((got - want).abs() <= ulp).all()
+
+
+def test_workload2_full_size():
+    hs = lib()
+    cfg = W.get_config(2)
+    rc = W.resident_case(cfg, 0, device=DEV)
+    idx = torch.empty_like(rc["topk"])
+    valid = torch.empty_like(rc["req"])
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hs.hs_resolve_topk(rc["req"], rc["clen"], rc["bt"], rc["topk"], cfg.block_size,
+                       cfg.block_size, idx, valid, st)
+    out = torch.empty((cfg.R, cfg.H, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((cfg.R, cfg.H), dtype=torch.float32, device=DEV)
+    hs.hs_sparse_attn_decode(rc["q"], rc["kv"], idx, cfg.scale, out, lse)
+    torch.cuda.synchronize()
+    e_idx, e_valid, e_st = O.resolve_topk(rc["req_np"], rc["clen_np"], rc["bt_np"],
+                                          rc["topk_np"], cfg.block_size, cfg.block_size)
+    assert np.array_equal(np_(idx), e_idx) and np.array_equal(np_(valid), e_valid)
+    assert int(st.item()) == e_st == 0
+    rows = [0, 1, 2, 3, 45, 64, 101, 127]
+    kvc = rc["kv"]
+    outs, lses = O.sparse_attn_decode_rows(
+        rc["q"].cpu(), lambda r: kvc[torch.as_tensor(r, device=DEV)].cpu().double().numpy(),
+        e_idx, cfg.scale, rows)
+    check_attn(out, np.stack([outs[r] for r in rows]), lse, np.stack([lses[r] for r in rows]),
+               rows=rows)

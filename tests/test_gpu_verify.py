@@ -1,0 +1,176 @@
+"""GPU parity of a7-a8 (greedy verify + commit) and of the whole path over
+workloads 1 and 5: accepted lengths, next tokens, kv_len, maps, host-pool
+rows and hot rows match the oracle bit-exactly."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import hs_oracle as O
+from gpu_util import check_attn, lib, np_
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _t(a):
+    return torch.as_tensor(np.ascontiguousarray(a), device=DEV)
+
+
+def _u16(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def test_worked_example_through_the_abi():
+    hs = lib()
+    g = json.load(open(os.path.join(GOLD, "p2_worked_example.json")))
+    V, P, bs, max_ctx, S = g["vocab"], g["prompt_len"], 4, 16, 6
+    for case in g["cases"]:
+        e = case["expected"]
+        pool = torch.zeros((max_ctx, 576), dtype=torch.bfloat16).pin_memory()
+        hot = torch.zeros((S + 4, 576), dtype=torch.bfloat16, device=DEV)
+        hbt = _t(np.arange(max_ctx // bs, dtype=np.int32)[None, :])
+        buf = hs.HsBuffer(1, S, 4, max_ctx, bs, hot, pool, hbt)
+        lg = np.random.default_rng(0).standard_normal((1, 4, V)).astype(np.float32)
+        for i, a in enumerate(case["target_argmax_per_input"]):
+            lg[0, i, a] = lg[0, i].max() + 1.0
+        step_kv = W.bf16_normal((1, 4, 576), 1.0, 0, "p2")
+        kv_len = _t(np.array([P], np.int32))
+        acc = torch.empty(1, dtype=torch.int32, device=DEV)
+        nxt = torch.empty_like(acc)
+        hs.hs_verify_finalize(buf, _t(lg), _t(np.array([g["drafts"]], np.int32)),
+                              step_kv.to(DEV), kv_len, acc, nxt)
+        assert hs.hs_get_status(buf) == 0
+        assert acc.item() == e["accept_len"] and nxt.item() == e["next_token"]
+        assert kv_len.item() == e["kv_len_after"]
+        ts, stok, sts = buf.dump()
+        held = sorted(t for t in stok[0].tolist() if t >= 0)
+        assert held == e["committed_positions"]
+        for t, k in zip(e["committed_positions"], e["committed_step_rows"]):
+            s = int(ts[0, t])
+            assert torch.equal(hot[s].cpu(), step_kv[0, k])
+            assert torch.equal(pool[t], step_kv[0, k])          # identity host block table
+        for t in e["positions_without_kv"]:
+            assert int(ts[0, t]) == -1 and not pool[t].any()
+        buf.close()
+
+
+def test_argmax_ties_and_unaligned_vocab():
+    hs = lib()
+    for V, dt in [(1000, torch.float32), (129, torch.bfloat16), (4099, torch.float32)]:
+        B, d = 3, 2
+        g = np.random.default_rng(V)
+        lg = g.integers(-3, 4, size=(B, d + 1, V)).astype(np.float32)   # many ties
+        drafts = g.integers(0, V, size=(B, d)).astype(np.int32)
+        drafts[0, 0] = int(np.argmax(lg[0, 0]))
+        logits = torch.as_tensor(lg).to(dt)
+        pool = torch.zeros((B * 64, 576), dtype=torch.bfloat16).pin_memory()
+        hot = torch.zeros((B * 8, 576), dtype=torch.bfloat16, device=DEV)
+        hbt = _t(np.arange(B * 4, dtype=np.int32).reshape(B, 4))
+        buf = hs.HsBuffer(B, 5, 3, 64, 16, hot, pool, hbt)
+        ref = O.HotBuffer(B, 5, 3, 64, 16, np_(hbt), pool.clone())
+        skv = W.bf16_normal((B, d + 1, 576), 1.0, V, "skv")
+        kv_len = _t(np.array([10, 20, 30], np.int32))
+        acc = torch.empty(B, dtype=torch.int32, device=DEV)
+        nxt = torch.empty_like(acc)
+        hs.hs_verify_finalize(buf, logits.to(DEV), _t(drafts), skv.to(DEV), kv_len, acc, nxt)
+        e_acc, e_nxt, e_L, e_st = O.verify_finalize(ref, logits, drafts, skv, [10, 20, 30])
+        assert np.array_equal(np_(acc), e_acc) and np.array_equal(np_(nxt), e_nxt)
+        assert np.array_equal(np_(kv_len), e_L) and hs.hs_get_status(buf) == e_st
+        buf.close()
+
+
+def test_workload1_two_steps_end_to_end():
+    """Workload 1: per step, row-waves of swap-in + attention on the hot
+    buffer, then greedy verify + commit; every piece of state is compared
+    with the oracle after every call."""
+    hs = lib()
+    cfg = W.get_config(1)
+    req, ri = W.rows_of(cfg)
+    hb = W.host_backed_case(cfg, device=DEV, extra_positions=cfg.steps * (cfg.d + 1))
+    buf = hs.HsBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hb["hot"],
+                      hb["pool"], hb["hbt"])
+    ref = O.HotBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hb["hbt_np"],
+                      hb["pool"].clone())
+    L = list(cfg.L)
+    kv_len = hb["kv_len"]
+    logits, drafts, _ = W.planted_logits(cfg)
+    for step in range(cfg.steps):
+        skv = W.step_kv(cfg, step, device=DEV)
+        # the step's own KV goes into the step slots (written by the model)
+        for b in range(cfg.B):
+            lo = b * hb["S_tot"] + cfg.S
+            hb["hot"][lo:lo + cfg.d + 1] = skv[b]
+            ref.hot[lo:lo + cfg.d + 1] = _u16(skv[b])
+        topk = W.topk_independent(cfg, step, L, req, ri)
+        clen = W.causal_lengths(L, req, ri)
+        q = W.step_q(cfg, step, device=DEV)
+        for wave in range(cfg.d + 1):
+            rows = np.where(ri == wave)[0]
+            out_idx = torch.empty((len(rows), cfg.K), dtype=torch.int32, device=DEV)
+            hs.hs_swap_in(buf, _t(req[rows]), _t(clen[rows]), kv_len, _t(topk[rows]), out_idx)
+            e_idx, _, e_st, _ = ref.swap_in(req[rows], clen[rows], L, topk[rows])
+            assert np.array_equal(np_(out_idx), e_idx)
+            assert hs.hs_get_status(buf) == e_st == 0
+            qq = q[_t(rows)].contiguous()
+            out = torch.empty((len(rows), cfg.H, 512), dtype=torch.bfloat16, device=DEV)
+            lse = torch.empty((len(rows), cfg.H), dtype=torch.float32, device=DEV)
+            hs.hs_sparse_attn_decode(qq, hb["hot"], out_idx, cfg.scale, out, lse)
+            e_out, e_lse = O.sparse_attn_decode(qq.cpu(), ref.hot, e_idx, cfg.scale)
+            check_attn(out, e_out, lse, e_lse)
+        acc = torch.empty(cfg.B, dtype=torch.int32, device=DEV)
+        nxt = torch.empty_like(acc)
+        hs.hs_verify_finalize(buf, logits.to(DEV), _t(drafts), skv, kv_len, acc, nxt)
+        e_acc, e_nxt, e_L, e_st = O.verify_finalize(ref, logits, drafts, skv.cpu(), L)
+        assert np.array_equal(np_(acc), e_acc) and np.array_equal(np_(nxt), e_nxt)
+        assert np.array_equal(np_(kv_len), e_L) and hs.hs_get_status(buf) == e_st == 0
+        L = [int(x) for x in e_L]
+        ts, stok, sts = buf.dump()
+        for b in range(cfg.B):
+            assert stok[b].tolist() == ref.slot_token[b]
+            assert sts[b].tolist() == ref.slot_ts[b]
+            assert np.array_equal(ts[b].numpy(), ref.token_slot_array(b))
+        assert np.array_equal(_u16(hb["pool"]), ref.host_pool)
+        lru = np.concatenate([np.arange(b * hb["S_tot"], b * hb["S_tot"] + cfg.S)
+                              for b in range(cfg.B)])
+        assert np.array_equal(_u16(hb["hot"])[lru], ref.hot[lru])
+
+
+def test_workload5_verify_finalize():
+    hs = lib()
+    cfg = W.get_config(5)
+    req, ri = W.rows_of(cfg)
+    hb = W.host_backed_case(cfg, device=DEV)
+    buf = hs.HsBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hb["hot"],
+                      hb["pool"], hb["hbt"])
+    ref = O.HotBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hb["hbt_np"],
+                      hb["pool"].clone())
+    # warm state: one swap-in of a uniform 2048-set per request
+    sets = [W.locality_sets(cfg, cfg.L[b], b, 1) for b in range(cfg.B)]
+    topk = W.topk_shared_sets(cfg, sets, 0)
+    clen = W.causal_lengths(cfg.L, req, ri)
+    out_idx = torch.empty((cfg.R, cfg.K), dtype=torch.int32, device=DEV)
+    hs.hs_swap_in(buf, _t(req), _t(clen), hb["kv_len"], _t(topk), out_idx)
+    e_idx, _, _, _ = ref.swap_in(req, clen, cfg.L, topk)
+    assert np.array_equal(np_(out_idx), e_idx)
+    logits, drafts, planted = W.planted_logits(cfg, device=DEV)
+    skv = W.step_kv(cfg, 0, device=DEV)
+    acc = torch.empty(cfg.B, dtype=torch.int32, device=DEV)
+    nxt = torch.empty_like(acc)
+    hs.hs_verify_finalize(buf, logits, _t(drafts), skv, hb["kv_len"], acc, nxt)
+    e_acc, e_nxt, e_L, e_st = O.verify_finalize(ref, logits.cpu(), drafts, skv.cpu(), cfg.L)
+    assert np.array_equal(np_(acc), e_acc) and np.array_equal(np_(nxt), e_nxt)
+    assert np.array_equal(np_(hb["kv_len"]), e_L) and hs.hs_get_status(buf) == e_st == 0
+    # acceptance follows the planting: accepted prefix never passes an unplanted draft
+    for b in range(cfg.B):
+        m = int(e_acc[b])
+        assert planted[b, :m].all() and (m == cfg.d or not planted[b, m])
+    ts, stok, sts = buf.dump()
+    for b in range(0, cfg.B, 17):
+        assert stok[b].tolist() == ref.slot_token[b]
+        assert sts[b].tolist() == ref.slot_ts[b]
+    assert np.array_equal(_u16(hb["pool"]), ref.host_pool)

@@ -257,3 +257,73 @@ def planted_logits(cfg: Config, device="cpu", p_plant: float = 0.7):
                         break
             drafts[b, i] = tok
     return logits, drafts, planted
+
+
+# ------------------------------------------------------------ placement --
+# Tensors of a workload on a device. These helpers only draw and place
+# inputs; the path's arithmetic lives in the library and in the oracle.
+
+def _i32(x, device):
+    return torch.as_tensor(np.ascontiguousarray(x), dtype=torch.int32).to(device)
+
+
+def blocks_needed(n_positions: int, block_size: int) -> int:
+    return (int(n_positions) + block_size - 1) // block_size
+
+
+def resident_case(cfg: Config, step: int = 0, device="cuda") -> dict:
+    """Fully-resident workload: a paged latent cache covering every request's
+    positions 0 .. L_b + d (a shuffled physical block table), q, and top-k."""
+    req, ri = rows_of(cfg)
+    clen = causal_lengths(cfg.L, req, ri)
+    nblk = [blocks_needed(L + cfg.d + 1, cfg.block_size) for L in cfg.L]
+    bt, total = shuffled_block_table(cfg.seed, "bt", nblk)
+    kv = bf16_normal((total * cfg.block_size, LATENT), KV_SCALE, cfg.seed, "kvcache",
+                     device=device)
+    q = bf16_normal((cfg.R, cfg.H, LATENT), KV_SCALE, cfg.seed, "q", step, device=device)
+    topk = topk_independent(cfg, step, cfg.L, req, ri)
+    return dict(req=_i32(req, device), clen=_i32(clen, device), bt=_i32(bt, device),
+                topk=_i32(topk, device), q=q, kv=kv, topk_np=topk, req_np=req,
+                clen_np=clen, bt_np=bt)
+
+
+def host_pool_tensor(rows: int, seed: int, device="cuda", pin=True) -> torch.Tensor:
+    """A [rows][576] bf16 pool ~ N(0,1)/24 in page-locked host memory (drawn on
+    ``device`` in chunks and copied down)."""
+    pool = torch.empty((rows, LATENT), dtype=torch.bfloat16, pin_memory=pin)
+    chunk = 1 << 19
+    for c, start in enumerate(range(0, rows, chunk)):
+        stop = min(rows, start + chunk)
+        part = bf16_normal((stop - start, LATENT), KV_SCALE, seed, "hostpool", c,
+                           device=device, chunk_rows=chunk)
+        pool[start:stop].copy_(part)
+    return pool
+
+
+def host_backed_case(cfg: Config, device="cuda", extra_positions: int = 0) -> dict:
+    """Host-backed workload: a paged page-locked host pool covering each
+    request's positions 0 .. max_ctx - 1 (a shuffled host block table), an
+    empty device hot buffer of B * (S + d + 1) rows, and kv_len = L."""
+    bs = cfg.block_size
+    max_ctx = max(cfg.L) + (cfg.d + 1) + extra_positions
+    nblk = [blocks_needed(min(max_ctx, L + cfg.d + 1 + extra_positions), bs) for L in cfg.L]
+    hbt, total = shuffled_block_table(cfg.seed, "hbt", nblk)
+    width = blocks_needed(max_ctx, bs)
+    if hbt.shape[1] < width:
+        hbt = np.concatenate([hbt, np.full((cfg.B, width - hbt.shape[1]), -1, np.int32)], 1)
+    pool = host_pool_tensor(total * bs, cfg.seed, device=device,
+                            pin=torch.cuda.is_available())
+    S_tot = cfg.S + cfg.d + 1
+    hot = torch.zeros((cfg.B * S_tot, LATENT), dtype=torch.bfloat16, device=device)
+    return dict(max_ctx=max_ctx, hbt=_i32(hbt, device), hbt_np=hbt, pool=pool, hot=hot,
+                kv_len=_i32(np.asarray(cfg.L), device), S_tot=S_tot)
+
+
+def step_kv(cfg: Config, step: int, device="cuda") -> torch.Tensor:
+    """Fresh KV of each request's step positions L .. L + d (anchor + drafts)."""
+    return bf16_normal((cfg.B, cfg.d + 1, LATENT), KV_SCALE, cfg.seed, "stepkv", step,
+                       device=device)
+
+
+def step_q(cfg: Config, step: int, device="cuda") -> torch.Tensor:
+    return bf16_normal((cfg.R, cfg.H, LATENT), KV_SCALE, cfg.seed, "q", step, device=device)
