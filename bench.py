@@ -68,7 +68,7 @@ def _attn_bytes(valid_counts: np.ndarray, H: int, K: int) -> int:
 
 
 class Clocks:
-    """nvidia-smi samples during the timed region."""
+    """nvidia-smi samples (written to a file every 100 ms) while active."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -77,32 +77,38 @@ class Clocks:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
+        self.path = os.path.join("/tmp", f"hs_bench_clocks_{os.getpid()}.csv")
+        self.lines = []
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
         return self
 
     def __exit__(self, *a):
-        self.lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+                self.proc.wait()
+            try:
+                with open(self.path) as f:
+                    self.lines = [ln for ln in f if ln.strip()]
+                os.remove(self.path)
+            except OSError:
+                self.lines = []
 
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
+        for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -181,20 +187,32 @@ def run_ours(args):
             dist.barrier()
 
     step_ms, attn_ms = [], []
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
     with Clocks(local) as clk:
-        for _ in range(args.steps):
+        # soak: the same step, untimed, for about a second so the clock sampler
+        # sees the GPU under this load before and during the timed steps
+        t_end = time.perf_counter() + args.soak_s
+        while time.perf_counter() < t_end:
             flush.fill_(1)
-            s0.record(stream)
             step()
-            s1.record(stream)
-            s1.synchronize()
-            step_ms.append(s0.elapsed_time(s1))
-            attn_ms.append(ev_a0.elapsed_time(ev_a1))
-    torch.cuda.synchronize()
-    barrier()
+            torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        for e in evs:
+            flush.fill_(1)
+            e[0].record(stream)
+            hs.hs_resolve_topk(rc["req"], rc["clen"], rc["bt"], rc["topk"], cfg.block_size,
+                               cfg.block_size, idx, valid)
+            e[1].record(stream)
+            hs.hs_sparse_attn_decode(rc["q"], rc["kv"], idx, cfg.scale, out, lse)
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    for e in evs:
+        step_ms.append(e[0].elapsed_time(e[2]))
+        attn_ms.append(e[1].elapsed_time(e[2]))
     t_step = sum(step_ms) / len(step_ms)
     if ws > 1:
         import torch.distributed as dist
@@ -231,6 +249,7 @@ def run_ours(args):
                        "value_dim": 512, "block_size": cfg.block_size,
                        "step": "hs_resolve_topk + hs_sparse_attn_decode",
                        "l2": "flushed before every timed step (256 MiB write)",
+                       "clocks_window": "a 1 s untimed soak of the same step, then the timed steps",
                        "parallelism": f"replicas x{ws}, requests sharded, no collective"},
             "gpu_launches": 2 * args.steps,
             "roofline": roofline, "e2e": e2e, "clocks": clk.summary(),
@@ -366,15 +385,14 @@ def cpu_baseline(cfg, rc, budget_s: float = 12.0):
     topk, req, clen, bt = rc["topk_np"], rc["req_np"], rc["clen_np"], rc["bt_np"]
     rows_done = 0
     t0 = time.perf_counter()
-    r = 0
-    while time.perf_counter() - t0 < budget_s and r < cfg.R:
+    while time.perf_counter() - t0 < budget_s:
+        r = rows_done % cfg.R
         idx, _, _ = O.resolve_topk(req[r:r + 1], clen[r:r + 1], bt, topk[r:r + 1],
                                    cfg.block_size, cfg.block_size)
         rows = torch.as_tensor(idx[0][idx[0] >= 0], device=kv.device)
         kv_rows = kv[rows].cpu()
         O.sparse_attn_decode(q[r:r + 1], kv_rows, np.arange(len(rows))[None, :], cfg.scale)
         rows_done += 1
-        r += 1
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"value": round(rows_done / dt, 3), "unit": "query-rows/s", "cores": cores,
@@ -441,6 +459,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-swap", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=1.0)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
