@@ -36,6 +36,7 @@ EXPORTS = (
     "hs_buffer_create", "hs_buffer_destroy", "hs_request_reset", "hs_get_status",
     "hs_buffer_dump", "hs_buffer_clock", "hs_last_error_string", "hs_resolve_topk",
     "hs_swap_in", "hs_sparse_attn_decode", "hs_verify_finalize", "hs_read_probe",
+    "hs_verify_accept_noalloc",
 )
 
 
@@ -84,6 +85,7 @@ def lib() -> ctypes.CDLL:
                                            _P, _P, _P]),
             "hs_verify_finalize": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
             "hs_read_probe": (_I, [_P, ctypes.c_size_t, _P, _I, _P]),
+            "hs_verify_accept_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -261,6 +263,26 @@ def hs_verify_finalize(buf: HsBuffer, logits, draft_tokens, step_kv, kv_len, acc
         _ptr(accept_len, "accept_len", torch.int32, (B,)),
         _ptr(next_token, "next_token", torch.int32, (B,)),
         _stream(stream)), "hs_verify_finalize")
+
+
+def hs_verify_accept_noalloc(logits, draft_tokens, accept_len, next_token,
+                             stream=None) -> None:
+    """Greedy acceptance without any allocation (static scratch in the
+    library); see include/hisparse.h."""
+    B, d1, V = logits.shape
+    d = d1 - 1
+    if logits.dtype == torch.float32:
+        dt = HS_LOGITS_F32
+    elif logits.dtype == torch.bfloat16:
+        dt = HS_LOGITS_BF16
+    else:
+        raise TypeError("logits must be float32 or bfloat16")
+    _check(lib().hs_verify_accept_noalloc(
+        _ptr(logits, "logits"), dt, B, d, V,
+        _ptr(draft_tokens, "draft_tokens", torch.int32, (B, d), allow_none=(d == 0)),
+        _ptr(accept_len, "accept_len", torch.int32, (B,)),
+        _ptr(next_token, "next_token", torch.int32, (B,)),
+        _stream(stream)), "hs_verify_accept_noalloc")
 
 
 def hs_read_probe(src: torch.Tensor, sink: torch.Tensor, blocks: int, stream=None) -> None:

@@ -1,0 +1,157 @@
+// hs_verify_accept_noalloc: greedy acceptance (the argmax and accepted-prefix
+// half of hs_verify_finalize) for callers that cannot allocate device memory.
+//
+// Who needs it: code that runs where cudaMalloc is not available to it -- a
+// plugin inside a host framework whose allocator owns all device memory, or a
+// serving loop whose latency budget forbids the implicit synchronisation an
+// allocation can cause. Such a caller can still hand over its own logits,
+// drafts and output arrays, but cannot create an hs_buffer (that allocates).
+//
+// The per-row argmax needs scratch (one int32 per verified row). Here it lives
+// in a file-scope __device__ array of fixed size, which every GPU that loads
+// this library holds until the process exits. No call below allocates.
+
+#include <mutex>
+
+#include "hs_internal.cuh"
+
+#define HS_NOALLOC_MAX_ROWS 65536   // B * (d + 1) limit: 256 KiB of int32 scratch
+#define HS_NOALLOC_MAX_DEVICES 64
+
+static __device__ __align__(256) int32_t g_accept_scratch[HS_NOALLOC_MAX_ROWS];
+
+namespace {
+
+// Device address of g_accept_scratch on each device, looked up once. In host
+// code the array's name is only a host-side stand-in; kernels must receive the
+// address that cudaGetSymbolAddress returns for the current device.
+int32_t *g_scratch_dev[HS_NOALLOC_MAX_DEVICES] = {nullptr};
+std::mutex g_scratch_mu;
+
+int scratch_for_current_device(int32_t **out) {
+  int dev = -1;
+  HS_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= HS_NOALLOC_MAX_DEVICES)
+    return hs_set_error(HS_ERR_UNSUPPORTED, "device %d beyond %d", dev, HS_NOALLOC_MAX_DEVICES);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_dev[dev]) {
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_accept_scratch);
+    if (e != cudaSuccess || !p)
+      return hs_set_error(HS_ERR_CUDA, "cudaGetSymbolAddress(g_accept_scratch) failed: %s",
+                          cudaGetErrorString(e));
+    g_scratch_dev[dev] = static_cast<int32_t *>(p);
+  }
+  *out = g_scratch_dev[dev];
+  return HS_OK;
+}
+
+struct Best {
+  float v;
+  int32_t i;
+};
+
+__device__ __forceinline__ void take(Best &b, float v, int32_t i) {
+  if (v > b.v || (v == b.v && i < b.i)) { b.v = v; b.i = i; }
+}
+
+__device__ __forceinline__ Best warp_best(Best b) {
+  for (int off = 16; off; off >>= 1) {
+    const float v = __shfl_xor_sync(0xffffffffu, b.v, off);
+    const int32_t i = __shfl_xor_sync(0xffffffffu, b.i, off);
+    take(b, v, i);
+  }
+  return b;
+}
+
+// Block per logits row: argmax with ties to the lowest index, written to
+// pred[row] (every row of the call is written, so nothing needs clearing).
+template <int DTYPE>
+__global__ void __launch_bounds__(512) k_accept_argmax(const void *__restrict__ logits,
+                                                       int32_t V, int32_t *__restrict__ pred) {
+  const int64_t row = blockIdx.x;
+  const int64_t elem = (DTYPE == HS_LOGITS_F32) ? 4 : 2;
+  const char *base = reinterpret_cast<const char *>(logits) + row * (int64_t)V * elem;
+  auto load = [&](int32_t i) -> float {
+    if (DTYPE == HS_LOGITS_F32) return reinterpret_cast<const float *>(base)[i];
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[i]);
+  };
+  Best best{-INFINITY, INT32_MAX};
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(base);
+  const int per16 = 16 / (int)elem;
+  int head = (int)(((16 - (addr & 15)) & 15) / elem);
+  if ((addr & (elem - 1)) != 0) head = V;
+  if (head > V) head = V;
+  const int nvec = (V - head) / per16;
+  for (int i = threadIdx.x; i < head; i += blockDim.x) take(best, load(i), i);
+  const uint4 *body = reinterpret_cast<const uint4 *>(base + (int64_t)head * elem);
+  for (int k = threadIdx.x; k < nvec; k += blockDim.x) {
+    const uint4 w = __ldcs(body + k);
+    const int32_t i0 = head + k * per16;
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (DTYPE == HS_LOGITS_F32) {
+        take(best, __uint_as_float(ws[q]), i0 + q);
+      } else {
+        take(best, __uint_as_float(ws[q] << 16), i0 + 2 * q);
+        take(best, __uint_as_float(ws[q] & 0xFFFF0000u), i0 + 2 * q + 1);
+      }
+    }
+  }
+  for (int i = head + nvec * per16 + threadIdx.x; i < V; i += blockDim.x) take(best, load(i), i);
+  best = warp_best(best);
+  __shared__ Best wb[16];
+  if ((threadIdx.x & 31) == 0) wb[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    Best b = (threadIdx.x < (blockDim.x >> 5)) ? wb[threadIdx.x] : Best{-INFINITY, INT32_MAX};
+    b = warp_best(b);
+    if (threadIdx.x == 0) pred[row] = b.i;
+  }
+}
+
+// Thread per request: longest agreeing prefix and the next token.
+__global__ void k_accept_prefix(const int32_t *__restrict__ pred,
+                                const int32_t *__restrict__ drafts, int32_t B, int32_t d,
+                                int32_t *__restrict__ accept_len,
+                                int32_t *__restrict__ next_token) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int32_t *p = pred + (int64_t)b * (d + 1);
+  int m = 0;
+  while (m < d && drafts[(int64_t)b * d + m] == p[m]) ++m;
+  accept_len[b] = m;
+  next_token[b] = p[m];
+}
+
+}  // namespace
+
+extern "C" int hs_verify_accept_noalloc(const void *logits, int32_t logits_dtype, int32_t B,
+                                        int32_t d, int32_t V, const int32_t *draft_tokens,
+                                        int32_t *accept_len, int32_t *next_token,
+                                        hs_stream_t stream) {
+  if (B < 1 || d < 0 || V < 1)
+    return hs_set_error(HS_ERR_INVALID_ARG, "bad sizes B=%d d=%d V=%d", B, d, V);
+  if ((int64_t)B * (d + 1) > HS_NOALLOC_MAX_ROWS)
+    return hs_set_error(HS_ERR_INVALID_ARG,
+                        "B*(d+1) = %lld rows exceeds the static scratch of %d rows",
+                        (long long)B * (d + 1), HS_NOALLOC_MAX_ROWS);
+  if (logits_dtype != HS_LOGITS_F32 && logits_dtype != HS_LOGITS_BF16)
+    return hs_set_error(HS_ERR_INVALID_ARG, "logits_dtype %d", logits_dtype);
+  if (!logits || (d > 0 && !draft_tokens) || !accept_len || !next_token)
+    return hs_set_error(HS_ERR_INVALID_ARG, "NULL argument");
+  int32_t *pred = nullptr;
+  int rc = scratch_for_current_device(&pred);
+  if (rc) return rc;
+  const int rows = B * (d + 1);
+  if (logits_dtype == HS_LOGITS_F32)
+    k_accept_argmax<HS_LOGITS_F32><<<rows, 512, 0, stream>>>(logits, V, pred);
+  else
+    k_accept_argmax<HS_LOGITS_BF16><<<rows, 512, 0, stream>>>(logits, V, pred);
+  HS_LAUNCH_CHECK("k_accept_argmax");
+  k_accept_prefix<<<(B + 127) / 128, 128, 0, stream>>>(pred, draft_tokens, B, d, accept_len,
+                                                       next_token);
+  HS_LAUNCH_CHECK("k_accept_prefix");
+  return HS_OK;
+}
