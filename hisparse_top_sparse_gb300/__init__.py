@@ -27,6 +27,7 @@ HS_ERR_TIMEOUT = -5
 HS_ERR_UNSUPPORTED = -6
 HS_STATUS_INDEX = 1
 HS_STATUS_CAPACITY = 2
+HS_STATUS_TIMEOUT = 4
 HS_LOGITS_F32 = 0
 HS_LOGITS_BF16 = 1
 LATENT_DIM = 576
@@ -82,7 +83,7 @@ def lib() -> ctypes.CDLL:
             "hs_resolve_topk": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
             "hs_swap_in": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P]),
             "hs_sparse_attn_decode": (_I, [_P, _P, _I64, _P, _I, _I, _I, ctypes.c_float,
-                                           _P, _P, _P]),
+                                           _P, _P, _P, _P]),
             "hs_verify_finalize": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
             "hs_read_probe": (_I, [_P, ctypes.c_size_t, _P, _I, _P]),
             "hs_verify_accept_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
@@ -231,7 +232,8 @@ def hs_swap_in(buf: HsBuffer, req_id_per_row, row_causal_len, kv_len, topk, out_
         _stream(stream)), "hs_swap_in")
 
 
-def hs_sparse_attn_decode(q, kv, idx, scale: float, out, lse=None, stream=None) -> None:
+def hs_sparse_attn_decode(q, kv, idx, scale: float, out, lse=None, status=None,
+                          stream=None) -> None:
     R, H, D = q.shape
     if D != LATENT_DIM:
         raise ValueError("q must be [R][H][576]")
@@ -241,6 +243,7 @@ def hs_sparse_attn_decode(q, kv, idx, scale: float, out, lse=None, stream=None) 
         _ptr(idx, "idx", torch.int32, (R, K)), R, H, K, float(scale),
         _ptr(out, "out", torch.bfloat16, (R, H, VALUE_DIM)),
         _ptr(lse, "lse", torch.float32, (R, H), allow_none=True),
+        _ptr(status, "status", torch.int32, (1,), allow_none=True),
         _stream(stream)), "hs_sparse_attn_decode")
 
 

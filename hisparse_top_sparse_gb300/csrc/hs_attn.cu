@@ -1,24 +1,32 @@
-// a6: sparse attention over the selected latent KV rows (decode, one query
-// row per (request, input), H heads sharing one 576-dim latent KV row per
-// selected position; values are its first 512 dims).
+// a6: sparse attention over the selected latent KV rows (decode: one query row
+// per (request, input), H heads sharing one 576-dim latent KV row per selected
+// position; values are its first 512 dims).
 //
 // The consumer of resolve_topk / swap_in on the pages is the DSA attention
 // backend ("hiSparse-MTP", section 1: init_attention_backend hands the
 // coordinator to the DSA backend; "vllm 分析(十二) HiSparse 下篇",
 // resolve_topk returns (attention cache, indices[, valid counts])).
 //
-// Kernel k_attn_mma: one CTA per (query row, group of 64 heads), 8 warps.
-//   * Q of the 64 heads (64 x 576 bf16) is staged once in shared memory.
-//   * The row's selected KV rows are gathered 64 at a time with 16-byte
-//     cp.async into a double-buffered tile (64 x 1152 B); invalid or padding
-//     entries are zero-filled and masked to -inf in the scores.
-//   * S = Q K^T on bf16 mma.sync tensor-core instructions (fp32 accumulate):
-//     warp w computes heads 16*(w%4).. x keys 32*(w/4)..; online softmax in
-//     the log2 domain with the running max shared through shared memory.
-//   * O += P V: P goes to shared memory as bf16; warp w owns value dims
-//     64*w .. 64*w+63 of all 64 heads (128 fp32 accumulators per thread).
-//   * Shared-memory rows are XOR-swizzled in 16-byte chunks so that every
-//     ldmatrix phase touches 8 distinct bank groups.
+// k_attn_umma -- 5th-generation tensor cores (tcgen05) with TMEM accumulators.
+//
+// Per row, Q (128 heads x 576 bf16 = 147 KB) and O (128 x 512 fp32 = 256 KB,
+// all of TMEM) do not fit one SM together with KV tiles. Each row is therefore
+// served by two CTAs, c = 0 / 1, each owning value dims [256c, 256c + 256):
+//   * O_c (128 x 256 fp32) lives in TMEM columns [0, 256);
+//   * Q dims 0..383 live in TMEM columns [256, 448) as the MMA's A operand;
+//     Q dims 384..575 live in shared memory (3 x 16 KB, 128-byte swizzle);
+//   * S = Q K^T (128 x 32 fp32, all 576 dims -- both CTAs compute it) is
+//     double-buffered in TMEM columns [448, 512);
+//   * KV rows are gathered 32 at a time by 16-byte cp.async into a 4-stage
+//     ring of swizzled tiles (36 KB each): the tile is the K-major B operand
+//     of Q K^T and, read MN-major, the B operand of P V;
+//   * P (bf16) goes through shared memory (double-buffered) as P V's A.
+// Warp roles (288 threads): warps 0-3 softmax + epilogue (thread = head =
+// TMEM lane), warps 4-7 gather producers, warp 8 lane 0 issues the MMAs.
+// Online softmax in the log2 domain with lazy rescaling: O is rescaled (in
+// TMEM) only when a row's running max grows by more than 2^8.
+// Every mbarrier wait is bounded; a wait that gives up sets HS_STATUS_TIMEOUT
+// in the caller's status word and the CTA winds down.
 
 #include <math.h>
 
@@ -28,58 +36,155 @@ namespace {
 
 constexpr int D = HS_LATENT_DIM;
 constexpr int DV = HS_VALUE_DIM;
-constexpr int HG = 64;                 // heads per CTA
-constexpr int NT = 64;                 // keys per tile
-constexpr int ROWB = D * 2;            // 1152 bytes per latent row
-constexpr int NCH = ROWB / 16;         // 72 chunks of 16 bytes
-constexpr int THREADS = 256;
+constexpr int HG = 128;                   // heads per CTA (MMA M)
+constexpr int NK = 32;                    // keys per tile (MMA N of Q K^T)
+constexpr int STAGES = 4;
+constexpr int LAG = 2;                    // producer: cp.async groups kept in flight
+constexpr int ROWB = D * 2;               // 1152
+constexpr int NCH = ROWB / 16;            // 72 chunks of 16 B per latent row
+constexpr int QT_DIMS = 384;              // Q dims held in TMEM
+constexpr int QS_BLOCKS = (D - QT_DIMS) / 64;   // 3 swizzle blocks of Q in SMEM
+constexpr int KV_BLOCKS = D / 64;         // 9 swizzle blocks per KV tile
+constexpr int THREADS = 288;
+constexpr int NPROD = 128;
 
-constexpr int SQ_OFF = 0;
-constexpr int SKV_OFF = SQ_OFF + HG * ROWB;          // two tiles
-constexpr int SP_OFF = SKV_OFF + 2 * NT * ROWB;      // P tile, 64 x 64 bf16
-constexpr int SMAX_OFF = SP_OFF + HG * NT * 2;       // [2][64] float
-constexpr int SSUM_OFF = SMAX_OFF + 2 * HG * 4;      // [2][64] float
-constexpr int SALPHA_OFF = SSUM_OFF + 2 * HG * 4;    // [64] float
-constexpr int SVALID_OFF = SALPHA_OFF + HG * 4;      // [2][64] int
-constexpr int SMEM_BYTES = SVALID_OFF + 2 * NT * 4;  // 231,168
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+// shared memory (offsets from a 1024-byte aligned base)
+constexpr int QS_OFF = 0;
+constexpr int QS_BYTES = QS_BLOCKS * HG * 128;         // 49152
+constexpr int KV_OFF = QS_OFF + QS_BYTES;
+constexpr int KV_BLOCK_BYTES = NK * 128;               // 4096
+constexpr int KV_STAGE_BYTES = KV_BLOCKS * KV_BLOCK_BYTES;   // 36864
+constexpr int P_OFF = KV_OFF + STAGES * KV_STAGE_BYTES;
+constexpr int P_BYTES = HG * 128;                      // 16384 (keys 0..31 used)
+constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
+constexpr int SMEM_USED = BAR_OFF + 256;
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;           // slack for the 1 KB alignment
+static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return (uint32_t)((chunk & ~7) | ((chunk ^ row) & 7));
+// TMEM columns
+constexpr uint32_t COL_O = 0, COL_Q = 256, COL_S = 448;
+
+// barriers (8-byte words at BAR_OFF)
+enum { B_FULL = 0, B_EMPTY = B_FULL + STAGES, B_SFULL = B_EMPTY + STAGES, B_SFREE = B_SFULL + 2,
+       B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2, B_OFULL = B_PVDONE + 2, B_COUNT = B_OFULL + 1 };
+static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
+
+constexpr int WAIT_LIMIT = 1 << 24;
+
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
+  return row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  // shared-memory matrix descriptor, 128-byte swizzle, descriptor version 1
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
+  // kind::f16 instruction descriptor: D fp32, A and B bf16, A K-major
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+constexpr uint32_t IDESC_QK = idesc_bf16(128, NK, 0);
+constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, 1);
+
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void bar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+// Bounded wait for the phase of the given parity: gives up (false) after
+// about 2^31 SM cycles (~1 s) or WAIT_LIMIT polls, whichever comes first.
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  for (int i = 0; i < WAIT_LIMIT; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > (1ll << 31)) break;
+  }
+  return false;
+}
+
+// The same wait taken by a whole warp, with one verdict for every lane (the
+// warp then issues warp-collective tcgen05 loads and stores).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, bar_wait(bar, parity));
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-  const int sz = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz)
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+#define TMEM_LD32(taddr, r)                                                                    \
+  asm volatile(                                                                                \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13," \
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"    \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),   \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),            \
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),         \
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),         \
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),         \
+        "=r"(r[31])                                                                            \
+      : "r"(taddr))
+#define TMEM_ST32(taddr, r)                                                                    \
+  asm volatile(                                                                                \
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12," \
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"  \
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),         \
+        "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),       \
+        "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),   \
+        "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),   \
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]))
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1,
-                                          uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16(float *c, uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -88,217 +193,290 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-    k_attn_mma(const char *__restrict__ q, const char *__restrict__ kv, int64_t n_kv,
-               const int32_t *__restrict__ idx, int32_t H, int32_t K, float scale_log2,
-               __nv_bfloat16 *__restrict__ out, float *__restrict__ lse) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
-  const uint32_t sQ = sbase + SQ_OFF;
-  const uint32_t sKV = sbase + SKV_OFF;
-  const uint32_t sP = sbase + SP_OFF;
-  float *sMax = reinterpret_cast<float *>(smem + SMAX_OFF);
-  float *sSum = reinterpret_cast<float *>(smem + SSUM_OFF);
-  float *sAlpha = reinterpret_cast<float *>(smem + SALPHA_OFF);
-  int *sValid = reinterpret_cast<int *>(smem + SVALID_OFF);
+    k_attn_umma(const char *__restrict__ q, const char *__restrict__ kv, int64_t n_kv,
+                const int32_t *__restrict__ idx, int32_t H, int32_t K, float scale_log2,
+                __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, uint32_t *status) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *sm =
+      reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(sm);
+  const uint32_t bars = sbase + BAR_OFF;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + BAR_OFF + B_COUNT * 8);
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, qd = lane & 3;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_hg = (H + HG - 1) / HG;
-  const int r = blockIdx.x / n_hg;           // head groups of a row are adjacent,
-  const int h0 = (blockIdx.x % n_hg) * HG;   // so the row's KV is read once from HBM
-  const int mt = warp & 3, nh = warp >> 2;
-  const int ntiles = (K + NT - 1) / NT;
+  const int c = blockIdx.x & 1;                     // value half
+  const int rg = blockIdx.x >> 1;
+  const int r = rg / n_hg;
+  const int h0 = (rg % n_hg) * HG;
+  const int T = (K + NK - 1) / NK;
   const int32_t *idx_row = idx + (int64_t)r * K;
 
-  // Q of this head group (rows beyond H are zero)
-  for (int i = tid; i < HG * NCH; i += THREADS) {
-    const int hr = i / NCH, c = i % NCH;
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      bar_init(bar(B_FULL + s), NPROD);
+      bar_init(bar(B_EMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      bar_init(bar(B_SFULL + b), 1);
+      bar_init(bar(B_SFREE + b), 4);
+      bar_init(bar(B_PFULL + b), 4);
+      bar_init(bar(B_PVDONE + b), 1);
+    }
+    bar_init(bar(B_OFULL), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(
+        (uint32_t)__cvta_generic_to_shared(tmem_slot)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+
+  // Q dims 384..575 -> SMEM (three 64-dim swizzle blocks), all threads
+  for (int i = tid; i < HG * QS_BLOCKS * 8; i += THREADS) {
+    const int hr = i / (QS_BLOCKS * 8), rem = i % (QS_BLOCKS * 8);
+    const int j = rem / 8, cc = rem % 8;
     const int h = h0 + hr;
     const bool v = h < H;
-    const char *src = q + (((int64_t)r * H + (v ? h : 0)) * ROWB) + c * 16;
-    cp_async16(sQ + hr * ROWB + swz(hr, c) * 16, src, v);
+    const char *src = v ? q + ((int64_t)r * H + h) * ROWB + (QT_DIMS + 64 * j) * 2 + cc * 16 : q;
+    cp_async16(sbase + QS_OFF + j * (HG * 128) + sw128(hr, cc), src, v);
   }
-  auto issue_tile = [&](int t, int st) {
-    const uint32_t dst0 = sKV + st * NT * ROWB;
-    for (int i = tid; i < NT * NCH; i += THREADS) {
-      const int kr = i / NCH, c = i % NCH;
-      const int j = t * NT + kr;
-      const int32_t id = (j < K) ? idx_row[j] : -1;
-      const bool v = id >= 0 && id < n_kv;
-      if (c == 0) sValid[st * NT + kr] = v;
-      const char *src = v ? kv + (int64_t)id * ROWB + c * 16 : q;
-      cp_async16(dst0 + kr * ROWB + swz(kr, c) * 16, src, v);
-    }
-  };
-  if (ntiles > 0) issue_tile(0, 0);
   cp_async_commit();
 
-  float o[4][8][4];
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int b = 0; b < 8; ++b)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) o[a][b][c] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
 
-  for (int t = 0; t < ntiles; ++t) {
-    const int st = t & 1;
-    cp_async_wait_all();
-    __syncthreads();  // tile t is in; every warp is done with tile t-1
-    if (t + 1 < ntiles) issue_tile(t + 1, st ^ 1);
-    cp_async_commit();
-    const uint32_t tile = sKV + st * NT * ROWB;
+  if (warp < 4) {
+    // Q dims 0..383 -> TMEM columns [256, 448): lane = head, column j holds
+    // dims 2j, 2j+1
+    const int h = h0 + tid;
+    const uint4 *qrow = reinterpret_cast<const uint4 *>(q + ((int64_t)r * H + (h < H ? h : 0)) * ROWB);
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll
+    for (int part = 0; part < QT_DIMS / 64; ++part) {
+      uint32_t v[32];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (h < H) w = qrow[part * 8 + k];
+        v[4 * k] = w.x; v[4 * k + 1] = w.y; v[4 * k + 2] = w.z; v[4 * k + 3] = w.w;
+      }
+      TMEM_ST32(lane_base + COL_Q + part * 32, v);
+    }
+    tmem_wait_st();
+  }
+  cp_async_wait<0>();
+  fence_proxy_async();
+  fence_before();
+  __syncthreads();
+  fence_after();
 
-    // ---- S = Q K^T: heads 16*mt.., keys 32*nh.. ----
-    float acc[4][4];
+  bool timed_out = false;
+
+  if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------ gather producers ----
+    const int p = tid - 128;          // 0..127
+    const int key = p >> 2;           // 32 keys per tile, 4 threads per key
+    const int sub = p & 3;            // chunks sub, sub+4, ..., 18 per thread
+    for (int t = 0; t < T && !timed_out; ++t) {
+      const int st = t % STAGES;
+      if (t >= STAGES && !bar_wait(bar(B_EMPTY + st), ((t / STAGES) - 1) & 1)) {
+        timed_out = true;
+        break;
+      }
+      const int j = t * NK + key;
+      const int32_t id = (j < K) ? idx_row[j] : -1;
+      const bool v = id >= 0 && id < n_kv;
+      const char *src = kv + (v ? (int64_t)id * ROWB : 0);
+      const uint32_t dst = sbase + KV_OFF + st * KV_STAGE_BYTES;
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
-    const int arow = 16 * mt + (lane & 15);
-#pragma unroll 4
-    for (int kk = 0; kk < D / 16; ++kk) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(sQ + arow * ROWB + swz(arow, 2 * kk + (lane >> 4)) * 16, a0, a1, a2, a3);
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        const int key = 32 * nh + 16 * np + (lane & 7) + ((lane >> 4) << 3);
-        const int ch = 2 * kk + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(tile + key * ROWB + swz(key, ch) * 16, b0, b1, b2, b3);
-        mma_bf16(acc[2 * np], a0, a1, a2, a3, b0, b1);
-        mma_bf16(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+      for (int k = 0; k < NCH / 4; ++k) {
+        const int ch = sub + 4 * k;
+        cp_async16(dst + (ch >> 3) * KV_BLOCK_BYTES + sw128(key, ch & 7), v ? src + ch * 16 : q, v);
+      }
+      cp_async_commit();
+      if (t >= LAG) {
+        cp_async_wait<LAG>();
+        fence_proxy_async();
+        bar_arrive(bar(B_FULL + (t - LAG) % STAGES));
       }
     }
+    cp_async_wait<0>();
+    fence_proxy_async();
+    if (!timed_out)
+      for (int t = (T > LAG ? T - LAG : 0); t < T; ++t) bar_arrive(bar(B_FULL + t % STAGES));
+  } else if (warp == 8) {
+    // ------------------------------------------------------ MMA issuer ----
+    if (lane == 0) {
+      const uint32_t kv0 = sbase + KV_OFF, qs0 = sbase + QS_OFF, p0 = sbase + P_OFF;
+      auto issue_pv = [&](int u) -> bool {
+        const int sb = u & 1, st = u % STAGES;
+        if (!bar_wait(bar(B_PFULL + sb), (u >> 1) & 1)) return false;
+        fence_after();
+        const uint32_t vbase = kv0 + st * KV_STAGE_BYTES + (4 * c) * KV_BLOCK_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < NK / 16; ++ks)
+          mma_ss(tmem + COL_O, sdesc(p0 + sb * P_BYTES + ks * 32, 16, 1024),
+                 sdesc(vbase + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (u > 0 || ks > 0));
+        mma_commit(bar(B_PVDONE + sb));
+        mma_commit(bar(B_EMPTY + st));
+        return true;
+      };
+      bool ok = true;
+      for (int t = 0; t < T && ok; ++t) {
+        const int st = t % STAGES, sb = t & 1;
+        ok = bar_wait(bar(B_FULL + st), (t / STAGES) & 1);
+        if (ok && t >= 2) ok = bar_wait(bar(B_SFREE + sb), ((t >> 1) - 1) & 1);
+        if (!ok) break;
+        fence_after();
+        const uint32_t kt = kv0 + st * KV_STAGE_BYTES;
+        const uint32_t sd = tmem + COL_S + sb * NK;
+#pragma unroll
+        for (int kk = 0; kk < QT_DIMS / 16; ++kk)
+          mma_ts(sd, tmem + COL_Q + kk * 8,
+                 sdesc(kt + (kk >> 2) * KV_BLOCK_BYTES + (kk & 3) * 32, 16, 1024), IDESC_QK,
+                 kk > 0);
+#pragma unroll
+        for (int kk = QT_DIMS / 16; kk < D / 16; ++kk) {
+          const int qk = kk - QT_DIMS / 16;
+          mma_ss(sd, sdesc(qs0 + (qk >> 2) * (HG * 128) + (qk & 3) * 32, 16, 1024),
+                 sdesc(kt + (kk >> 2) * KV_BLOCK_BYTES + (kk & 3) * 32, 16, 1024), IDESC_QK, 1);
+        }
+        mma_commit(bar(B_SFULL + sb));
+        if (t >= 1) ok = issue_pv(t - 1);
+      }
+      if (ok && T > 0) ok = issue_pv(T - 1);
+      if (ok) mma_commit(bar(B_OFULL));
+      timed_out = !ok;
+    }
+  } else {
+    // ---------------------------------------------- softmax (warps 0-3) ----
+    const int hrow = tid;                          // head row = TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    float m_used = -INFINITY, l = 0.f;
+    const uint32_t p0 = sbase + P_OFF;
+    for (int t = 0; t < T; ++t) {
+      const int sb = t & 1;
+      if (!warp_wait(bar(B_SFULL + sb), (t >> 1) & 1)) { timed_out = true; break; }
+      fence_after();
+      uint32_t sr[32];
+      TMEM_LD32(lane_base + COL_S + sb * NK, sr);
+      tmem_wait_ld();
+      fence_before();
+      __syncwarp();
+      if (lane == 0) bar_arrive(bar(B_SFREE + sb));
 
-    // ---- online softmax (log2 domain) ----
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+      // key validity of this tile (same for every head)
+      float x[NK];
+      float mt = -INFINITY;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
+      for (int k4 = 0; k4 < NK / 4; ++k4) {
+        const int j0 = t * NK + 4 * k4;
+        int4 ids = make_int4(-1, -1, -1, -1);
+        if (j0 + 3 < K && (K & 3) == 0) {
+          ids = *reinterpret_cast<const int4 *>(idx_row + j0);
+        } else {
+          if (j0 < K) ids.x = idx_row[j0];
+          if (j0 + 1 < K) ids.y = idx_row[j0 + 1];
+          if (j0 + 2 < K) ids.z = idx_row[j0 + 2];
+          if (j0 + 3 < K) ids.w = idx_row[j0 + 3];
+        }
+        const int32_t idv[4] = {ids.x, ids.y, ids.z, ids.w};
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = 32 * nh + 8 * nt + 2 * qd + e;
-        const bool v = sValid[st * NT + key] != 0;
-        acc[nt][e] = v ? acc[nt][e] * scale_log2 : -INFINITY;
-        acc[nt][2 + e] = v ? acc[nt][2 + e] * scale_log2 : -INFINITY;
-        mx0 = fmaxf(mx0, acc[nt][e]);
-        mx1 = fmaxf(mx1, acc[nt][2 + e]);
-      }
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const int row0 = 16 * mt + g, row1 = row0 + 8;
-    if (qd == 0) {
-      sMax[nh * HG + row0] = mx0;
-      sMax[nh * HG + row1] = mx1;
-    }
-    __syncthreads();
-    const float tm0 = fmaxf(sMax[row0], sMax[HG + row0]);
-    const float tm1 = fmaxf(sMax[row1], sMax[HG + row1]);
-    const float mn0 = fmaxf(m_run[0], tm0), mn1 = fmaxf(m_run[1], tm1);
-    const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m_run[0] - mn0);
-    const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m_run[1] - mn1);
-    const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
-    const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
-    m_run[0] = mn0;
-    m_run[1] = mn1;
-    float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const float p00 = exp2f(acc[nt][0] - mu0), p01 = exp2f(acc[nt][1] - mu0);
-      const float p10 = exp2f(acc[nt][2] - mu1), p11 = exp2f(acc[nt][3] - mu1);
-      ps0 += p00 + p01;
-      ps1 += p10 + p11;
-      const int chunk = 4 * nh + nt;  // 8 keys per 16-byte chunk
-      asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(sP + row0 * 128 + swz(row0, chunk) * 16 +
-                                                       qd * 4),
-                   "r"(pack_bf16(p00, p01)));
-      asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(sP + row1 * 128 + swz(row1, chunk) * 16 +
-                                                       qd * 4),
-                   "r"(pack_bf16(p10, p11)));
-    }
-    l_run[0] = l_run[0] * al0 + ps0;
-    l_run[1] = l_run[1] * al1 + ps1;
-    if (nh == 0 && qd == 0) {
-      sAlpha[row0] = al0;
-      sAlpha[row1] = al1;
-    }
-    __syncthreads();
-
-    // ---- O = O * alpha + P V: value dims 64*warp .. ----
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const float x0 = sAlpha[16 * m + g], x1 = sAlpha[16 * m + g + 8];
-#pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        o[m][n][0] *= x0; o[m][n][1] *= x0;
-        o[m][n][2] *= x1; o[m][n][3] *= x1;
-      }
-    }
-#pragma unroll
-    for (int ks = 0; ks < NT / 16; ++ks) {
-      uint32_t pa[4][4];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int prow = 16 * m + (lane & 15);
-        ldsm_x4(sP + prow * 128 + swz(prow, 2 * ks + (lane >> 4)) * 16, pa[m][0], pa[m][1],
-                pa[m][2], pa[m][3]);
-      }
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        const int key = 16 * ks + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int ch = 8 * warp + 2 * np + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(tile + key * ROWB + swz(key, ch) * 16, b0, b1, b2, b3);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          mma_bf16(o[m][2 * np], pa[m][0], pa[m][1], pa[m][2], pa[m][3], b0, b1);
-          mma_bf16(o[m][2 * np + 1], pa[m][0], pa[m][1], pa[m][2], pa[m][3], b2, b3);
+        for (int e = 0; e < 4; ++e) {
+          const int k = 4 * k4 + e;
+          const bool v = idv[e] >= 0 && idv[e] < n_kv;
+          x[k] = v ? __uint_as_float(sr[k]) * scale_log2 : -INFINITY;
+          mt = fmaxf(mt, x[k]);
         }
       }
-    }
-  }
-  cp_async_wait_all();
+      // lazy rescale: only when the running max grows by more than 8 (log2)
+      const bool grow = mt > m_used + 8.0f;
+      const bool need_o = grow && m_used != -INFINITY;
+      if (__any_sync(0xffffffffu, need_o)) {
+        // O must hold every PV issued so far before it is rescaled
+        if (t >= 1 && !warp_wait(bar(B_PVDONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1)) {
+          timed_out = true;
+          break;
+        }
+        fence_after();
+        const float alpha = need_o ? exp2f(m_used - mt) : 1.0f;
+#pragma unroll 1
+        for (int part = 0; part < 256 / 32; ++part) {
+          uint32_t o[32];
+          TMEM_LD32(lane_base + COL_O + part * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          TMEM_ST32(lane_base + COL_O + part * 32, o);
+        }
+        tmem_wait_st();
+        if (need_o) l *= alpha;
+      }
+      if (grow) m_used = mt;
 
-  // ---- epilogue: row sums, output, lse ----
-  l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 1);
-  l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 2);
-  l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 1);
-  l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 2);
-  if (qd == 0) {
-    sSum[nh * HG + 16 * mt + g] = l_run[0];
-    sSum[nh * HG + 16 * mt + g + 8] = l_run[1];
-    if (nh == 0) {
-      sMax[16 * mt + g] = m_run[0];
-      sMax[16 * mt + g + 8] = m_run[1];
+      // P = exp2(x - m) as bf16 into P[sb] (keys 0..31 = chunks 0..3 of row hrow)
+      if (t >= 2 && !warp_wait(bar(B_PVDONE + sb), ((t >> 1) - 1) & 1)) { timed_out = true; break; }
+      float ps = 0.f;
+      uint32_t pk[NK / 2];
+#pragma unroll
+      for (int k = 0; k < NK; k += 2) {
+        const float a = (m_used == -INFINITY) ? 0.f : exp2f(x[k] - m_used);
+        const float b = (m_used == -INFINITY) ? 0.f : exp2f(x[k + 1] - m_used);
+        ps += a + b;
+        pk[k / 2] = pack_bf16(a, b);
+      }
+      l += ps;
+      unsigned char *prow = sm + P_OFF + sb * P_BYTES;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+        *reinterpret_cast<uint4 *>(prow + sw128(hrow, ch)) =
+            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      fence_proxy_async();
+      fence_before();
+      __syncwarp();
+      if (lane == 0) bar_arrive(bar(B_PFULL + sb));
     }
-  }
-  __syncthreads();
+
+    // ---------------------------------------------------------- epilogue --
+    const int h = h0 + hrow;
+    if (!timed_out && T > 0 && !warp_wait(bar(B_OFULL), 0)) timed_out = true;
+    fence_after();
+    const float inv = l > 0.f ? 1.0f / l : 0.f;
+    __nv_bfloat16 *orow = out + ((int64_t)r * H + (h < H ? h : 0)) * DV + 256 * c;
+#pragma unroll 1
+    for (int part = 0; part < 256 / 32; ++part) {
+      uint32_t o[32];
+      if (T > 0 && !timed_out) {
+        TMEM_LD32(lane_base + COL_O + part * 32, o);
+        tmem_wait_ld();
+      } else {
 #pragma unroll
-  for (int m = 0; m < 4; ++m) {
+        for (int k = 0; k < 32; ++k) o[k] = 0u;
+      }
+      if (h < H) {
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + part * 32);
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int row = 16 * m + g + 8 * hh;
-      const int h = h0 + row;
-      if (h >= H) continue;
-      const float l = sSum[row] + sSum[HG + row];
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16 *orow = out + ((int64_t)r * H + h) * DV + 64 * warp + 2 * qd;
-#pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        *reinterpret_cast<uint32_t *>(orow + 8 * n) =
-            pack_bf16(o[m][n][2 * hh] * inv, o[m][n][2 * hh + 1] * inv);
+        for (int k = 0; k < 4; ++k)
+          dst[k] = make_uint4(pack_bf16(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv),
+                              pack_bf16(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv),
+                              pack_bf16(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
+                              pack_bf16(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
       }
     }
+    if (lse && c == 0 && h < H)
+      lse[(int64_t)r * H + h] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
   }
-  if (lse && tid < HG && h0 + tid < H) {
-    const float l = sSum[tid] + sSum[HG + tid];
-    lse[(int64_t)r * H + h0 + tid] =
-        l > 0.f ? (sMax[tid] + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+
+  if (timed_out && status) atomicOr(status, 4u);
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem));
   }
 }
 
@@ -306,29 +484,30 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 extern "C" int hs_sparse_attn_decode(const void *q, const void *kv, int64_t n_kv_rows,
                                      const int32_t *idx, int32_t R, int32_t H, int32_t K,
-                                     float scale, void *out, float *lse, hs_stream_t stream) {
+                                     float scale, void *out, float *lse, uint32_t *status,
+                                     hs_stream_t stream) {
   if (R < 0 || H < 1 || H > 1024 || K < 0 || n_kv_rows < 0)
     return hs_set_error(HS_ERR_INVALID_ARG, "bad sizes R=%d H=%d (1..1024) K=%d n_kv_rows=%lld",
                         R, H, K, (long long)n_kv_rows);
   if (R == 0) return HS_OK;
   if (!q || !out || (K > 0 && (!idx || (!kv && n_kv_rows > 0))))
     return hs_set_error(HS_ERR_INVALID_ARG, "NULL q/kv/idx/out");
-  if (((uintptr_t)q & 15) || ((uintptr_t)kv & 15) || ((uintptr_t)out & 3))
-    return hs_set_error(HS_ERR_INVALID_ARG, "q and kv must be 16-byte aligned, out 4-byte");
+  if (((uintptr_t)q & 15) || ((uintptr_t)kv & 15) || ((uintptr_t)out & 15))
+    return hs_set_error(HS_ERR_INVALID_ARG, "q, kv and out must be 16-byte aligned");
   if (!(scale == scale)) return hs_set_error(HS_ERR_INVALID_ARG, "scale is NaN");
   int dev = 0;
   HS_CUDA_TRY(cudaGetDevice(&dev));
   static bool attr_done[64] = {false};
   if (dev >= 64 || !attr_done[dev]) {
-    HS_CUDA_TRY(cudaFuncSetAttribute(k_attn_mma, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES));
+    HS_CUDA_TRY(cudaFuncSetAttribute(k_attn_umma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_ALLOC));
     if (dev < 64) attr_done[dev] = true;
   }
-  const int64_t blocks = (int64_t)R * ((H + HG - 1) / HG);
+  const int64_t blocks = (int64_t)R * ((H + HG - 1) / HG) * 2;
   if (blocks > INT32_MAX) return hs_set_error(HS_ERR_UNSUPPORTED, "R*H too large");
-  k_attn_mma<<<(unsigned)blocks, THREADS, SMEM_BYTES, stream>>>(
+  k_attn_umma<<<(unsigned)blocks, THREADS, SMEM_ALLOC, stream>>>(
       reinterpret_cast<const char *>(q), reinterpret_cast<const char *>(kv), n_kv_rows, idx, H,
-      K, scale * 1.4426950408889634f, reinterpret_cast<__nv_bfloat16 *>(out), lse);
-  HS_LAUNCH_CHECK("k_attn_mma");
+      K, scale * 1.4426950408889634f, reinterpret_cast<__nv_bfloat16 *>(out), lse, status);
+  HS_LAUNCH_CHECK("k_attn_umma");
   return HS_OK;
 }

@@ -67,6 +67,8 @@ enum hs_status_code {
                                  outside the buffer                          */
 #define HS_STATUS_CAPACITY 2u /* a request needed more than S positions in one
                                  swap-in, or a commit would pass max_ctx      */
+#define HS_STATUS_TIMEOUT 4u  /* a bounded wait inside a kernel gave up (the
+                                 kernel wound down; its outputs are invalid) */
 
 #define HS_LATENT_DIM 576 /* q and latent KV row: 512 value dims + 64 rope */
 #define HS_VALUE_DIM 512  /* attention values are dims 0..511 of a row     */
@@ -230,13 +232,16 @@ int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
  *   kv     device bf16 [n_kv_rows][576], 16-byte aligned (the paged cache for
  *          resolve indices, hot_kv for swap-in indices)
  *   idx    device int32 [R][K]
- *   out    device bf16 [R][H][512]
+ *   out    device bf16 [R][H][512], 16-byte aligned
  *   lse    device float [R][H] or NULL
+ *   status device uint32 or NULL: HS_STATUS_TIMEOUT is OR-ed in if one of
+ *          the kernel's bounded internal waits gives up (never expected)
  * Requirements: R >= 0, 1 <= H <= 1024, K >= 0.
  */
 int hs_sparse_attn_decode(const void *q, const void *kv, int64_t n_kv_rows,
                           const int32_t *idx, int32_t R, int32_t H, int32_t K,
-                          float scale, void *out, float *lse, hs_stream_t stream);
+                          float scale, void *out, float *lse, uint32_t *status,
+                          hs_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* a7-a8: greedy verify and commit of the accepted prefix ([KVF] ④-⑥)       */

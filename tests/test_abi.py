@@ -36,7 +36,7 @@ def test_argument_errors_return_without_a_gpu():
                              None) == hs.HS_ERR_INVALID_ARG
     assert b"bad sizes" in L.hs_last_error_string()
     assert L.hs_sparse_attn_decode(None, None, 0, None, 1, 0, 1, ctypes.c_float(1.0), None,
-                                   None, None) == hs.HS_ERR_INVALID_ARG
+                                   None, None, None) == hs.HS_ERR_INVALID_ARG
     assert L.hs_buffer_create(None, None) == hs.HS_ERR_INVALID_ARG
     assert L.hs_swap_in(None, None, None, None, None, 0, 0, None, None, None,
                         None) == hs.HS_ERR_INVALID_ARG
