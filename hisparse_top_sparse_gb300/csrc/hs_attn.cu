@@ -18,11 +18,15 @@
 //   * S = Q K^T (128 x 32 fp32, all 576 dims -- both CTAs compute it) is
 //     double-buffered in TMEM columns [448, 512);
 //   * KV rows are gathered 32 at a time by 16-byte cp.async into a 4-stage
-//     ring of swizzled tiles (36 KB each): the tile is the K-major B operand
+//     ring of swizzled tiles (36 KB each), each producer thread's copies
+//     arriving on the stage's mbarrier as they land (cp.async.mbarrier.arrive),
+//     so up to four tiles are in flight: the tile is the K-major B operand
 //     of Q K^T and, read MN-major, the B operand of P V;
 //   * P (bf16) goes through shared memory (double-buffered) as P V's A.
-// Warp roles (288 threads): warps 0-3 softmax + epilogue (thread = head =
-// TMEM lane), warps 4-7 gather producers, warp 8 lane 0 issues the MMAs.
+// Warp roles (352 threads): warps 0-3 softmax + epilogue (thread = head =
+// TMEM lane), warps 4-7 gather producers, warps 8 and 9 issue Q K^T for even
+// and odd tiles (a single thread issues one tcgen05.mma per ~100-160 cycles,
+// so two chains are kept in flight), warp 10 issues P V.
 // Online softmax in the log2 domain with lazy rescaling: O is rescaled (in
 // TMEM) only when a row's running max grows by more than 2^8.
 // Every mbarrier wait is bounded; a wait that gives up sets HS_STATUS_TIMEOUT
@@ -39,13 +43,12 @@ constexpr int DV = HS_VALUE_DIM;
 constexpr int HG = 128;                   // heads per CTA (MMA M)
 constexpr int NK = 32;                    // keys per tile (MMA N of Q K^T)
 constexpr int STAGES = 4;
-constexpr int LAG = 2;                    // producer: cp.async groups kept in flight
 constexpr int ROWB = D * 2;               // 1152
 constexpr int NCH = ROWB / 16;            // 72 chunks of 16 B per latent row
 constexpr int QT_DIMS = 384;              // Q dims held in TMEM
 constexpr int QS_BLOCKS = (D - QT_DIMS) / 64;   // 3 swizzle blocks of Q in SMEM
 constexpr int KV_BLOCKS = D / 64;         // 9 swizzle blocks per KV tile
-constexpr int THREADS = 288;
+constexpr int THREADS = 352;
 constexpr int NPROD = 128;
 
 // shared memory (offsets from a 1024-byte aligned base)
@@ -281,14 +284,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int p = tid - 128;          // 0..127
     const int key = p >> 2;           // 32 keys per tile, 4 threads per key
     const int sub = p & 3;            // chunks sub, sub+4, ..., 18 per thread
+    // this thread's key index for tiles t and t+1 is loaded two tiles ahead so
+    // the index load never sits between a stage becoming free and its refill
+    auto load_id = [&](int t) -> int32_t {
+      const int j = t * NK + key;
+      return (t < T && j < K) ? __ldg(idx_row + j) : -1;
+    };
+    int32_t id0 = load_id(0), id1 = load_id(1);
     for (int t = 0; t < T && !timed_out; ++t) {
       const int st = t % STAGES;
+      const int32_t id = id0;
+      id0 = id1;
+      id1 = load_id(t + 2);
       if (t >= STAGES && !bar_wait(bar(B_EMPTY + st), ((t / STAGES) - 1) & 1)) {
         timed_out = true;
         break;
       }
-      const int j = t * NK + key;
-      const int32_t id = (j < K) ? idx_row[j] : -1;
       const bool v = id >= 0 && id < n_kv;
       const char *src = kv + (v ? (int64_t)id * ROWB : 0);
       const uint32_t dst = sbase + KV_OFF + st * KV_STAGE_BYTES;
@@ -297,41 +308,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int ch = sub + 4 * k;
         cp_async16(dst + (ch >> 3) * KV_BLOCK_BYTES + sw128(key, ch & 7), v ? src + ch * 16 : q, v);
       }
-      cp_async_commit();
-      if (t >= LAG) {
-        cp_async_wait<LAG>();
-        fence_proxy_async();
-        bar_arrive(bar(B_FULL + (t - LAG) % STAGES));
-      }
+      // the stage's barrier gets this thread's arrival when its copies land
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(
+                       bar(B_FULL + st))
+                   : "memory");
     }
     cp_async_wait<0>();
-    fence_proxy_async();
-    if (!timed_out)
-      for (int t = (T > LAG ? T - LAG : 0); t < T; ++t) bar_arrive(bar(B_FULL + t % STAGES));
-  } else if (warp == 8) {
-    // ------------------------------------------------------ MMA issuer ----
+  } else if (warp == 8 || warp == 9) {
+    // ------------------------------------------ Q K^T issuers (2 warps) ----
+    // warp 8 issues tiles 0, 2, 4, ... into S buffer 0, warp 9 tiles 1, 3, ...
+    // into S buffer 1, so two 36-instruction chains are in flight at once
     if (lane == 0) {
-      const uint32_t kv0 = sbase + KV_OFF, qs0 = sbase + QS_OFF, p0 = sbase + P_OFF;
-      auto issue_pv = [&](int u) -> bool {
-        const int sb = u & 1, st = u % STAGES;
-        if (!bar_wait(bar(B_PFULL + sb), (u >> 1) & 1)) return false;
-        fence_after();
-        const uint32_t vbase = kv0 + st * KV_STAGE_BYTES + (4 * c) * KV_BLOCK_BYTES;
-#pragma unroll
-        for (int ks = 0; ks < NK / 16; ++ks)
-          mma_ss(tmem + COL_O, sdesc(p0 + sb * P_BYTES + ks * 32, 16, 1024),
-                 sdesc(vbase + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (u > 0 || ks > 0));
-        mma_commit(bar(B_PVDONE + sb));
-        mma_commit(bar(B_EMPTY + st));
-        return true;
-      };
+      const uint32_t kv0 = sbase + KV_OFF, qs0 = sbase + QS_OFF;
+      const int sb = warp - 8;
       bool ok = true;
-      for (int t = 0; t < T && ok; ++t) {
-        const int st = t % STAGES, sb = t & 1;
+      for (int t = sb; t < T && ok; t += 2) {
+        const int st = t % STAGES;
         ok = bar_wait(bar(B_FULL + st), (t / STAGES) & 1);
         if (ok && t >= 2) ok = bar_wait(bar(B_SFREE + sb), ((t >> 1) - 1) & 1);
         if (!ok) break;
         fence_after();
+        fence_proxy_async();   // the tile was written by cp.async (generic proxy)
         const uint32_t kt = kv0 + st * KV_STAGE_BYTES;
         const uint32_t sd = tmem + COL_S + sb * NK;
 #pragma unroll
@@ -346,10 +343,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                  sdesc(kt + (kk >> 2) * KV_BLOCK_BYTES + (kk & 3) * 32, 16, 1024), IDESC_QK, 1);
         }
         mma_commit(bar(B_SFULL + sb));
-        if (t >= 1) ok = issue_pv(t - 1);
       }
-      if (ok && T > 0) ok = issue_pv(T - 1);
-      if (ok) mma_commit(bar(B_OFULL));
+      timed_out = !ok;
+    }
+  } else if (warp == 10) {
+    // --------------------------------------------------- P V issuer ----
+    if (lane == 0) {
+      const uint32_t kv0 = sbase + KV_OFF, p0 = sbase + P_OFF;
+      bool ok = true;
+      for (int u = 0; u < T && ok; ++u) {
+        const int sb = u & 1, st = u % STAGES;
+        ok = bar_wait(bar(B_PFULL + sb), (u >> 1) & 1);
+        if (!ok) break;
+        fence_after();
+        const uint32_t vbase = kv0 + st * KV_STAGE_BYTES + (4 * c) * KV_BLOCK_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < NK / 16; ++ks)
+          mma_ss(tmem + COL_O, sdesc(p0 + sb * P_BYTES + ks * 32, 16, 1024),
+                 sdesc(vbase + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (u > 0 || ks > 0));
+        mma_commit(bar(B_PVDONE + sb));
+        mma_commit(bar(B_EMPTY + st));
+      }
+      if (ok && T > 0) mma_commit(bar(B_OFULL));
       timed_out = !ok;
     }
   } else {
@@ -357,7 +372,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int hrow = tid;                          // head row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     float m_used = -INFINITY, l = 0.f;
-    const uint32_t p0 = sbase + P_OFF;
+    int32_t my_id = (T > 0 && lane < K) ? __ldg(idx_row + lane) : -1;
     for (int t = 0; t < T; ++t) {
       const int sb = t & 1;
       if (!warp_wait(bar(B_SFULL + sb), (t >> 1) & 1)) { timed_out = true; break; }
@@ -369,29 +384,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) bar_arrive(bar(B_SFREE + sb));
 
-      // key validity of this tile (same for every head)
+      // key validity of this tile: one index per lane, loaded a tile ahead
+      const uint32_t vmask = __ballot_sync(0xffffffffu, my_id >= 0 && my_id < n_kv);
+      my_id = (t + 1 < T && (t + 1) * NK + lane < K) ? __ldg(idx_row + (t + 1) * NK + lane) : -1;
       float x[NK];
       float mt = -INFINITY;
 #pragma unroll
-      for (int k4 = 0; k4 < NK / 4; ++k4) {
-        const int j0 = t * NK + 4 * k4;
-        int4 ids = make_int4(-1, -1, -1, -1);
-        if (j0 + 3 < K && (K & 3) == 0) {
-          ids = *reinterpret_cast<const int4 *>(idx_row + j0);
-        } else {
-          if (j0 < K) ids.x = idx_row[j0];
-          if (j0 + 1 < K) ids.y = idx_row[j0 + 1];
-          if (j0 + 2 < K) ids.z = idx_row[j0 + 2];
-          if (j0 + 3 < K) ids.w = idx_row[j0 + 3];
-        }
-        const int32_t idv[4] = {ids.x, ids.y, ids.z, ids.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k = 4 * k4 + e;
-          const bool v = idv[e] >= 0 && idv[e] < n_kv;
-          x[k] = v ? __uint_as_float(sr[k]) * scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[k]);
-        }
+      for (int k = 0; k < NK; ++k) {
+        x[k] = ((vmask >> k) & 1u) ? __uint_as_float(sr[k]) * scale_log2 : -INFINITY;
+        mt = fmaxf(mt, x[k]);
       }
       // lazy rescale: only when the running max grows by more than 8 (log2)
       const bool grow = mt > m_used + 8.0f;
