@@ -13,20 +13,22 @@
 // all of TMEM) do not fit one SM together with KV tiles. Each row is therefore
 // served by two CTAs, c = 0 / 1, each owning value dims [256c, 256c + 256):
 //   * O_c (128 x 256 fp32) lives in TMEM columns [0, 256);
-//   * Q dims 0..383 live in TMEM columns [256, 448) as the MMA's A operand;
-//     Q dims 384..575 live in shared memory (3 x 16 KB, 128-byte swizzle);
-//   * S = Q K^T (128 x 32 fp32, all 576 dims -- both CTAs compute it) is
-//     double-buffered in TMEM columns [448, 512);
+//   * Q dims 0..255 live in TMEM columns [256, 384) as the MMA's A operand;
+//     Q dims 256..575 live in shared memory (5 x 16 KB, 128-byte swizzle);
+//   * S = Q K^T (128 x 32 fp32, all 576 dims -- both CTAs compute it) has
+//     three buffers in TMEM columns [384, 480);
 //   * KV rows are gathered 32 at a time by 16-byte cp.async into a 4-stage
 //     ring of swizzled tiles (36 KB each), each producer thread's copies
 //     arriving on the stage's mbarrier as they land (cp.async.mbarrier.arrive),
 //     so up to four tiles are in flight: the tile is the K-major B operand
 //     of Q K^T and, read MN-major, the B operand of P V;
-//   * P (bf16) goes through shared memory (double-buffered) as P V's A.
-// Warp roles (352 threads): warps 0-3 softmax + epilogue (thread = head =
-// TMEM lane), warps 4-7 gather producers, warps 8 and 9 issue Q K^T for even
-// and odd tiles (a single thread issues one tcgen05.mma per ~100-160 cycles,
-// so two chains are kept in flight), warp 10 issues P V.
+//   * P (bf16, 128 x 32) has two 16-column buffers in TMEM [480, 512) and is
+//     read from TMEM as P V's A operand.
+// Warp roles (384 threads): warps 0-3 softmax + epilogue (thread = head =
+// TMEM lane), warps 4-7 gather producers, warps 8-10
+// issue Q K^T for tiles t = 0, 1, 2 (mod 3) into three S buffers (one thread
+// issues a tcgen05.mma only every ~60-150 cycles, so three chains are kept in
+// flight), warp 11 issues P V.
 // Online softmax in the log2 domain with lazy rescaling: O is rescaled (in
 // TMEM) only when a row's running max grows by more than 2^8.
 // Every mbarrier wait is bounded; a wait that gives up sets HS_STATUS_TIMEOUT
@@ -45,31 +47,32 @@ constexpr int NK = 32;                    // keys per tile (MMA N of Q K^T)
 constexpr int STAGES = 4;
 constexpr int ROWB = D * 2;               // 1152
 constexpr int NCH = ROWB / 16;            // 72 chunks of 16 B per latent row
-constexpr int QT_DIMS = 384;              // Q dims held in TMEM
-constexpr int QS_BLOCKS = (D - QT_DIMS) / 64;   // 3 swizzle blocks of Q in SMEM
+constexpr int QT_DIMS = 256;              // Q dims held in TMEM
+constexpr int QS_BLOCKS = (D - QT_DIMS) / 64;   // 5 swizzle blocks of Q in SMEM
+constexpr int NSB = 3;                    // S buffers = Q K^T chains in flight
 constexpr int KV_BLOCKS = D / 64;         // 9 swizzle blocks per KV tile
-constexpr int THREADS = 352;
+constexpr int THREADS = 384;
 constexpr int NPROD = 128;
 
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr int QS_OFF = 0;
-constexpr int QS_BYTES = QS_BLOCKS * HG * 128;         // 49152
+constexpr int QS_BYTES = QS_BLOCKS * HG * 128;         // 81920
 constexpr int KV_OFF = QS_OFF + QS_BYTES;
 constexpr int KV_BLOCK_BYTES = NK * 128;               // 4096
 constexpr int KV_STAGE_BYTES = KV_BLOCKS * KV_BLOCK_BYTES;   // 36864
-constexpr int P_OFF = KV_OFF + STAGES * KV_STAGE_BYTES;
-constexpr int P_BYTES = HG * 128;                      // 16384 (keys 0..31 used)
-constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
+constexpr int BAR_OFF = KV_OFF + STAGES * KV_STAGE_BYTES;
 constexpr int SMEM_USED = BAR_OFF + 256;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;           // slack for the 1 KB alignment
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
 // TMEM columns
-constexpr uint32_t COL_O = 0, COL_Q = 256, COL_S = 448;
+constexpr uint32_t COL_O = 0, COL_Q = 256, COL_S = 384, COL_P = 480;
+static_assert(COL_Q + QT_DIMS / 2 == COL_S && COL_S + NSB * NK == COL_P && COL_P + 2 * NK / 2 == 512,
+              "TMEM column map");
 
 // barriers (8-byte words at BAR_OFF)
-enum { B_FULL = 0, B_EMPTY = B_FULL + STAGES, B_SFULL = B_EMPTY + STAGES, B_SFREE = B_SFULL + 2,
-       B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2, B_OFULL = B_PVDONE + 2, B_COUNT = B_OFULL + 1 };
+enum { B_FULL = 0, B_EMPTY = B_FULL + STAGES, B_SFULL = B_EMPTY + STAGES, B_SFREE = B_SFULL + NSB,
+       B_PFULL = B_SFREE + NSB, B_PVDONE = B_PFULL + 2, B_OFULL = B_PVDONE + 2, B_COUNT = B_OFULL + 1 };
 static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
 
 constexpr int WAIT_LIMIT = 1 << 24;
@@ -183,11 +186,25 @@ __device__ __forceinline__ void cp_async_wait() {
         "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),   \
         "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),   \
         "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]))
+#define TMEM_ST16(taddr, r)                                                                    \
+  asm volatile(                                                                                \
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12," \
+      "%13,%14,%15,%16};\n" ::"r"(taddr),                                                     \
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),  \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),       \
+      "r"(r[15]))
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
+// 2^x with the PTX approximate base-2 exponential (flushes subnormal results)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -221,9 +238,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       bar_init(bar(B_FULL + s), NPROD);
       bar_init(bar(B_EMPTY + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NSB; ++b) {
       bar_init(bar(B_SFULL + b), 1);
       bar_init(bar(B_SFREE + b), 4);
+    }
+    for (int b = 0; b < 2; ++b) {
       bar_init(bar(B_PFULL + b), 4);
       bar_init(bar(B_PVDONE + b), 1);
     }
@@ -314,18 +333,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                    : "memory");
     }
     cp_async_wait<0>();
-  } else if (warp == 8 || warp == 9) {
-    // ------------------------------------------ Q K^T issuers (2 warps) ----
-    // warp 8 issues tiles 0, 2, 4, ... into S buffer 0, warp 9 tiles 1, 3, ...
-    // into S buffer 1, so two 36-instruction chains are in flight at once
+  } else if (warp >= 8 && warp < 8 + NSB) {
+    // ------------------------------------------ Q K^T issuers (3 warps) ----
+    // warp 8 + b issues tiles t = b, b + 3, ... into S buffer b, so three
+    // 36-instruction chains are in flight at once
     if (lane == 0) {
       const uint32_t kv0 = sbase + KV_OFF, qs0 = sbase + QS_OFF;
       const int sb = warp - 8;
       bool ok = true;
-      for (int t = sb; t < T && ok; t += 2) {
+      for (int t = sb; t < T && ok; t += NSB) {
         const int st = t % STAGES;
         ok = bar_wait(bar(B_FULL + st), (t / STAGES) & 1);
-        if (ok && t >= 2) ok = bar_wait(bar(B_SFREE + sb), ((t >> 1) - 1) & 1);
+        if (ok && t >= NSB) ok = bar_wait(bar(B_SFREE + sb), ((t / NSB) - 1) & 1);
         if (!ok) break;
         fence_after();
         fence_proxy_async();   // the tile was written by cp.async (generic proxy)
@@ -346,10 +365,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       timed_out = !ok;
     }
-  } else if (warp == 10) {
+  } else if (warp == 8 + NSB) {
     // --------------------------------------------------- P V issuer ----
     if (lane == 0) {
-      const uint32_t kv0 = sbase + KV_OFF, p0 = sbase + P_OFF;
+      const uint32_t kv0 = sbase + KV_OFF;
       bool ok = true;
       for (int u = 0; u < T && ok; ++u) {
         const int sb = u & 1, st = u % STAGES;
@@ -359,7 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t vbase = kv0 + st * KV_STAGE_BYTES + (4 * c) * KV_BLOCK_BYTES;
 #pragma unroll
         for (int ks = 0; ks < NK / 16; ++ks)
-          mma_ss(tmem + COL_O, sdesc(p0 + sb * P_BYTES + ks * 32, 16, 1024),
+          mma_ts(tmem + COL_O, tmem + COL_P + sb * (NK / 2) + ks * 8,
                  sdesc(vbase + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (u > 0 || ks > 0));
         mma_commit(bar(B_PVDONE + sb));
         mma_commit(bar(B_EMPTY + st));
@@ -372,28 +391,34 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int hrow = tid;                          // head row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     float m_used = -INFINITY, l = 0.f;
-    int32_t my_id = (T > 0 && lane < K) ? __ldg(idx_row + lane) : -1;
+    // index of key `lane` of tile t, loaded a tile ahead
+    auto load_id = [&](int t) -> int32_t {
+      return (t < T && t * NK + lane < K) ? __ldg(idx_row + t * NK + lane) : -1;
+    };
+    int32_t my_id = load_id(0);
     for (int t = 0; t < T; ++t) {
-      const int sb = t & 1;
-      if (!warp_wait(bar(B_SFULL + sb), (t >> 1) & 1)) { timed_out = true; break; }
+      const int sb = t % NSB, pb = t & 1;
+      if (!warp_wait(bar(B_SFULL + sb), (t / NSB) & 1)) { timed_out = true; break; }
       fence_after();
-      uint32_t sr[32];
+      uint32_t sr[NK];
       TMEM_LD32(lane_base + COL_S + sb * NK, sr);
       tmem_wait_ld();
       fence_before();
       __syncwarp();
-      if (lane == 0) bar_arrive(bar(B_SFREE + sb));
+      if (lane == 0) bar_arrive(bar(B_SFREE + sb));   // the S buffer may be refilled
 
-      // key validity of this tile: one index per lane, loaded a tile ahead
+      // invalid keys -> -inf in place (warp-uniform skip when all are valid)
       const uint32_t vmask = __ballot_sync(0xffffffffu, my_id >= 0 && my_id < n_kv);
-      my_id = (t + 1 < T && (t + 1) * NK + lane < K) ? __ldg(idx_row + (t + 1) * NK + lane) : -1;
-      float x[NK];
-      float mt = -INFINITY;
+      my_id = load_id(t + 1);
+      if (vmask != 0xffffffffu) {
 #pragma unroll
-      for (int k = 0; k < NK; ++k) {
-        x[k] = ((vmask >> k) & 1u) ? __uint_as_float(sr[k]) * scale_log2 : -INFINITY;
-        mt = fmaxf(mt, x[k]);
+        for (int k = 0; k < NK; ++k)
+          if (!((vmask >> k) & 1u)) sr[k] = 0xff800000u;
       }
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int k = 0; k < NK; ++k) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(sr[k]));
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
       // lazy rescale: only when the running max grows by more than 8 (log2)
       const bool grow = mt > m_used + 8.0f;
       const bool need_o = grow && m_used != -INFINITY;
@@ -404,7 +429,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         fence_after();
-        const float alpha = need_o ? exp2f(m_used - mt) : 1.0f;
+        const float alpha = need_o ? ex2(m_used - mt) : 1.0f;
 #pragma unroll 1
         for (int part = 0; part < 256 / 32; ++part) {
           uint32_t o[32];
@@ -419,27 +444,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (grow) m_used = mt;
 
-      // P = exp2(x - m) as bf16 into P[sb] (keys 0..31 = chunks 0..3 of row hrow)
-      if (t >= 2 && !warp_wait(bar(B_PVDONE + sb), ((t >> 1) - 1) & 1)) { timed_out = true; break; }
-      float ps = 0.f;
-      uint32_t pk[NK / 2];
+      // P = exp2(s * scale - m) as bf16 into P buffer pb (P V reads it from
+      // TMEM as its A operand) once P V(t-2) has finished with that buffer
+      if (t >= 2 && !warp_wait(bar(B_PVDONE + pb), ((t >> 1) - 1) & 1)) { timed_out = true; break; }
+      const float mu = (m_used == -INFINITY) ? 0.f : m_used;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < NK; k += 2) {
-        const float a = (m_used == -INFINITY) ? 0.f : exp2f(x[k] - m_used);
-        const float b = (m_used == -INFINITY) ? 0.f : exp2f(x[k + 1] - m_used);
-        ps += a + b;
-        pk[k / 2] = pack_bf16(a, b);
+      for (int k = 0; k < NK / 2; ++k) {
+        const float a = ex2(fmaf(__uint_as_float(sr[2 * k]), scale_log2, -mu));
+        const float b = ex2(fmaf(__uint_as_float(sr[2 * k + 1]), scale_log2, -mu));
+        ps[k & 3] += a + b;
+        sr[k] = pack_bf16(a, b);          // in place: pair k of P
       }
-      l += ps;
-      unsigned char *prow = sm + P_OFF + sb * P_BYTES;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-        *reinterpret_cast<uint4 *>(prow + sw128(hrow, ch)) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      fence_proxy_async();
+      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      TMEM_ST16(lane_base + COL_P + pb * (NK / 2), sr);
+      tmem_wait_st();
       fence_before();
       __syncwarp();
-      if (lane == 0) bar_arrive(bar(B_PFULL + sb));
+      if (lane == 0) bar_arrive(bar(B_PFULL + pb));
     }
 
     // ---------------------------------------------------------- epilogue --
