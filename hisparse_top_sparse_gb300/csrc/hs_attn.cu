@@ -24,12 +24,11 @@
 //     of Q K^T and, read MN-major, the B operand of P V;
 //   * P (bf16, 128 x 32) has two 16-column buffers in TMEM [480, 512) and is
 //     read from TMEM as P V's A operand.
-// Warp roles (512 threads): warps 0-7 softmax + epilogue (two warps per TMEM
-// lane quadrant, thread = head = TMEM lane, each warp half of a tile's keys
-// and half of O's columns), warps 8-11 gather producers, warps 12-14 issue
-// Q K^T for tiles t = 0, 1, 2 (mod 3) into three S buffers (one thread issues
-// a tcgen05.mma only every ~60-150 cycles, so three chains are kept in
-// flight), warp 15 issues P V.
+// Warp roles (384 threads): warps 0-3 softmax + epilogue (thread = head =
+// TMEM lane), warps 4-7 gather producers, warps 8-10
+// issue Q K^T for tiles t = 0, 1, 2 (mod 3) into three S buffers (one thread
+// issues a tcgen05.mma only every ~60-150 cycles, so three chains are kept in
+// flight), warp 11 issues P V.
 // Online softmax in the log2 domain with lazy rescaling: O is rescaled (in
 // TMEM) only when a row's running max grows by more than 2^8.
 // Every mbarrier wait is bounded; a wait that gives up sets HS_STATUS_TIMEOUT
@@ -46,15 +45,13 @@ constexpr int DV = HS_VALUE_DIM;
 constexpr int HG = 128;                   // heads per CTA (MMA M)
 constexpr int NK = 32;                    // keys per tile (MMA N of Q K^T)
 constexpr int STAGES = 4;
-constexpr int PF_DIST = 8;                // L2 prefetch distance in tiles
 constexpr int ROWB = D * 2;               // 1152
 constexpr int NCH = ROWB / 16;            // 72 chunks of 16 B per latent row
 constexpr int QT_DIMS = 256;              // Q dims held in TMEM
 constexpr int QS_BLOCKS = (D - QT_DIMS) / 64;   // 5 swizzle blocks of Q in SMEM
 constexpr int NSB = 3;                    // S buffers = Q K^T chains in flight
 constexpr int KV_BLOCKS = D / 64;         // 9 swizzle blocks per KV tile
-constexpr int THREADS = 512;
-constexpr int NSOFT = 8;                  // softmax warps: two per TMEM lane quadrant
+constexpr int THREADS = 384;
 constexpr int NPROD = 128;
 
 // shared memory (offsets from a 1024-byte aligned base)
@@ -64,7 +61,7 @@ constexpr int KV_OFF = QS_OFF + QS_BYTES;
 constexpr int KV_BLOCK_BYTES = NK * 128;               // 4096
 constexpr int KV_STAGE_BYTES = KV_BLOCKS * KV_BLOCK_BYTES;   // 36864
 constexpr int BAR_OFF = KV_OFF + STAGES * KV_STAGE_BYTES;
-constexpr int SMEM_USED = BAR_OFF + 256 + 1024;
+constexpr int SMEM_USED = BAR_OFF + 256;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;           // slack for the 1 KB alignment
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
@@ -76,8 +73,6 @@ static_assert(COL_Q + QT_DIMS / 2 == COL_S && COL_S + NSB * NK == COL_P && COL_P
 // barriers (8-byte words at BAR_OFF)
 enum { B_FULL = 0, B_EMPTY = B_FULL + STAGES, B_SFULL = B_EMPTY + STAGES, B_SFREE = B_SFULL + NSB,
        B_PFULL = B_SFREE + NSB, B_PVDONE = B_PFULL + 2, B_OFULL = B_PVDONE + 2, B_COUNT = B_OFULL + 1 };
-constexpr int LSUM_OFF = BAR_OFF + 256;                // [2][128] float row sums at the end
-static_assert(LSUM_OFF + 1024 + 1024 <= 232448, "row-sum area");
 static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
 
 constexpr int WAIT_LIMIT = 1 << 24;
@@ -163,10 +158,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool v
                "r"(valid ? 16 : 0)
                : "memory");
 }
-// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
@@ -195,9 +186,6 @@ __device__ __forceinline__ void cp_async_wait() {
         "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),   \
         "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),   \
         "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]))
-#define TMEM_ST8(taddr, r)                                                                     \
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr), \
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]))
 #define TMEM_ST16(taddr, r)                                                                    \
   asm volatile(                                                                                \
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12," \
@@ -252,10 +240,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < NSB; ++b) {
       bar_init(bar(B_SFULL + b), 1);
-      bar_init(bar(B_SFREE + b), NSOFT);
+      bar_init(bar(B_SFREE + b), 4);
     }
     for (int b = 0; b < 2; ++b) {
-      bar_init(bar(B_PFULL + b), NSOFT);
+      bar_init(bar(B_PFULL + b), 4);
       bar_init(bar(B_PVDONE + b), 1);
     }
     bar_init(bar(B_OFULL), 1);
@@ -310,9 +298,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   bool timed_out = false;
 
-  if (warp >= 8 && warp < 12) {
+  if (warp >= 4 && warp < 8) {
     // ------------------------------------------------ gather producers ----
-    const int p = tid - 256;          // 0..127
+    const int p = tid - 128;          // 0..127
     const int key = p >> 2;           // 32 keys per tile, 4 threads per key
     const int sub = p & 3;            // chunks sub, sub+4, ..., 18 per thread
     // this thread's key index for tiles t and t+1 is loaded two tiles ahead so
@@ -322,23 +310,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       return (t < T && j < K) ? __ldg(idx_row + j) : -1;
     };
     int32_t id0 = load_id(0), id1 = load_id(1);
-    // rows of tile t + PF_DIST are prefetched into L2 while tile t is issued,
-    // so the copy into a freed stage hits L2 instead of waiting on DRAM
-    int32_t pf0 = load_id(PF_DIST), pf1 = load_id(PF_DIST + 1);
-    if (sub == 0) {
-      for (int t = 0; t < PF_DIST && t < T; ++t) {
-        const int32_t id = load_id(t);
-        if (id >= 0 && id < n_kv) prefetch_l2(kv + (int64_t)id * ROWB, ROWB);
-      }
-    }
     for (int t = 0; t < T && !timed_out; ++t) {
       const int st = t % STAGES;
       const int32_t id = id0;
       id0 = id1;
       id1 = load_id(t + 2);
-      if (sub == 0 && pf0 >= 0 && pf0 < n_kv) prefetch_l2(kv + (int64_t)pf0 * ROWB, ROWB);
-      pf0 = pf1;
-      pf1 = load_id(t + PF_DIST + 2);
       if (t >= STAGES && !bar_wait(bar(B_EMPTY + st), ((t / STAGES) - 1) & 1)) {
         timed_out = true;
         break;
@@ -357,13 +333,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                    : "memory");
     }
     cp_async_wait<0>();
-  } else if (warp >= 12 && warp < 12 + NSB) {
+  } else if (warp >= 8 && warp < 8 + NSB) {
     // ------------------------------------------ Q K^T issuers (3 warps) ----
-    // warp 12 + b issues tiles t = b, b + 3, ... into S buffer b, so three
+    // warp 8 + b issues tiles t = b, b + 3, ... into S buffer b, so three
     // 36-instruction chains are in flight at once
     if (lane == 0) {
       const uint32_t kv0 = sbase + KV_OFF, qs0 = sbase + QS_OFF;
-      const int sb = warp - 12;
+      const int sb = warp - 8;
       bool ok = true;
       for (int t = sb; t < T && ok; t += NSB) {
         const int st = t % STAGES;
@@ -389,7 +365,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       timed_out = !ok;
     }
-  } else if (warp == 12 + NSB) {
+  } else if (warp == 8 + NSB) {
     // --------------------------------------------------- P V issuer ----
     if (lane == 0) {
       const uint32_t kv0 = sbase + KV_OFF;
@@ -411,15 +387,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       timed_out = !ok;
     }
   } else {
-    // ---------------------------------------------- softmax (warps 0-7) ----
-    // warps q and q + 4 share TMEM lanes 32q..32q+31 (heads); both load all 32
-    // scores of a tile and take the same max / rescale decision, then warp
-    // half hf = 0 / 1 handles keys 16 hf .. 16 hf + 15 and O columns
-    // 128 hf .. 128 hf + 127
-    const int quad = warp & 3, hf = warp >> 2;
-    const int hrow = quad * 32 + lane;             // head row = TMEM lane
-    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    // ---------------------------------------------- softmax (warps 0-3) ----
+    const int hrow = tid;                          // head row = TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     float m_used = -INFINITY, l = 0.f;
+    // index of key `lane` of tile t, loaded a tile ahead
     auto load_id = [&](int t) -> int32_t {
       return (t < T && t * NK + lane < K) ? __ldg(idx_row + t * NK + lane) : -1;
     };
@@ -459,38 +431,33 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_after();
         const float alpha = need_o ? ex2(m_used - mt) : 1.0f;
 #pragma unroll 1
-        for (int part = 0; part < 128 / 32; ++part) {
+        for (int part = 0; part < 256 / 32; ++part) {
           uint32_t o[32];
-          const uint32_t col = COL_O + hf * 128 + part * 32;
-          TMEM_LD32(lane_base + col, o);
+          TMEM_LD32(lane_base + COL_O + part * 32, o);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-          TMEM_ST32(lane_base + col, o);
+          TMEM_ST32(lane_base + COL_O + part * 32, o);
         }
         tmem_wait_st();
         if (need_o) l *= alpha;
       }
       if (grow) m_used = mt;
 
-      // P = exp2(s * scale - m) for this warp's 16 keys, as bf16 pairs into P
-      // buffer pb once P V(t-2) has finished with it
+      // P = exp2(s * scale - m) as bf16 into P buffer pb (P V reads it from
+      // TMEM as its A operand) once P V(t-2) has finished with that buffer
       if (t >= 2 && !warp_wait(bar(B_PVDONE + pb), ((t >> 1) - 1) & 1)) { timed_out = true; break; }
       const float mu = (m_used == -INFINITY) ? 0.f : m_used;
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[NK / 4];
-      uint32_t mine[NK / 2];                      // this warp's 16 keys (static indices)
 #pragma unroll
-      for (int k = 0; k < NK / 2; ++k) mine[k] = hf ? sr[NK / 2 + k] : sr[k];
-#pragma unroll
-      for (int k = 0; k < NK / 4; ++k) {
-        const float a = ex2(fmaf(__uint_as_float(mine[2 * k]), scale_log2, -mu));
-        const float b = ex2(fmaf(__uint_as_float(mine[2 * k + 1]), scale_log2, -mu));
+      for (int k = 0; k < NK / 2; ++k) {
+        const float a = ex2(fmaf(__uint_as_float(sr[2 * k]), scale_log2, -mu));
+        const float b = ex2(fmaf(__uint_as_float(sr[2 * k + 1]), scale_log2, -mu));
         ps[k & 3] += a + b;
-        pk[k] = pack_bf16(a, b);
+        sr[k] = pack_bf16(a, b);          // in place: pair k of P
       }
       l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      TMEM_ST8(lane_base + COL_P + pb * (NK / 2) + hf * (NK / 4), pk);
+      TMEM_ST16(lane_base + COL_P + pb * (NK / 2), sr);
       tmem_wait_st();
       fence_before();
       __syncwarp();
@@ -498,21 +465,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     // ---------------------------------------------------------- epilogue --
-    // the row sum is split over the two halves: combine through SMEM
-    float *lsum = reinterpret_cast<float *>(sm + LSUM_OFF);
-    lsum[hf * HG + hrow] = l;
-    asm volatile("bar.sync 1, 256;\n" ::: "memory");   // the 8 softmax warps only
-    const float ltot = lsum[hrow] + lsum[HG + hrow];
     const int h = h0 + hrow;
     if (!timed_out && T > 0 && !warp_wait(bar(B_OFULL), 0)) timed_out = true;
     fence_after();
-    const float inv = ltot > 0.f ? 1.0f / ltot : 0.f;
-    __nv_bfloat16 *orow = out + ((int64_t)r * H + (h < H ? h : 0)) * DV + 256 * c + 128 * hf;
+    const float inv = l > 0.f ? 1.0f / l : 0.f;
+    __nv_bfloat16 *orow = out + ((int64_t)r * H + (h < H ? h : 0)) * DV + 256 * c;
 #pragma unroll 1
-    for (int part = 0; part < 128 / 32; ++part) {
+    for (int part = 0; part < 256 / 32; ++part) {
       uint32_t o[32];
       if (T > 0 && !timed_out) {
-        TMEM_LD32(lane_base + COL_O + hf * 128 + part * 32, o);
+        TMEM_LD32(lane_base + COL_O + part * 32, o);
         tmem_wait_ld();
       } else {
 #pragma unroll
@@ -528,8 +490,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                               pack_bf16(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
       }
     }
-    if (lse && c == 0 && hf == 0 && h < H)
-      lse[(int64_t)r * H + h] = ltot > 0.f ? (m_used + log2f(ltot)) * 0.69314718055994530942f : -INFINITY;
+    if (lse && c == 0 && h < H)
+      lse[(int64_t)r * H + h] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
   }
 
   if (timed_out && status) atomicOr(status, 4u);
