@@ -229,7 +229,7 @@ def run_ours(args):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "traffic": _traffic(), "peak_kind": peak_kind,
-                "kernel": "k_attn_mma", "algorithmic_bytes_per_launch": alg_bytes,
+                "kernel": "k_attn_umma", "algorithmic_bytes_per_launch": alg_bytes,
                 "attn_ms": round(t_attn * 1e3, 4),
                 "tensor_floor_ms": round(R * H * K * 2 * (576 + 512) / (peaks["bf16_tflops"] * 1e12)
                                          * 1e3, 4)}
@@ -373,7 +373,7 @@ def run_swap_bench(hs, dev, args):
             "cold_step_gbs": round(miss[0] * ROW_BYTES / (swap_ms[0] * 1e-3) / 1e9, 2),
             "attn_ms_per_step_mean": round(statistics.mean(attn_ms[1:]), 4),
             "query_rows_per_s_attention": round(cfg.R / (statistics.mean(attn_ms[1:]) * 1e-3), 1),
-            "status": st, "gpu_launches_per_step": 6}
+            "status": st, "gpu_launches_per_step": 4}
 
 
 def cpu_baseline(cfg, rc, budget_s: float = 12.0):
@@ -460,11 +460,18 @@ def main():
     ap.add_argument("--skip-swap", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.0)
+    ap.add_argument("--swap-only", action="store_true",
+                    help="run only the host-backed swap-in section and print its JSON")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.swap_only:
+        import hisparse_top_sparse_gb300 as hs
+        from hisparse_top_sparse_gb300 import _build
+        _build.build()
+        print(json.dumps(run_swap_bench(hs, torch.device("cuda", 0), args)))
     else:
         run_ours(args)
 

@@ -11,6 +11,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "hs_internal.cuh"
 
 static thread_local char g_err[512] = "no error";
@@ -46,23 +48,29 @@ int hs_check_buffer(const hs_buffer *buf) {
 
 static void free_buffer(hs_buffer *b) {
   if (!b) return;
-  void *ptrs[] = {b->token_slot, b->slot_token, b->slot_ts,  b->pos_mark,
-                  b->slot_mark,  b->req_mark,   b->fail_mark, b->counters,
-                  b->miss_list,  b->copy_src,   b->copy_dst, b->pred,
-                  b->status};
+  void *ptrs[] = {b->token_slot, b->slot_token, b->slot_ts, b->lru_order, b->pos_mark,
+                  b->copy_desc,  b->copy_cnt,   b->pred,    b->status};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   free(b);
 }
 
+// Every request starts with all slots empty (ts = -1): LRU order = slot order.
+__global__ void k_order_init(int32_t *order, int32_t S, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    order[i] = (int32_t)(i % S);
+}
+
 extern "C" int hs_buffer_create(const hs_buffer_desc *d, hs_buffer **out) {
   if (!d || !out) return hs_set_error(HS_ERR_INVALID_ARG, "desc/out is NULL");
   *out = nullptr;
-  if (d->max_reqs < 1 || d->slots_per_req < 1 || d->slots_per_req > HS_MAX_SLOTS ||
+  if (d->max_reqs < 1 || d->max_reqs > HS_MAX_REQS || d->slots_per_req < 1 ||
+      d->slots_per_req > HS_MAX_SLOTS ||
       d->step_slots < 1 || d->step_slots > HS_MAX_STEP || d->max_ctx < 1 ||
       d->block_size < 1 || d->host_pool_rows < 1)
     return hs_set_error(HS_ERR_INVALID_ARG,
-                        "bad sizes: max_reqs=%d S=%d (1..%d) step_slots=%d (1..%d) "
+                        "bad sizes: max_reqs=%d (1..16384) S=%d (1..%d) step_slots=%d (1..%d) "
                         "max_ctx=%d block_size=%d host_pool_rows=%lld",
                         d->max_reqs, d->slots_per_req, HS_MAX_SLOTS, d->step_slots,
                         HS_MAX_STEP, d->max_ctx, d->block_size,
@@ -113,14 +121,10 @@ extern "C" int hs_buffer_create(const hs_buffer_desc *d, hs_buffer **out) {
       {(void **)&b->token_slot, R * C * 4, 0xFF},
       {(void **)&b->slot_token, R * S * 4, 0xFF},
       {(void **)&b->slot_ts, R * S * 8, 0xFF},
+      {(void **)&b->lru_order, R * S * 4, 0},
       {(void **)&b->pos_mark, R * C * 4, 0},
-      {(void **)&b->slot_mark, R * S * 4, 0},
-      {(void **)&b->req_mark, R * 4, 0},
-      {(void **)&b->fail_mark, R * 4, 0},
-      {(void **)&b->counters, (2 * R + 1) * 4, 0},
-      {(void **)&b->miss_list, R * S * 4, 0},
-      {(void **)&b->copy_src, R * S * 8, 0},
-      {(void **)&b->copy_dst, R * S * 4, 0},
+      {(void **)&b->copy_desc, R * S * 8, 0},
+      {(void **)&b->copy_cnt, R * 4, 0},
       {(void **)&b->pred, R * (size_t)d->step_slots * 4, 0},
       {(void **)&b->status, 4, 0},
   };
@@ -133,7 +137,10 @@ extern "C" int hs_buffer_create(const hs_buffer_desc *d, hs_buffer **out) {
                           e.bytes, cudaGetErrorString(err));
     }
   }
-  cudaError_t err = cudaDeviceSynchronize();
+  k_order_init<<<(int)std::min<size_t>(R * S / 256 + 1, 65535), 256>>>(b->lru_order, b->S,
+                                                                        (int64_t)R * S);
+  cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) err = cudaDeviceSynchronize();
   if (err != cudaSuccess) {
     free_buffer(b);
     return hs_set_error(HS_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(err));
@@ -150,13 +157,14 @@ extern "C" int hs_buffer_destroy(hs_buffer *buf) {
 extern "C" int64_t hs_buffer_clock(const hs_buffer *buf) { return buf ? buf->clock : -1; }
 
 __global__ void k_request_reset(int32_t *token_slot, int32_t *slot_token, int64_t *slot_ts,
-                                int32_t S, int32_t max_ctx, int32_t req) {
+                                int32_t *order, int32_t S, int32_t max_ctx, int32_t req) {
   for (int s = threadIdx.x; s < S; s += blockDim.x) {
     int64_t k = (int64_t)req * S + s;
     int32_t t = slot_token[k];
     if (t >= 0 && t < max_ctx) token_slot[(int64_t)req * max_ctx + t] = -1;
     slot_token[k] = -1;
     slot_ts[k] = -1;
+    order[k] = s;      // all empty: slot order
   }
 }
 
@@ -166,7 +174,7 @@ extern "C" int hs_request_reset(hs_buffer *buf, int32_t req, hs_stream_t stream)
   if (req < 0 || req >= buf->max_reqs)
     return hs_set_error(HS_ERR_INVALID_ARG, "req %d outside [0, %d)", req, buf->max_reqs);
   k_request_reset<<<1, 1024, 0, stream>>>(buf->token_slot, buf->slot_token, buf->slot_ts,
-                                          buf->S, buf->max_ctx, req);
+                                          buf->lru_order, buf->S, buf->max_ctx, req);
   HS_LAUNCH_CHECK("k_request_reset");
   return HS_OK;
 }

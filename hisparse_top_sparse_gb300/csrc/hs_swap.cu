@@ -7,30 +7,33 @@
 // device buffer of LRU slots per request, the slot -> position and position ->
 // slot maps, and the host pool that holds every position's KV.
 //
-// One call = five launches on the caller's stream:
-//   k_swap_begin   zero the per-request need/miss counters and the copy count
-//   k_swap_probe   warp per 32 entries of a row: classify, claim each needed
-//                  position once per call (epoch-stamped marks), mark hit slots,
-//                  compact misses with __ballot_sync / __popc into a per-request
-//                  list
-//   k_swap_assign  block per request: capacity check, hit timestamps, sort the
-//                  misses ascending and the unneeded slots by (ts, slot) in
-//                  shared memory (bitonic), pair them in order, update the maps
-//                  and emit (host row, hot row) copy descriptors
-//   k_swap_gather  copy every missed 1152-byte row from the device-mapped
-//                  page-locked host pool with 16-byte loads and stores
-//   k_swap_table   block per row: the hot-row index table and valid counts
+// Two launches. k_swap_request: one 1024-thread block per request that has
+// rows in the call works through that request alone:
+//   probe   every entry of the request's rows: classify it, claim each needed
+//           committed position once per call (epoch-stamped marks), record hit
+//           slots in a shared-memory bitmap, compact misses with
+//           __ballot_sync / __popc into a shared-memory list
+//   assign  capacity check; the victims are the first slots of the request's
+//           LRU order (a persistent array kept in ascending (ts, slot) order)
+//           that hold no needed position (one block prefix scan); the misses,
+//           sorted ascending (bitonic, shared memory), take them in order; hits
+//           and victims take the current time and move to the end of the order
+//           in slot order (two prefix scans) -- no sort over all S slots
+//   table   the hot-row index of every entry and the valid count of every row
+//   publish (host pool row, hot slot) of every miss
+// k_swap_gather: every SM copies a share of every request's missed 1152-byte
+// rows from the device-mapped page-locked host pool with 16-byte loads (four
+// in flight per thread): reads over the host link need requests in flight
+// from all SMs to reach the link's bandwidth.
+// Rows are found by scanning the row descriptors, 1024 rows of the request at
+// a time.
 
 #include "hs_internal.cuh"
 
 namespace {
 
-constexpr int kWarpsPerBlock = 8;
-
-__global__ void k_swap_begin(int32_t *counters, int32_t n) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
-    counters[i] = 0;
-}
+constexpr int SW_THREADS = 1024;
+constexpr int ROW_CHUNK = 1024;   // rows of one request handled per pass
 
 struct SwapArgs {
   const int32_t *req_id, *clen, *kv_len, *topk;
@@ -39,63 +42,18 @@ struct SwapArgs {
   const int32_t *hbt;
   int32_t *token_slot, *slot_token;
   int64_t *slot_ts;
-  uint32_t *pos_mark, *slot_mark, *req_mark, *fail_mark;
-  int32_t *need_cnt, *miss_cnt, *copy_cnt;
-  int32_t *miss_list;
-  int64_t *copy_src;
-  int32_t *copy_dst;
+  int32_t *lru_order;
+  uint32_t *pos_mark;
+  uint64_t *copy_desc;
+  int32_t *copy_cnt;
+  const uint4 *pool;
+  int64_t pool_rows;
+  uint4 *hot;
   int64_t *stats;
   uint32_t *status;
   uint32_t epoch;
   int64_t now;
 };
-
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) k_swap_probe(SwapArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int chunks = (a.K + 31) / 32;
-  const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (gw >= (int64_t)a.R * chunks) return;
-  const int r = (int)(gw / chunks);
-  const int j = (int)(gw % chunks) * 32 + lane;
-  const int32_t b = a.req_id[r];
-  if (b < 0 || b >= a.max_reqs) {
-    if (lane == 0) atomicOr(a.status, HS_STATUS_INDEX);
-    return;
-  }
-  const int32_t n = a.clen[r];
-  const int32_t L = a.kv_len[b];
-  const int32_t t = (j < a.K) ? a.topk[(int64_t)r * a.K + j] : -1;
-  const bool in_range = t >= 0 && t < n;
-  const bool bad = (t >= 0 && t >= n) || (t >= 0 && t < L && t >= a.max_ctx);
-  if (__ballot_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.status, HS_STATUS_INDEX);
-  if (lane == 0) a.req_mark[b] = a.epoch;
-  const bool committed = in_range && t < L && t < a.max_ctx;
-
-  // claim: the first thread to stamp a position in this call owns it
-  bool first = false;
-  int32_t s = -1;
-  if (committed) {
-    const uint32_t old = atomicExch(&a.pos_mark[(int64_t)b * a.max_ctx + t], a.epoch);
-    first = (old != a.epoch);
-    if (first) {
-      s = a.token_slot[(int64_t)b * a.max_ctx + t];
-      if (s >= 0) a.slot_mark[(int64_t)b * a.S + s] = a.epoch;   // hit: protect slot
-    }
-  }
-  const unsigned first_mask = __ballot_sync(0xffffffffu, first);
-  const bool miss = first && s < 0;
-  const unsigned miss_mask = __ballot_sync(0xffffffffu, miss);
-  int base = 0;
-  if (lane == 0) {
-    if (first_mask) atomicAdd(&a.need_cnt[b], __popc(first_mask));
-    if (miss_mask) base = atomicAdd(&a.miss_cnt[b], __popc(miss_mask));
-  }
-  base = __shfl_sync(0xffffffffu, base, 0);
-  if (miss) {
-    const int pos = base + __popc(miss_mask & ((1u << lane) - 1u));
-    if (pos < a.S) a.miss_list[(int64_t)b * a.S + pos] = t;   // beyond S: overflow, refused later
-  }
-}
 
 // In-place ascending bitonic sort of n (a power of two) keys in shared memory.
 template <typename T>
@@ -115,135 +73,219 @@ __device__ void block_bitonic_sort(T *keys, int n) {
   }
 }
 
-__device__ __forceinline__ int pow2_ceil(int x) {
+__host__ __device__ inline int pow2_ceil(int x) {
   int p = 1;
   while (p < x) p <<= 1;
   return p;
 }
 
-// Victim key: (ts + 1) in the high bits, slot in the low 16; needed slots sort last.
-__global__ void __launch_bounds__(1024) k_swap_assign(SwapArgs a) {
+// Shared-memory layout (bytes): mkey[nS] i32 (misses, sorted) | ord[S] i32
+// (LRU order) | vict[S] i32 (victim slots) | hit / touched bitmap [S/32] u32 |
+// rows[ROW_CHUNK] i32 | row valid counts [ROW_CHUNK] i32
+__host__ __device__ inline size_t swap_smem_bytes(int S) {
+  const int nS = pow2_ceil(S);
+  return (size_t)nS * 4 + (size_t)S * 8 + (size_t)((S + 31) / 32) * 4 + ROW_CHUNK * 8;
+}
+
+__device__ __forceinline__ bool bit_of(const uint32_t *bm, int s) { return (bm[s >> 5] >> (s & 31)) & 1u; }
+
+// Rows of request b among rows [from, R): fills rows[] with up to ROW_CHUNK of
+// them (in row order) and returns the count and the next scan position.
+__device__ int collect_rows(const SwapArgs &a, int b, int from, int *rows, int *next, int *s_cnt) {
+  if (threadIdx.x == 0) *s_cnt = 0;
+  __syncthreads();
+  int r = from;
+  for (; r < a.R; r += SW_THREADS) {
+    const int rr = r + (int)threadIdx.x;
+    const bool mine = rr < a.R && a.req_id[rr] == b;
+    const unsigned m = __ballot_sync(0xffffffffu, mine);
+    __shared__ int warp_base[SW_THREADS / 32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (lane == 0) warp_base[w] = __popc(m);
+    __syncthreads();
+    // exclusive prefix over warps, in row order
+    __shared__ int total;
+    if (threadIdx.x == 0) {
+      int acc = *s_cnt;
+      for (int i = 0; i < SW_THREADS / 32; ++i) {
+        const int c = warp_base[i];
+        warp_base[i] = acc;
+        acc += c;
+      }
+      total = acc;
+    }
+    __syncthreads();
+    if (mine) {
+      const int pos = warp_base[w] + __popc(m & ((1u << lane) - 1u));
+      if (pos < ROW_CHUNK) rows[pos] = rr;
+    }
+    __syncthreads();
+    const int t = total;
+    if (threadIdx.x == 0) *s_cnt = t < ROW_CHUNK ? t : ROW_CHUNK;
+    __syncthreads();
+    if (t >= ROW_CHUNK) {
+      // the chunk is full: resume after the last row placed in it
+      r = rows[ROW_CHUNK - 1] + 1;
+      *next = r;
+      return ROW_CHUNK;
+    }
+  }
+  *next = a.R;
+  return *s_cnt;
+}
+
+__global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
+                                                                 int32_t *__restrict__ out,
+                                                                 int32_t *__restrict__ out_valid) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int b = blockIdx.x;
-  if (a.req_mark[b] != a.epoch) return;
-  const int need = a.need_cnt[b];
-  const int nm = a.miss_cnt[b];
-  const int64_t sbase = (int64_t)b * a.S;
-  if (need > a.S) {  // refused: nothing about this request changes
-    if (threadIdx.x == 0) {
-      atomicOr(a.status, HS_STATUS_CAPACITY);
-      a.fail_mark[b] = a.epoch;
-    }
-    return;
-  }
-  if (threadIdx.x == 0 && a.stats) {
-    atomicAdd((unsigned long long *)&a.stats[0], (unsigned long long)(need - nm));
-    atomicAdd((unsigned long long *)&a.stats[1], (unsigned long long)nm);
-  }
-  // hits take the current time
-  for (int s = threadIdx.x; s < a.S; s += blockDim.x)
-    if (a.slot_mark[sbase + s] == a.epoch) a.slot_ts[sbase + s] = a.now;
-  if (nm == 0) return;
-
   const int nS = pow2_ceil(a.S);
-  const int nM = pow2_ceil(nm);
-  uint64_t *vkey = reinterpret_cast<uint64_t *>(smem);
-  int32_t *mkey = reinterpret_cast<int32_t *>(smem + (size_t)nS * sizeof(uint64_t));
-  __shared__ int copy_base;
-  for (int s = threadIdx.x; s < nS; s += blockDim.x) {
-    uint64_t key = ~0ull;
-    if (s < a.S && a.slot_mark[sbase + s] != a.epoch)
-      key = ((uint64_t)(a.slot_ts[sbase + s] + 1) << 16) | (uint64_t)s;
-    vkey[s] = key;
-  }
-  for (int i = threadIdx.x; i < nM; i += blockDim.x)
-    mkey[i] = (i < nm) ? a.miss_list[sbase + i] : INT32_MAX;
-  if (threadIdx.x == 0) copy_base = atomicAdd(a.copy_cnt, nm);
+  int32_t *mkey = reinterpret_cast<int32_t *>(smem);
+  int32_t *ord = mkey + nS;
+  int32_t *vict = ord + a.S;
+  uint32_t *hitmap = reinterpret_cast<uint32_t *>(vict + a.S);
+  int32_t *rows = reinterpret_cast<int32_t *>(hitmap + (a.S + 31) / 32);
+  int32_t *rvalid = rows + ROW_CHUNK;
+  __shared__ int s_need, s_miss, s_cnt, s_any, s_bad;
+  __shared__ int scan_tmp[33];
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) { s_need = 0; s_miss = 0; s_any = 0; s_bad = 0; a.copy_cnt[b] = 0; }
+  for (int i = threadIdx.x; i < (a.S + 31) / 32; i += SW_THREADS) hitmap[i] = 0u;
   __syncthreads();
-  block_bitonic_sort(mkey, nM);
-  block_bitonic_sort(vkey, nS);
 
+  const int32_t L = a.kv_len[b];
   const int64_t cbase = (int64_t)b * a.max_ctx;
-  const int32_t *hbt_row = a.hbt + (int64_t)b * a.hbt_stride;
-  for (int i = threadIdx.x; i < nm; i += blockDim.x) {
-    const int32_t t = mkey[i];
-    if (vkey[i] == ~0ull) {   // fewer victims than misses: the maps are inconsistent
-      atomicOr(a.status, HS_STATUS_CAPACITY);
-      a.copy_src[copy_base + i] = -1;
-      a.copy_dst[copy_base + i] = 0;
-      continue;
-    }
-    const int32_t s = (int32_t)(vkey[i] & 0xFFFF);
-    const int32_t old = a.slot_token[sbase + s];
-    if (old >= 0 && old < a.max_ctx) a.token_slot[cbase + old] = -1;   // not needed now
-    a.slot_token[sbase + s] = t;
-    a.token_slot[cbase + t] = s;
-    a.slot_ts[sbase + s] = a.now;
-    const int32_t hb = hbt_row[t / a.block_size];
-    int64_t src = -1;
-    if (hb >= 0) src = (int64_t)hb * a.block_size + t % a.block_size;
-    else atomicOr(a.status, HS_STATUS_INDEX);
-    a.copy_src[copy_base + i] = src;
-    a.copy_dst[copy_base + i] = b * a.S_tot + s;
-  }
-}
+  const int64_t sbase = (int64_t)b * a.S;
 
-// Flattened (copy, 16-byte chunk) space; four independent 16-byte loads in
-// flight per thread per iteration to cover the host-link latency.
-__global__ void __launch_bounds__(256) k_swap_gather(const int32_t *__restrict__ copy_cnt,
-                                                     const int64_t *__restrict__ copy_src,
-                                                     const int32_t *__restrict__ copy_dst,
-                                                     const uint4 *__restrict__ pool,
-                                                     int64_t pool_rows, uint4 *__restrict__ hot,
-                                                     uint32_t *status) {
-  const int64_t total = (int64_t)(*copy_cnt) * HS_ROW_VEC16;
-  const int64_t step = (int64_t)gridDim.x * blockDim.x;
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  constexpr int U = 4;
-  for (; i < total; i += U * step) {
-    uint4 v[U];
-    int64_t dst[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t k = i + u * step;
-      dst[u] = -1;
-      if (k < total) {
-        const int64_t e = k / HS_ROW_VEC16;
-        const int c = (int)(k - e * HS_ROW_VEC16);
-        const int64_t src = copy_src[e];
-        if (src >= 0 && src < pool_rows) {
-          v[u] = pool[src * HS_ROW_VEC16 + c];
-          dst[u] = (int64_t)copy_dst[e] * HS_ROW_VEC16 + c;
-        } else if (c == 0) {
-          atomicOr(status, HS_STATUS_INDEX);
+  // ---- probe ----------------------------------------------------------------
+  for (int from = 0; from < a.R;) {
+    int next;
+    const int n = collect_rows(a, b, from, rows, &next, &s_cnt);
+    from = next;
+    if (n == 0) break;
+    if (threadIdx.x == 0) s_any = 1;
+    const int items = n * a.K;
+    for (int base = 0; base < items; base += SW_THREADS) {
+      const int i = base + (int)threadIdx.x;
+      int32_t t = -1, clen = 0;
+      if (i < items) {
+        const int row = rows[i / a.K];
+        t = a.topk[(int64_t)row * a.K + i % a.K];
+        clen = a.clen[row];
+      }
+      const bool bad = t >= 0 && (t >= clen || (t < L && t >= a.max_ctx));
+      const bool committed = t >= 0 && t < clen && t < L && t < a.max_ctx;
+      bool first = false;
+      int32_t s = -1;
+      if (committed) {
+        first = atomicExch(&a.pos_mark[cbase + t], a.epoch) != a.epoch;
+        if (first) {
+          s = a.token_slot[cbase + t];
+          if (s >= 0 && s < a.S) atomicOr(&hitmap[s >> 5], 1u << (s & 31));
         }
       }
+      const unsigned bad_mask = __ballot_sync(0xffffffffu, bad);
+      const unsigned first_mask = __ballot_sync(0xffffffffu, first);
+      const unsigned miss_mask = __ballot_sync(0xffffffffu, first && s < 0);
+      int mbase = 0;
+      if (lane == 0) {
+        if (bad_mask) s_bad = 1;
+        if (first_mask) atomicAdd(&s_need, __popc(first_mask));
+        if (miss_mask) mbase = atomicAdd(&s_miss, __popc(miss_mask));
+      }
+      mbase = __shfl_sync(0xffffffffu, mbase, 0);
+      if (first && s < 0) {
+        const int pos = mbase + __popc(miss_mask & ((1u << lane) - 1u));
+        if (pos < a.S) mkey[pos] = t;   // beyond S the request is refused below
+      }
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (dst[u] >= 0) hot[dst[u]] = v[u];
+    __syncthreads();
   }
-}
+  __syncthreads();
+  if (!s_any) return;                    // no rows of this request in the call
+  if (threadIdx.x == 0 && s_bad) atomicOr(a.status, HS_STATUS_INDEX);
 
-__global__ void __launch_bounds__(256) k_swap_table(SwapArgs a, int32_t *__restrict__ out,
-                                                    int32_t *__restrict__ out_valid) {
-  const int r = blockIdx.x;
-  const int32_t b = a.req_id[r];
-  int32_t *o = out + (int64_t)r * a.K;
-  const int32_t *tk = a.topk + (int64_t)r * a.K;
-  int cnt = 0;
-  if (b < 0 || b >= a.max_reqs) {
-    for (int j = threadIdx.x; j < a.K; j += blockDim.x) o[j] = -1;
+  // ---- assign ---------------------------------------------------------------
+  const int need = s_need, nm = s_miss;
+  const bool failed = need > a.S;
+  if (failed) {
+    if (threadIdx.x == 0) atomicOr(a.status, HS_STATUS_CAPACITY);
   } else {
-    const int32_t n = a.clen[r];
-    const int32_t L = a.kv_len[b];
-    const bool failed = a.fail_mark[b] == a.epoch;
-    const int32_t row0 = b * a.S_tot;
-    const int32_t *ts_row = a.token_slot + (int64_t)b * a.max_ctx;
-    for (int j = threadIdx.x; j < a.K; j += blockDim.x) {
-      const int32_t t = tk[j];
+    if (threadIdx.x == 0 && a.stats) {
+      atomicAdd((unsigned long long *)&a.stats[0], (unsigned long long)(need - nm));
+      atomicAdd((unsigned long long *)&a.stats[1], (unsigned long long)nm);
+    }
+    // victims: the first nm slots of the LRU order (ascending (ts, slot)) that
+    // hold no position needed in this call
+    int32_t *lru = a.lru_order + sbase;
+    for (int i = threadIdx.x; i < a.S; i += SW_THREADS) ord[i] = lru[i];
+    __syncthreads();
+    {
+      const int E = (a.S + SW_THREADS - 1) / SW_THREADS;
+      const int lo = threadIdx.x * E, hi = min(a.S, lo + E);
+      int cnt = 0;
+      for (int i = lo; i < hi; ++i) cnt += !bit_of(hitmap, ord[i]);
+      int tot;
+      int k = hs_block_exscan(cnt, scan_tmp, &tot);
+      for (int i = lo; i < hi && k < nm; ++i)
+        if (!bit_of(hitmap, ord[i])) vict[k++] = ord[i];
+    }
+    __syncthreads();
+    // hits and victims take the current time; the LRU order moves them last
+    for (int i = threadIdx.x; i < nm; i += SW_THREADS)
+      atomicOr(&hitmap[vict[i] >> 5], 1u << (vict[i] & 31));
+    __syncthreads();
+    hs_lru_reorder(ord, hitmap, a.S, lru, scan_tmp);
+    for (int sl = threadIdx.x; sl < a.S; sl += SW_THREADS)
+      if (bit_of(hitmap, sl)) a.slot_ts[sbase + sl] = a.now;
+    if (nm > 0) {
+      // misses in ascending position order take the victims in order
+      const int nM = pow2_ceil(nm);
+      for (int i = nm + threadIdx.x; i < nM; i += SW_THREADS) mkey[i] = INT32_MAX;
+      __syncthreads();
+      block_bitonic_sort(mkey, nM);
+      const int32_t *hbt_row = a.hbt + (int64_t)b * a.hbt_stride;
+      uint64_t *desc = a.copy_desc + sbase;
+      for (int i = threadIdx.x; i < nm; i += SW_THREADS) {
+        const int32_t t = mkey[i];
+        const int32_t sl = vict[i];
+        const int32_t old = a.slot_token[sbase + sl];
+        if (old >= 0 && old < a.max_ctx) a.token_slot[cbase + old] = -1;   // not needed now
+        a.slot_token[sbase + sl] = t;
+        a.token_slot[cbase + t] = sl;
+        const int32_t hb = hbt_row[t / a.block_size];
+        const int64_t src = (int64_t)hb * a.block_size + t % a.block_size;
+        uint64_t copy = ~0ull;
+        if (hb >= 0 && src < a.pool_rows)
+          copy = ((uint64_t)src << 16) | (uint64_t)sl;   // host row, hot slot
+        else
+          atomicOr(a.status, HS_STATUS_INDEX);
+        desc[i] = copy;
+      }
+      if (threadIdx.x == 0) a.copy_cnt[b] = nm;      // published for the gather
+    }
+  }
+  __syncthreads();
+
+  // ---- table: hot-row index of every entry, valid count of every row -------
+  const int32_t row0 = b * a.S_tot;
+  const int32_t *ts_row = a.token_slot + cbase;
+  for (int from = 0; from < a.R;) {
+    int next;
+    const int n = collect_rows(a, b, from, rows, &next, &s_cnt);
+    from = next;
+    if (n == 0) break;
+    for (int i = threadIdx.x; i < n; i += SW_THREADS) rvalid[i] = 0;
+    __syncthreads();
+    const int items = n * a.K;
+    for (int i = threadIdx.x; i < items; i += SW_THREADS) {
+      const int ri = (int)(i / a.K);
+      const int row = rows[ri];
+      const int32_t t = a.topk[(int64_t)row * a.K + i % a.K];
+      const int32_t clen = a.clen[row];
       int32_t v = -1;
-      if (t >= 0 && t < n) {
+      if (t >= 0 && t < clen) {
         if (t >= L) {
           if (t - L < a.S_tot - a.S) v = row0 + a.S + (t - L);
         } else if (!failed && t < a.max_ctx) {
@@ -251,20 +293,95 @@ __global__ void __launch_bounds__(256) k_swap_table(SwapArgs a, int32_t *__restr
           if (s >= 0) v = row0 + s;
         }
       }
-      cnt += (v >= 0);
-      o[j] = v;
+      out[(int64_t)row * a.K + i % a.K] = v;
+      if (v >= 0) atomicAdd(&rvalid[ri], 1);
     }
-  }
-  if (out_valid) {
-    __shared__ int ws[8];
-    for (int off = 16; off; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
-    if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = cnt;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int s = 0;
-      for (int w = 0; w < 8; ++w) s += ws[w];
-      out_valid[r] = s;
+    if (out_valid)
+      for (int i = threadIdx.x; i < n; i += SW_THREADS) out_valid[rows[i]] = rvalid[i];
+    __syncthreads();
+  }
+}
+
+// Chunks of every request's misses are numbered consecutively (a prefix sum
+// over the per-request counts, computed by every block in shared memory) and
+// spread over the whole grid, four 16-byte loads in flight per thread.
+__global__ void __launch_bounds__(256) k_swap_gather(const int32_t *__restrict__ copy_cnt,
+                                                     const uint64_t *__restrict__ copy_desc,
+                                                     int32_t max_reqs, int32_t S, int32_t S_tot,
+                                                     const uint4 *__restrict__ pool,
+                                                     uint4 *__restrict__ hot) {
+  extern __shared__ int pre[];                     // [max_reqs + 1] chunk offsets
+  __shared__ int part[256];
+  const int tid = threadIdx.x;
+  const int seg = (max_reqs + 255) / 256;
+  int sum = 0;
+  for (int i = tid * seg; i < (tid + 1) * seg && i < max_reqs; ++i) sum += copy_cnt[i] * HS_ROW_VEC16;
+  part[tid] = sum;
+  __syncthreads();
+  if (tid < 32) {                                  // exclusive scan of the 256 partial sums
+    int v[8], run = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) { v[k] = part[tid * 8 + k]; run += v[k]; }
+    int incl = run;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (tid >= off) incl += o;
     }
+    int acc = incl - run;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) { part[tid * 8 + k] = acc; acc += v[k]; }
+  }
+  __syncthreads();
+  {
+    int acc = part[tid];
+    for (int i = tid * seg; i < (tid + 1) * seg && i < max_reqs; ++i) {
+      pre[i] = acc;
+      acc += copy_cnt[i] * HS_ROW_VEC16;
+    }
+    if (tid == 255) pre[max_reqs] = acc;
+  }
+  __syncthreads();
+  const int total = pre[max_reqs];
+  const int step = gridDim.x * blockDim.x;
+  for (int e = blockIdx.x * blockDim.x + tid; e < total; e += 4 * step) {
+    uint4 v[4];
+    int64_t dst[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = e + u * step;
+      dst[u] = -1;
+      if (k < total) {
+        int lo = 0, hi = max_reqs;                 // request b with pre[b] <= k < pre[b+1]
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (pre[mid] <= k) lo = mid; else hi = mid;
+        }
+        const int rel = k - pre[lo];
+        const int i = rel / HS_ROW_VEC16, c = rel % HS_ROW_VEC16;
+        const uint64_t d = copy_desc[(int64_t)lo * S + i];
+        if (d != ~0ull) {
+          v[u] = pool[(int64_t)(d >> 16) * HS_ROW_VEC16 + c];
+          dst[u] = ((int64_t)lo * S_tot + (int64_t)(d & 0xFFFF)) * HS_ROW_VEC16 + c;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (dst[u] >= 0) hot[dst[u]] = v[u];
+  }
+}
+
+// Rows whose request id is outside the buffer: every entry -1, index status.
+__global__ void k_swap_bad_rows(const int32_t *req_id, int32_t R, int32_t K, int32_t max_reqs,
+                                int32_t *out, int32_t *out_valid, uint32_t *status) {
+  const int r = blockIdx.x;
+  const int32_t b = req_id[r];
+  if (b >= 0 && b < max_reqs) return;
+  for (int j = threadIdx.x; j < K; j += blockDim.x) out[(int64_t)r * K + j] = -1;
+  if (threadIdx.x == 0) {
+    if (out_valid) out_valid[r] = 0;
+    if (K > 0) atomicOr(status, HS_STATUS_INDEX);
   }
 }
 
@@ -276,7 +393,8 @@ extern "C" int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
                           int32_t *out_valid, int64_t *stats, hs_stream_t stream) {
   int rc = hs_check_buffer(buf);
   if (rc) return rc;
-  if (R < 0 || K < 0) return hs_set_error(HS_ERR_INVALID_ARG, "bad sizes R=%d K=%d", R, K);
+  if (R < 0 || K < 0 || K > (1 << 20))
+    return hs_set_error(HS_ERR_INVALID_ARG, "bad sizes R=%d K=%d (0..2^20)", R, K);
   if (R > 0 && (!req_id_per_row || !row_causal_len || !kv_len))
     return hs_set_error(HS_ERR_INVALID_ARG, "NULL row descriptor");
   if (R > 0 && K > 0 && (!topk || !out_slot_idx))
@@ -291,47 +409,40 @@ extern "C" int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
   a.max_reqs = buf->max_reqs; a.S = buf->S; a.S_tot = buf->S_tot; a.max_ctx = buf->max_ctx;
   a.block_size = buf->block_size; a.hbt_stride = buf->hbt_stride; a.hbt = buf->hbt;
   a.token_slot = buf->token_slot; a.slot_token = buf->slot_token; a.slot_ts = buf->slot_ts;
-  a.pos_mark = buf->pos_mark; a.slot_mark = buf->slot_mark; a.req_mark = buf->req_mark;
-  a.fail_mark = buf->fail_mark;
-  a.need_cnt = buf->counters; a.miss_cnt = buf->counters + buf->max_reqs;
-  a.copy_cnt = buf->counters + 2 * buf->max_reqs;
-  a.miss_list = buf->miss_list; a.copy_src = buf->copy_src; a.copy_dst = buf->copy_dst;
+  a.lru_order = buf->lru_order;
+  a.pos_mark = buf->pos_mark;
+  a.copy_desc = buf->copy_desc;
+  a.copy_cnt = buf->copy_cnt;
+  a.pool = reinterpret_cast<const uint4 *>(buf->host_pool);
+  a.pool_rows = buf->host_pool_rows;
+  a.hot = reinterpret_cast<uint4 *>(buf->hot_kv);
   a.stats = stats; a.status = buf->status;
   a.epoch = (uint32_t)buf->clock;
   a.now = buf->clock;
 
-  const int ncnt = 2 * buf->max_reqs + 1;
-  k_swap_begin<<<(ncnt + 255) / 256, 256, 0, stream>>>(buf->counters, ncnt);
-  HS_LAUNCH_CHECK("k_swap_begin");
-  if (K > 0) {
-    const int64_t warps = (int64_t)R * ((K + 31) / 32);
-    const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    if (blocks > INT32_MAX) return hs_set_error(HS_ERR_UNSUPPORTED, "R*K too large");
-    k_swap_probe<<<(int)blocks, kWarpsPerBlock * 32, 0, stream>>>(a);
-    HS_LAUNCH_CHECK("k_swap_probe");
-  }
-  int nS = 1;
-  while (nS < buf->S) nS <<= 1;
-  const size_t smem = (size_t)nS * 8 + (size_t)nS * 4;
+  const size_t smem = swap_smem_bytes(buf->S);
   static bool attr_set[64] = {false};
-  if (buf->device >= 64 || !attr_set[buf->device]) {   // the kernel also has static SMEM
-    HS_CUDA_TRY(cudaFuncSetAttribute(k_swap_assign, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)(HS_MAX_SLOTS * 12)));
+  if (buf->device >= 64 || !attr_set[buf->device]) {
+    HS_CUDA_TRY(cudaFuncSetAttribute(k_swap_request, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)swap_smem_bytes(HS_MAX_SLOTS)));
+    HS_CUDA_TRY(cudaFuncSetAttribute(k_swap_gather, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)((HS_MAX_REQS + 1) * sizeof(int))));
     if (buf->device < 64) attr_set[buf->device] = true;
   }
-  k_swap_assign<<<buf->max_reqs, 1024, smem, stream>>>(a);
-  HS_LAUNCH_CHECK("k_swap_assign");
-  int dev_sms = 152;
-  cudaDeviceGetAttribute(&dev_sms, cudaDevAttrMultiProcessorCount, buf->device);
-  k_swap_gather<<<dev_sms * 8, 256, 0, stream>>>(
-      a.copy_cnt, buf->copy_src, buf->copy_dst, reinterpret_cast<const uint4 *>(buf->host_pool),
-      buf->host_pool_rows, reinterpret_cast<uint4 *>(buf->hot_kv), buf->status);
-  HS_LAUNCH_CHECK("k_swap_gather");
-  if (K > 0) {
-    k_swap_table<<<R, 256, 0, stream>>>(a, out_slot_idx, out_valid);
-    HS_LAUNCH_CHECK("k_swap_table");
-  } else if (out_valid) {
-    HS_CUDA_TRY(cudaMemsetAsync(out_valid, 0, (size_t)R * 4, stream));
+  k_swap_request<<<buf->max_reqs, SW_THREADS, smem, stream>>>(a, out_slot_idx, out_valid);
+  HS_LAUNCH_CHECK("k_swap_request");
+  static int sms[64] = {0};
+  int nsm = (buf->device < 64) ? sms[buf->device] : 0;
+  if (nsm == 0) {
+    HS_CUDA_TRY(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, buf->device));
+    if (buf->device < 64) sms[buf->device] = nsm;
   }
+  const size_t gsmem = (size_t)(buf->max_reqs + 1) * sizeof(int);
+  k_swap_gather<<<nsm * 8, 256, gsmem, stream>>>(buf->copy_cnt, buf->copy_desc, buf->max_reqs,
+                                                 buf->S, buf->S_tot, a.pool, a.hot);
+  HS_LAUNCH_CHECK("k_swap_gather");
+  k_swap_bad_rows<<<R, 128, 0, stream>>>(req_id_per_row, R, K, buf->max_reqs, out_slot_idx,
+                                         out_valid, buf->status);
+  HS_LAUNCH_CHECK("k_swap_bad_rows");
   return HS_OK;
 }

@@ -13,8 +13,8 @@
 //                    vocabulary with 16-byte loads, ties to the lowest index
 //   k_verify_commit  block per request: accepted length, next token, host-pool
 //                    write of the kept rows through the mapped pool, LRU slot
-//                    choice (m+1 rounds of a block-wide min over (ts, slot)),
-//                    hot-slot write and the kv_len update
+//                    choice (the head of the request's (ts, slot) order, which
+//                    is then rotated), hot-slot write and the kv_len update
 
 #include <float.h>
 
@@ -100,11 +100,11 @@ __global__ void __launch_bounds__(256) k_verify_commit(
     int32_t *kv_len, int32_t *accept_len, int32_t *next_token, int32_t max_reqs, int32_t S,
     int32_t S_tot, int32_t n_step, int32_t max_ctx, int32_t block_size, int32_t hbt_stride,
     const int32_t *__restrict__ hbt, int64_t pool_rows, uint4 *pool, uint4 *hot,
-    int32_t *token_slot, int32_t *slot_token, int64_t *slot_ts, uint32_t *status, int64_t now) {
+    int32_t *token_slot, int32_t *slot_token, int64_t *slot_ts, int32_t *lru_order,
+    uint32_t *status, int64_t now) {
   const int b = blockIdx.x;
   __shared__ int sm_m, sm_L, sm_ok;
   __shared__ int32_t chosen[HS_MAX_STEP];
-  __shared__ uint64_t wmin[8];
   const int32_t req = req_ids ? req_ids[b] : b;
   if (threadIdx.x == 0) {
     const int32_t *p = pred + (int64_t)b * n_step;
@@ -131,30 +131,27 @@ __global__ void __launch_bounds__(256) k_verify_commit(
   const int n = sm_m + 1, L = sm_L;
   const int64_t sbase = (int64_t)req * S;
 
-  // n rounds of a block-wide minimum over (ts + 1, slot): the LRU order with
-  // no protected slot. Keys of slots already chosen are skipped.
-  for (int k = 0; k < n; ++k) {
-    uint64_t best = ~0ull;
-    for (int s = threadIdx.x; s < S; s += blockDim.x) {
-      bool used = false;
-      for (int q = 0; q < k; ++q) used |= (chosen[q] == s);
-      if (!used) {
-        const uint64_t key = ((uint64_t)(slot_ts[sbase + s] + 1) << 16) | (uint64_t)s;
-        best = key < best ? key : best;
-      }
+  // The victims are the first n slots of the LRU order (ascending (ts, slot),
+  // nothing protected). They take the current time, so the new order is the
+  // rest of the order followed by the victims in slot order.
+  extern __shared__ int32_t ord[];                 // [S]
+  int32_t *lru = lru_order + sbase;
+  for (int i = threadIdx.x; i < S; i += blockDim.x) ord[i] = lru[i];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < n; ++k) chosen[k] = ord[k];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < S - n; i += blockDim.x) lru[i] = ord[n + i];
+  if (threadIdx.x == 0) {
+    int32_t sorted[HS_MAX_STEP];
+    for (int k = 0; k < n; ++k) {               // insertion sort of at most 16 slots
+      int32_t v = chosen[k];
+      int j = k;
+      while (j > 0 && sorted[j - 1] > v) { sorted[j] = sorted[j - 1]; --j; }
+      sorted[j] = v;
     }
-    for (int off = 16; off; off >>= 1) {
-      const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
-      best = o < best ? o : best;
-    }
-    if ((threadIdx.x & 31) == 0) wmin[threadIdx.x >> 5] = best;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      uint64_t m = wmin[0];
-      for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = wmin[w] < m ? wmin[w] : m;
-      chosen[k] = (int32_t)(m & 0xFFFF);
-    }
-    __syncthreads();
+    for (int k = 0; k < n; ++k) lru[S - n + k] = sorted[k];
   }
 
   // map updates (one thread per kept position)
@@ -209,13 +206,13 @@ extern "C" int hs_verify_finalize(hs_buffer *buf, const void *logits, int32_t lo
     k_verify_argmax<HS_LOGITS_BF16><<<rows, 512, 0, stream>>>(logits, V, d + 1, buf->n_step,
                                                               buf->pred);
   HS_LAUNCH_CHECK("k_verify_argmax");
-  k_verify_commit<<<B, 256, 0, stream>>>(
+  k_verify_commit<<<B, 256, (size_t)buf->S * sizeof(int32_t), stream>>>(
       d, draft_tokens, buf->pred, reinterpret_cast<const uint4 *>(step_kv), req_ids, kv_len,
       accept_len, next_token, buf->max_reqs, buf->S, buf->S_tot, buf->n_step, buf->max_ctx,
       buf->block_size, buf->hbt_stride, buf->hbt, buf->host_pool_rows,
       reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(buf->host_pool)),
       reinterpret_cast<uint4 *>(buf->hot_kv), buf->token_slot, buf->slot_token, buf->slot_ts,
-      buf->status, buf->clock);
+      buf->lru_order, buf->status, buf->clock);
   HS_LAUNCH_CHECK("k_verify_commit");
   return HS_OK;
 }

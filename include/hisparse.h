@@ -88,7 +88,8 @@ enum hs_status_code {
  * (anchor + drafts), which the caller writes before hs_swap_in (they are
  * always hits and never evicted).
  *
- *   max_reqs          number of requests the buffer serves (ids 0..max_reqs-1)
+ *   max_reqs          number of requests the buffer serves (ids 0..max_reqs-1),
+ *                     1 .. 16384
  *   slots_per_req     S, LRU slots per request, 1 .. 8192
  *   step_slots        rows per request per decode step (1 anchor + d drafts),
  *                     1 .. 16; a verify with d drafts needs d + 1 <= step_slots
