@@ -34,6 +34,7 @@ namespace {
 
 constexpr int SW_THREADS = 1024;
 constexpr int ROW_CHUNK = 1024;   // rows of one request handled per pass
+constexpr int PB = 4;             // entries per thread per probe / table round
 
 struct SwapArgs {
   const int32_t *req_id, *clen, *kv_len, *topk;
@@ -166,38 +167,48 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
     if (n == 0) break;
     if (threadIdx.x == 0) s_any = 1;
     const int items = n * a.K;
-    for (int base = 0; base < items; base += SW_THREADS) {
-      const int i = base + (int)threadIdx.x;
-      int32_t t = -1, clen = 0;
-      if (i < items) {
-        const int row = rows[i / a.K];
-        t = a.topk[(int64_t)row * a.K + i % a.K];
-        clen = a.clen[row];
-      }
-      const bool bad = t >= 0 && (t >= clen || (t < L && t >= a.max_ctx));
-      const bool committed = t >= 0 && t < clen && t < L && t < a.max_ctx;
-      bool first = false;
-      int32_t s = -1;
-      if (committed) {
-        first = atomicExch(&a.pos_mark[cbase + t], a.epoch) != a.epoch;
-        if (first) {
-          s = a.token_slot[cbase + t];
-          if (s >= 0 && s < a.S) atomicOr(&hitmap[s >> 5], 1u << (s & 31));
+    // PB entries per thread per round: their loads, claims and lookups are all
+    // in flight together (each is a dependent global access)
+    for (int base = 0; base < items; base += SW_THREADS * PB) {
+      int32_t t[PB], clen[PB], sl[PB];
+      bool first[PB];
+#pragma unroll
+      for (int u = 0; u < PB; ++u) {
+        const int i = base + u * SW_THREADS + (int)threadIdx.x;
+        t[u] = -1;
+        clen[u] = 0;
+        if (i < items) {
+          const int row = rows[i / a.K];
+          t[u] = a.topk[(int64_t)row * a.K + i % a.K];
+          clen[u] = a.clen[row];
         }
       }
-      const unsigned bad_mask = __ballot_sync(0xffffffffu, bad);
-      const unsigned first_mask = __ballot_sync(0xffffffffu, first);
-      const unsigned miss_mask = __ballot_sync(0xffffffffu, first && s < 0);
-      int mbase = 0;
-      if (lane == 0) {
-        if (bad_mask) s_bad = 1;
-        if (first_mask) atomicAdd(&s_need, __popc(first_mask));
-        if (miss_mask) mbase = atomicAdd(&s_miss, __popc(miss_mask));
+#pragma unroll
+      for (int u = 0; u < PB; ++u) {
+        const bool committed = t[u] >= 0 && t[u] < clen[u] && t[u] < L && t[u] < a.max_ctx;
+        first[u] = committed && atomicExch(&a.pos_mark[cbase + t[u]], a.epoch) != a.epoch;
       }
-      mbase = __shfl_sync(0xffffffffu, mbase, 0);
-      if (first && s < 0) {
-        const int pos = mbase + __popc(miss_mask & ((1u << lane) - 1u));
-        if (pos < a.S) mkey[pos] = t;   // beyond S the request is refused below
+#pragma unroll
+      for (int u = 0; u < PB; ++u) sl[u] = first[u] ? a.token_slot[cbase + t[u]] : -1;
+#pragma unroll
+      for (int u = 0; u < PB; ++u) {
+        if (first[u] && sl[u] >= 0 && sl[u] < a.S) atomicOr(&hitmap[sl[u] >> 5], 1u << (sl[u] & 31));
+        const bool bad = t[u] >= 0 && (t[u] >= clen[u] || (t[u] < L && t[u] >= a.max_ctx));
+        const bool miss = first[u] && sl[u] < 0;
+        const unsigned bad_mask = __ballot_sync(0xffffffffu, bad);
+        const unsigned first_mask = __ballot_sync(0xffffffffu, first[u]);
+        const unsigned miss_mask = __ballot_sync(0xffffffffu, miss);
+        int mbase = 0;
+        if (lane == 0) {
+          if (bad_mask) s_bad = 1;
+          if (first_mask) atomicAdd(&s_need, __popc(first_mask));
+          if (miss_mask) mbase = atomicAdd(&s_miss, __popc(miss_mask));
+        }
+        mbase = __shfl_sync(0xffffffffu, mbase, 0);
+        if (miss) {
+          const int pos = mbase + __popc(miss_mask & ((1u << lane) - 1u));
+          if (pos < a.S) mkey[pos] = t[u];   // beyond S the request is refused below
+        }
       }
     }
     __syncthreads();
@@ -279,22 +290,41 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
     for (int i = threadIdx.x; i < n; i += SW_THREADS) rvalid[i] = 0;
     __syncthreads();
     const int items = n * a.K;
-    for (int i = threadIdx.x; i < items; i += SW_THREADS) {
-      const int ri = (int)(i / a.K);
-      const int row = rows[ri];
-      const int32_t t = a.topk[(int64_t)row * a.K + i % a.K];
-      const int32_t clen = a.clen[row];
-      int32_t v = -1;
-      if (t >= 0 && t < clen) {
-        if (t >= L) {
-          if (t - L < a.S_tot - a.S) v = row0 + a.S + (t - L);
-        } else if (!failed && t < a.max_ctx) {
-          const int32_t s = ts_row[t];
-          if (s >= 0) v = row0 + s;
+    for (int base = 0; base < items; base += SW_THREADS * PB) {
+      int32_t t[PB], clen[PB], sl[PB];
+      int ri[PB];
+#pragma unroll
+      for (int u = 0; u < PB; ++u) {
+        const int i = base + u * SW_THREADS + (int)threadIdx.x;
+        t[u] = -1;
+        clen[u] = 0;
+        ri[u] = -1;
+        if (i < items) {
+          ri[u] = i / a.K;
+          t[u] = a.topk[(int64_t)rows[ri[u]] * a.K + i % a.K];
+          clen[u] = a.clen[rows[ri[u]]];
         }
       }
-      out[(int64_t)row * a.K + i % a.K] = v;
-      if (v >= 0) atomicAdd(&rvalid[ri], 1);
+#pragma unroll
+      for (int u = 0; u < PB; ++u)
+        sl[u] = (!failed && t[u] >= 0 && t[u] < clen[u] && t[u] < L && t[u] < a.max_ctx)
+                    ? ts_row[t[u]] : -1;
+#pragma unroll
+      for (int u = 0; u < PB; ++u) {
+        if (ri[u] < 0) continue;
+        const int32_t tt = t[u];
+        int32_t v = -1;
+        if (tt >= 0 && tt < clen[u]) {
+          if (tt >= L) {
+            if (tt - L < a.S_tot - a.S) v = row0 + a.S + (tt - L);
+          } else if (sl[u] >= 0) {
+            v = row0 + sl[u];
+          }
+        }
+        const int i = base + u * SW_THREADS + (int)threadIdx.x;
+        out[(int64_t)rows[ri[u]] * a.K + i % a.K] = v;
+        if (v >= 0) atomicAdd(&rvalid[ri[u]], 1);
+      }
     }
     __syncthreads();
     if (out_valid)
