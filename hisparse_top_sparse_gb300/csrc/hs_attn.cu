@@ -13,17 +13,20 @@
 // all of TMEM) do not fit one SM together with KV tiles. Each row is therefore
 // served by two CTAs, c = 0 / 1, each owning value dims [256c, 256c + 256):
 //   * O_c (128 x 256 fp32) lives in TMEM columns [0, 256);
-//   * Q dims 0..255 live in TMEM columns [256, 384) as the MMA's A operand;
-//     Q dims 256..575 live in shared memory (5 x 16 KB, 128-byte swizzle);
+//   * Q dims 0..319 live in TMEM columns [256, 416) as the MMA's A operand;
+//     Q dims 320..575 live in shared memory (4 x 16 KB, 128-byte swizzle);
 //   * S = Q K^T (128 x 32 fp32, all 576 dims -- both CTAs compute it) has
-//     three buffers in TMEM columns [384, 480);
-//   * KV rows are gathered 32 at a time by 16-byte cp.async into a 4-stage
-//     ring of swizzled tiles (36 KB each), each producer thread's copies
-//     arriving on the stage's mbarrier as they land (cp.async.mbarrier.arrive),
-//     so up to four tiles are in flight: the tile is the K-major B operand
-//     of Q K^T and, read MN-major, the B operand of P V;
-//   * P (bf16, 128 x 32) has two 16-column buffers in TMEM [480, 512) and is
-//     read from TMEM as P V's A operand.
+//     three buffers in TMEM columns [416, 512); the softmax overwrites the
+//     first 16 columns of its buffer with P (bf16 pairs), which P V then reads
+//     from TMEM as its A operand, so a buffer is free again once P V is done;
+//   * KV rows are gathered 32 at a time by 16-byte cp.async, each producer
+//     thread's copies arriving on the tile's mbarrier as they land
+//     (cp.async.mbarrier.arrive). A tile is split by 64-dim swizzle block over
+//     two rings: the four blocks of this CTA's value half go to ring B (five
+//     16 KB slots), held until P V is done; the other five blocks (the other
+//     value half and the rope dims, read by Q K^T only) go to ring A (four
+//     20 KB slots), free again as soon as Q K^T is done. A tile is the K-major
+//     B operand of Q K^T and, read MN-major from ring B, the B operand of P V.
 // Warp roles (384 threads): warps 0-3 softmax + epilogue (thread = head =
 // TMEM lane), warps 4-7 gather producers, warps 8-10
 // issue Q K^T for tiles t = 0, 1, 2 (mod 3) into three S buffers (one thread
@@ -44,36 +47,48 @@ constexpr int D = HS_LATENT_DIM;
 constexpr int DV = HS_VALUE_DIM;
 constexpr int HG = 128;                   // heads per CTA (MMA M)
 constexpr int NK = 32;                    // keys per tile (MMA N of Q K^T)
-constexpr int STAGES = 4;
 constexpr int ROWB = D * 2;               // 1152
 constexpr int NCH = ROWB / 16;            // 72 chunks of 16 B per latent row
-constexpr int QT_DIMS = 256;              // Q dims held in TMEM
-constexpr int QS_BLOCKS = (D - QT_DIMS) / 64;   // 5 swizzle blocks of Q in SMEM
+constexpr int QT_DIMS = 320;              // Q dims held in TMEM
+constexpr int QS_BLOCKS = (D - QT_DIMS) / 64;   // 4 swizzle blocks of Q in SMEM
 constexpr int NSB = 3;                    // S buffers = Q K^T chains in flight
 constexpr int KV_BLOCKS = D / 64;         // 9 swizzle blocks per KV tile
+constexpr int VB_BLOCKS = 4;              // blocks of one value half
+constexpr int RA_SLOTS = 4, RB_SLOTS = 5; // ring A (Q K^T only) / ring B (value half)
 constexpr int THREADS = 384;
 constexpr int NPROD = 128;
 
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr int QS_OFF = 0;
-constexpr int QS_BYTES = QS_BLOCKS * HG * 128;         // 81920
-constexpr int KV_OFF = QS_OFF + QS_BYTES;
+constexpr int QS_BYTES = QS_BLOCKS * HG * 128;         // 65536
 constexpr int KV_BLOCK_BYTES = NK * 128;               // 4096
-constexpr int KV_STAGE_BYTES = KV_BLOCKS * KV_BLOCK_BYTES;   // 36864
-constexpr int BAR_OFF = KV_OFF + STAGES * KV_STAGE_BYTES;
+constexpr int RA_SLOT_BYTES = (KV_BLOCKS - VB_BLOCKS) * KV_BLOCK_BYTES;   // 20480
+constexpr int RB_SLOT_BYTES = VB_BLOCKS * KV_BLOCK_BYTES;                 // 16384
+constexpr int RA_OFF = QS_OFF + QS_BYTES;
+constexpr int RB_OFF = RA_OFF + RA_SLOTS * RA_SLOT_BYTES;
+constexpr int BAR_OFF = RB_OFF + RB_SLOTS * RB_SLOT_BYTES;
 constexpr int SMEM_USED = BAR_OFF + 256;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;           // slack for the 1 KB alignment
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
 // TMEM columns
-constexpr uint32_t COL_O = 0, COL_Q = 256, COL_S = 384, COL_P = 480;
-static_assert(COL_Q + QT_DIMS / 2 == COL_S && COL_S + NSB * NK == COL_P && COL_P + 2 * NK / 2 == 512,
-              "TMEM column map");
+constexpr uint32_t COL_O = 0, COL_Q = 256, COL_S = 416;
+static_assert(COL_Q + QT_DIMS / 2 == COL_S && COL_S + NSB * NK == 512, "TMEM column map");
 
 // barriers (8-byte words at BAR_OFF)
-enum { B_FULL = 0, B_EMPTY = B_FULL + STAGES, B_SFULL = B_EMPTY + STAGES, B_SFREE = B_SFULL + NSB,
-       B_PFULL = B_SFREE + NSB, B_PVDONE = B_PFULL + 2, B_OFULL = B_PVDONE + 2, B_COUNT = B_OFULL + 1 };
+enum { B_FULL = 0, B_EMPTYA = B_FULL + RA_SLOTS, B_EMPTYB = B_EMPTYA + RA_SLOTS,
+       B_SFULL = B_EMPTYB + RB_SLOTS, B_SFREE = B_SFULL + NSB, B_PFULL = B_SFREE + NSB,
+       B_OFULL = B_PFULL + NSB, B_COUNT = B_OFULL + 1 };
 static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
+
+// Shared-memory address of swizzle block a (0..8) of a tile whose ring A /
+// ring B slots start at ra / rb, for the CTA owning value half c: blocks
+// 4c..4c+3 are in ring B, the others in ring A in ascending order.
+__device__ __forceinline__ uint32_t kv_block(uint32_t ra, uint32_t rb, int c, int a) {
+  if ((a >> 2) == c && a < 8) return rb + (uint32_t)(a & 3) * KV_BLOCK_BYTES;
+  const int pa = (c == 0) ? a - 4 : (a == 8 ? 4 : a);
+  return ra + (uint32_t)pa * KV_BLOCK_BYTES;
+}
 
 constexpr int WAIT_LIMIT = 1 << 24;
 
@@ -234,17 +249,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int32_t *idx_row = idx + (int64_t)r * K;
 
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < RA_SLOTS; ++s) {
       bar_init(bar(B_FULL + s), NPROD);
-      bar_init(bar(B_EMPTY + s), 1);
+      bar_init(bar(B_EMPTYA + s), 1);
     }
+    for (int s = 0; s < RB_SLOTS; ++s) bar_init(bar(B_EMPTYB + s), 1);
     for (int b = 0; b < NSB; ++b) {
       bar_init(bar(B_SFULL + b), 1);
-      bar_init(bar(B_SFREE + b), 4);
-    }
-    for (int b = 0; b < 2; ++b) {
+      bar_init(bar(B_SFREE + b), 1);
       bar_init(bar(B_PFULL + b), 4);
-      bar_init(bar(B_PVDONE + b), 1);
     }
     bar_init(bar(B_OFULL), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -255,7 +268,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
 
-  // Q dims 384..575 -> SMEM (three 64-dim swizzle blocks), all threads
+  // Q dims 320..575 -> SMEM (four 64-dim swizzle blocks), all threads
   for (int i = tid; i < HG * QS_BLOCKS * 8; i += THREADS) {
     const int hr = i / (QS_BLOCKS * 8), rem = i % (QS_BLOCKS * 8);
     const int j = rem / 8, cc = rem % 8;
@@ -272,7 +285,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    // Q dims 0..383 -> TMEM columns [256, 448): lane = head, column j holds
+    // Q dims 0..319 -> TMEM columns [256, 416): lane = head, column j holds
     // dims 2j, 2j+1
     const int h = h0 + tid;
     const uint4 *qrow = reinterpret_cast<const uint4 *>(q + ((int64_t)r * H + (h < H ? h : 0)) * ROWB);
@@ -311,25 +324,32 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     int32_t id0 = load_id(0), id1 = load_id(1);
     for (int t = 0; t < T && !timed_out; ++t) {
-      const int st = t % STAGES;
+      const int sa = t % RA_SLOTS, sbv = t % RB_SLOTS;
       const int32_t id = id0;
       id0 = id1;
       id1 = load_id(t + 2);
-      if (t >= STAGES && !bar_wait(bar(B_EMPTY + st), ((t / STAGES) - 1) & 1)) {
+      if (t >= RA_SLOTS && !bar_wait(bar(B_EMPTYA + sa), ((t / RA_SLOTS) - 1) & 1)) {
+        timed_out = true;
+        break;
+      }
+      if (t >= RB_SLOTS && !bar_wait(bar(B_EMPTYB + sbv), ((t / RB_SLOTS) - 1) & 1)) {
         timed_out = true;
         break;
       }
       const bool v = id >= 0 && id < n_kv;
       const char *src = kv + (v ? (int64_t)id * ROWB : 0);
-      const uint32_t dst = sbase + KV_OFF + st * KV_STAGE_BYTES;
+      const uint32_t ra = sbase + RA_OFF + sa * RA_SLOT_BYTES;
+      const uint32_t rb = sbase + RB_OFF + sbv * RB_SLOT_BYTES;
+      // copy k of this thread is chunk sub + 4k: swizzle block k / 2, chunk
+      // sub + 4 (k & 1) within the block's 128-byte row
 #pragma unroll
       for (int k = 0; k < NCH / 4; ++k) {
         const int ch = sub + 4 * k;
-        cp_async16(dst + (ch >> 3) * KV_BLOCK_BYTES + sw128(key, ch & 7), v ? src + ch * 16 : q, v);
+        cp_async16(kv_block(ra, rb, c, k >> 1) + sw128(key, ch & 7), v ? src + ch * 16 : q, v);
       }
-      // the stage's barrier gets this thread's arrival when its copies land
+      // the tile's barrier gets this thread's arrival when its copies land
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(
-                       bar(B_FULL + st))
+                       bar(B_FULL + sa))
                    : "memory");
     }
     cp_async_wait<0>();
@@ -338,50 +358,50 @@ __global__ void __launch_bounds__(THREADS, 1)
     // warp 8 + b issues tiles t = b, b + 3, ... into S buffer b, so three
     // 36-instruction chains are in flight at once
     if (lane == 0) {
-      const uint32_t kv0 = sbase + KV_OFF, qs0 = sbase + QS_OFF;
+      const uint32_t qs0 = sbase + QS_OFF;
       const int sb = warp - 8;
       bool ok = true;
       for (int t = sb; t < T && ok; t += NSB) {
-        const int st = t % STAGES;
-        ok = bar_wait(bar(B_FULL + st), (t / STAGES) & 1);
+        const int sa = t % RA_SLOTS;
+        ok = bar_wait(bar(B_FULL + sa), (t / RA_SLOTS) & 1);
         if (ok && t >= NSB) ok = bar_wait(bar(B_SFREE + sb), ((t / NSB) - 1) & 1);
         if (!ok) break;
         fence_after();
         fence_proxy_async();   // the tile was written by cp.async (generic proxy)
-        const uint32_t kt = kv0 + st * KV_STAGE_BYTES;
+        const uint32_t ra = sbase + RA_OFF + sa * RA_SLOT_BYTES;
+        const uint32_t rb = sbase + RB_OFF + (t % RB_SLOTS) * RB_SLOT_BYTES;
         const uint32_t sd = tmem + COL_S + sb * NK;
 #pragma unroll
         for (int kk = 0; kk < QT_DIMS / 16; ++kk)
           mma_ts(sd, tmem + COL_Q + kk * 8,
-                 sdesc(kt + (kk >> 2) * KV_BLOCK_BYTES + (kk & 3) * 32, 16, 1024), IDESC_QK,
-                 kk > 0);
+                 sdesc(kv_block(ra, rb, c, kk >> 2) + (kk & 3) * 32, 16, 1024), IDESC_QK, kk > 0);
 #pragma unroll
         for (int kk = QT_DIMS / 16; kk < D / 16; ++kk) {
           const int qk = kk - QT_DIMS / 16;
           mma_ss(sd, sdesc(qs0 + (qk >> 2) * (HG * 128) + (qk & 3) * 32, 16, 1024),
-                 sdesc(kt + (kk >> 2) * KV_BLOCK_BYTES + (kk & 3) * 32, 16, 1024), IDESC_QK, 1);
+                 sdesc(kv_block(ra, rb, c, kk >> 2) + (kk & 3) * 32, 16, 1024), IDESC_QK, 1);
         }
         mma_commit(bar(B_SFULL + sb));
+        mma_commit(bar(B_EMPTYA + sa));   // ring A slot: Q K^T was its last reader
       }
       timed_out = !ok;
     }
   } else if (warp == 8 + NSB) {
     // --------------------------------------------------- P V issuer ----
     if (lane == 0) {
-      const uint32_t kv0 = sbase + KV_OFF;
       bool ok = true;
       for (int u = 0; u < T && ok; ++u) {
-        const int sb = u & 1, st = u % STAGES;
-        ok = bar_wait(bar(B_PFULL + sb), (u >> 1) & 1);
+        const int sb = u % NSB, sbv = u % RB_SLOTS;
+        ok = bar_wait(bar(B_PFULL + sb), (u / NSB) & 1);
         if (!ok) break;
         fence_after();
-        const uint32_t vbase = kv0 + st * KV_STAGE_BYTES + (4 * c) * KV_BLOCK_BYTES;
+        const uint32_t vbase = sbase + RB_OFF + sbv * RB_SLOT_BYTES;
 #pragma unroll
         for (int ks = 0; ks < NK / 16; ++ks)
-          mma_ts(tmem + COL_O, tmem + COL_P + sb * (NK / 2) + ks * 8,
+          mma_ts(tmem + COL_O, tmem + COL_S + sb * NK + ks * 8,
                  sdesc(vbase + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (u > 0 || ks > 0));
-        mma_commit(bar(B_PVDONE + sb));
-        mma_commit(bar(B_EMPTY + st));
+        mma_commit(bar(B_SFREE + sb));    // S/P buffer may take tile u + 3
+        mma_commit(bar(B_EMPTYB + sbv));  // ring B slot may take tile u + 5
       }
       if (ok && T > 0) mma_commit(bar(B_OFULL));
       timed_out = !ok;
@@ -397,15 +417,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     int32_t my_id = load_id(0);
     for (int t = 0; t < T; ++t) {
-      const int sb = t % NSB, pb = t & 1;
+      const int sb = t % NSB;
       if (!warp_wait(bar(B_SFULL + sb), (t / NSB) & 1)) { timed_out = true; break; }
       fence_after();
       uint32_t sr[NK];
       TMEM_LD32(lane_base + COL_S + sb * NK, sr);
       tmem_wait_ld();
-      fence_before();
-      __syncwarp();
-      if (lane == 0) bar_arrive(bar(B_SFREE + sb));   // the S buffer may be refilled
 
       // invalid keys -> -inf in place (warp-uniform skip when all are valid)
       const uint32_t vmask = __ballot_sync(0xffffffffu, my_id >= 0 && my_id < n_kv);
@@ -424,7 +441,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool need_o = grow && m_used != -INFINITY;
       if (__any_sync(0xffffffffu, need_o)) {
         // O must hold every PV issued so far before it is rescaled
-        if (t >= 1 && !warp_wait(bar(B_PVDONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1)) {
+        if (t >= 1 && !warp_wait(bar(B_SFREE + (t - 1) % NSB), ((t - 1) / NSB) & 1)) {
           timed_out = true;
           break;
         }
@@ -444,9 +461,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (grow) m_used = mt;
 
-      // P = exp2(s * scale - m) as bf16 into P buffer pb (P V reads it from
-      // TMEM as its A operand) once P V(t-2) has finished with that buffer
-      if (t >= 2 && !warp_wait(bar(B_PVDONE + pb), ((t >> 1) - 1) & 1)) { timed_out = true; break; }
+      // P = exp2(s * scale - m) as bf16 over the first 16 columns of the same
+      // buffer (P V reads it from TMEM as its A operand)
       const float mu = (m_used == -INFINITY) ? 0.f : m_used;
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -457,11 +473,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         sr[k] = pack_bf16(a, b);          // in place: pair k of P
       }
       l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      TMEM_ST16(lane_base + COL_P + pb * (NK / 2), sr);
+      TMEM_ST16(lane_base + COL_S + sb * NK, sr);
       tmem_wait_st();
       fence_before();
       __syncwarp();
-      if (lane == 0) bar_arrive(bar(B_PFULL + pb));
+      if (lane == 0) bar_arrive(bar(B_PFULL + sb));
     }
 
     // ---------------------------------------------------------- epilogue --
