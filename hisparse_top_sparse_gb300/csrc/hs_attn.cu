@@ -7,33 +7,39 @@
 // coordinator to the DSA backend; "vllm 分析(十二) HiSparse 下篇",
 // resolve_topk returns (attention cache, indices[, valid counts])).
 //
-// k_attn_umma -- 5th-generation tensor cores (tcgen05) with TMEM accumulators.
+// k_attn_pair -- 5th-generation tensor cores (tcgen05) with TMEM accumulators,
+// one two-CTA cluster per (query row, group of 128 heads).
 //
 // Per row, Q (128 heads x 576 bf16 = 147 KB) and O (128 x 512 fp32 = 256 KB,
-// all of TMEM) do not fit one SM together with KV tiles. Each row is therefore
-// served by two CTAs, c = 0 / 1, each owning value dims [256c, 256c + 256):
-//   * O_c (128 x 256 fp32) lives in TMEM columns [0, 256);
-//   * Q dims 0..319 live in TMEM columns [256, 416) as the MMA's A operand;
-//     Q dims 320..575 live in shared memory (4 x 16 KB, 128-byte swizzle);
-//   * S = Q K^T (128 x 32 fp32, all 576 dims -- both CTAs compute it) has
-//     three buffers in TMEM columns [416, 512); the softmax overwrites the
-//     first 16 columns of its buffer with P (bf16 pairs), which P V then reads
-//     from TMEM as its A operand, so a buffer is free again once P V is done;
-//   * KV rows are gathered 32 at a time by 16-byte cp.async, each producer
-//     thread's copies arriving on the tile's mbarrier as they land
-//     (cp.async.mbarrier.arrive). A tile is split by 64-dim swizzle block over
-//     two rings: the four blocks of this CTA's value half go to ring B (five
-//     16 KB slots), held until P V is done; the other five blocks (the other
-//     value half and the rope dims, read by Q K^T only) go to ring A (four
-//     20 KB slots), free again as soon as Q K^T is done. A tile is the K-major
-//     B operand of Q K^T and, read MN-major from ring B, the B operand of P V.
-// Warp roles (384 threads): warps 0-3 softmax + epilogue (thread = head =
-// TMEM lane), warps 4-7 gather producers, warps 8-10
-// issue Q K^T for tiles t = 0, 1, 2 (mod 3) into three S buffers (one thread
-// issues a tcgen05.mma only every ~60-150 cycles, so three chains are kept in
-// flight), warp 11 issues P V.
-// Online softmax in the log2 domain with lazy rescaling: O is rescaled (in
-// TMEM) only when a row's running max grows by more than 2^8.
+// all of TMEM) do not fit one SM together with KV tiles, so the row's work is
+// split over the two CTAs of a cluster, c = 0 / 1:
+//   * CTA c owns value dims [256c, 256c + 256): O_c (128 x 256 fp32) lives in
+//     its TMEM columns [0, 256);
+//   * the selected keys come in tiles of 32; CTA c computes S = Q K^T (all 576
+//     dims) and the softmax numerators P only for its own tiles t = c, c + 2,
+//     ...; Q dims 0..383 sit in TMEM columns [256, 448) as the MMA's A
+//     operand, dims 384..575 in shared memory (3 x 16 KB, 128-byte swizzle);
+//     S has two 32-column TMEM buffers [448, 512), and the softmax writes P
+//     (bf16 pairs) over the first 16 columns of its buffer;
+//   * P of an own tile goes to the CTA's own P V (read from TMEM) and, by
+//     st.async into the peer's shared memory, to the peer's P V (read from
+//     shared memory); the peer's P V commit arrives back on this CTA's
+//     mbarrier (tcgen05.commit multicast), freeing the slot;
+//   * the KV rows of an own tile are gathered whole (16-byte cp.async, each
+//     producer thread's copies arriving on the tile's mbarrier as they land):
+//     the four 64-dim swizzle blocks of this CTA's value half into ring VO,
+//     the other five into ring A (freed once Q K^T is done); of a peer tile
+//     only this CTA's value half is gathered, into ring VP;
+//   * both CTAs use one softmax reference per head: the larger of their first
+//     tiles' maxima, agreed through distributed shared memory before any P is
+//     made, so every P of the row is on one scale and O is never rescaled. A
+//     later tile whose maximum exceeds the reference by more than 2^30 marks
+//     the row, and the pair then runs the row again with the exact maximum
+//     (exchanged at the end of the first pass) as the reference. The row sum
+//     l is the sum of both CTAs' partial sums.
+// Warp roles (352 threads): warps 0-3 softmax, P exchange and epilogue (thread
+// = head = TMEM lane), warps 4-7 gather producers, warps 8-9 issue Q K^T for
+// own tiles into S buffers 0 / 1, warp 10 issues P V for every tile in order.
 // Every mbarrier wait is bounded; a wait that gives up sets HS_STATUS_TIMEOUT
 // in the caller's status word and the CTA winds down.
 
@@ -45,52 +51,73 @@ namespace {
 
 constexpr int D = HS_LATENT_DIM;
 constexpr int DV = HS_VALUE_DIM;
-constexpr int HG = 128;                   // heads per CTA (MMA M)
+constexpr int HG = 128;                   // heads per cluster (MMA M)
 constexpr int NK = 32;                    // keys per tile (MMA N of Q K^T)
 constexpr int ROWB = D * 2;               // 1152
 constexpr int NCH = ROWB / 16;            // 72 chunks of 16 B per latent row
-constexpr int QT_DIMS = 320;              // Q dims held in TMEM
-constexpr int QS_BLOCKS = (D - QT_DIMS) / 64;   // 4 swizzle blocks of Q in SMEM
-constexpr int NSB = 3;                    // S buffers = Q K^T chains in flight
-constexpr int KV_BLOCKS = D / 64;         // 9 swizzle blocks per KV tile
-constexpr int VB_BLOCKS = 4;              // blocks of one value half
-constexpr int RA_SLOTS = 4, RB_SLOTS = 5; // ring A (Q K^T only) / ring B (value half)
-constexpr int THREADS = 384;
+constexpr int QT_DIMS = 384;              // Q dims held in TMEM
+constexpr int QS_BLOCKS = (D - QT_DIMS) / 64;   // 3 swizzle blocks of Q in SMEM
+constexpr int NSB = 2;                    // S / P buffers (own tiles)
+constexpr int VB_BLOCKS = 4;              // swizzle blocks of one value half
+constexpr int RA_SLOTS = 3, VO_SLOTS = 3, VP_SLOTS = 3, XP_SLOTS = 2;
+constexpr int THREADS = 352;
 constexpr int NPROD = 128;
+constexpr float REF_SLACK = 30.0f;        // P <= 2^30 on the shared reference
 
 // shared memory (offsets from a 1024-byte aligned base)
+constexpr int KV_BLOCK_BYTES = NK * 128;                    // 4096
 constexpr int QS_OFF = 0;
-constexpr int QS_BYTES = QS_BLOCKS * HG * 128;         // 65536
-constexpr int KV_BLOCK_BYTES = NK * 128;               // 4096
-constexpr int RA_SLOT_BYTES = (KV_BLOCKS - VB_BLOCKS) * KV_BLOCK_BYTES;   // 20480
-constexpr int RB_SLOT_BYTES = VB_BLOCKS * KV_BLOCK_BYTES;                 // 16384
-constexpr int RA_OFF = QS_OFF + QS_BYTES;
-constexpr int RB_OFF = RA_OFF + RA_SLOTS * RA_SLOT_BYTES;
-constexpr int BAR_OFF = RB_OFF + RB_SLOTS * RB_SLOT_BYTES;
-constexpr int SMEM_USED = BAR_OFF + 256;
-constexpr int SMEM_ALLOC = SMEM_USED + 1024;           // slack for the 1 KB alignment
+constexpr int QS_BYTES = QS_BLOCKS * HG * 128;              // 49152
+constexpr int XP_OFF = QS_OFF + QS_BYTES;                   // peer's P: 128 rows x 128 B,
+constexpr int XP_BYTES = HG * 128;                          // slot s = bytes [64s, 64s + 64)
+constexpr int RA_SLOT_BYTES = (D / 64 - VB_BLOCKS) * KV_BLOCK_BYTES;   // 20480
+constexpr int V_SLOT_BYTES = VB_BLOCKS * KV_BLOCK_BYTES;              // 16384
+constexpr int RA_OFF = XP_OFF + XP_BYTES;
+constexpr int VO_OFF = RA_OFF + RA_SLOTS * RA_SLOT_BYTES;
+constexpr int VP_OFF = VO_OFF + VO_SLOTS * V_SLOT_BYTES;
+constexpr int XMAX_OFF = VP_OFF + VP_SLOTS * V_SLOT_BYTES;  // peer's first-tile maxima
+constexpr int XEND_OFF = XMAX_OFF + HG * 4;                 // peer's (l, max, flag) per pass
+constexpr int BAR_OFF = XEND_OFF + 2 * HG * 16;
+constexpr int SMEM_USED = BAR_OFF + 512;
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;                // slack for the 1 KB alignment
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+static_assert(RA_OFF % 1024 == 0 && VO_OFF % 1024 == 0 && VP_OFF % 1024 == 0, "slot alignment");
 
 // TMEM columns
-constexpr uint32_t COL_O = 0, COL_Q = 256, COL_S = 416;
+constexpr uint32_t COL_O = 0, COL_Q = 256, COL_S = 448;
 static_assert(COL_Q + QT_DIMS / 2 == COL_S && COL_S + NSB * NK == 512, "TMEM column map");
 
 // barriers (8-byte words at BAR_OFF)
-enum { B_FULL = 0, B_EMPTYA = B_FULL + RA_SLOTS, B_EMPTYB = B_EMPTYA + RA_SLOTS,
-       B_SFULL = B_EMPTYB + RB_SLOTS, B_SFREE = B_SFULL + NSB, B_PFULL = B_SFREE + NSB,
-       B_OFULL = B_PFULL + NSB, B_COUNT = B_OFULL + 1 };
-static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
+enum {
+  B_FULLA = 0,                        // own tile landed (NPROD arrivals)
+  B_EMPTYA = B_FULLA + RA_SLOTS,      // ring A slot: Q K^T done
+  B_EMPTYVO = B_EMPTYA + RA_SLOTS,    // ring VO slot: own P V done
+  B_FULLVP = B_EMPTYVO + VO_SLOTS,    // peer tile's value half landed (NPROD arrivals)
+  B_EMPTYVP = B_FULLVP + VP_SLOTS,    // ring VP slot: P V done
+  B_SFULL = B_EMPTYVP + VP_SLOTS,     // S ready
+  B_SFREE = B_SFULL + NSB,            // own P V done with the S / P buffer
+  B_PFULL = B_SFREE + NSB,            // P in TMEM (4 softmax warps)
+  B_XPFULL = B_PFULL + NSB,           // the peer's P landed here (1 arrival + bytes)
+  B_XPFREE = B_XPFULL + XP_SLOTS,     // the peer is done with our P in its slot
+  B_XMAX = B_XPFREE + XP_SLOTS,       // the peer's first-tile maxima landed
+  B_XEND = B_XMAX + 1,                // the peer's end-of-pass figures (one per pass)
+  B_VOTE = B_XEND + 2,                // the four softmax warps have voted for a second pass
+  B_DECIDE = B_VOTE + 1,              // softmax -> other roles: second pass or not
+  B_OFULL = B_DECIDE + 1,             // all P V of a pass done (one per pass)
+  B_COUNT = B_OFULL + 2
+};
+static_assert(B_COUNT * 8 + 8 <= 512, "barrier area");
 
-// Shared-memory address of swizzle block a (0..8) of a tile whose ring A /
-// ring B slots start at ra / rb, for the CTA owning value half c: blocks
-// 4c..4c+3 are in ring B, the others in ring A in ascending order.
-__device__ __forceinline__ uint32_t kv_block(uint32_t ra, uint32_t rb, int c, int a) {
-  if ((a >> 2) == c && a < 8) return rb + (uint32_t)(a & 3) * KV_BLOCK_BYTES;
+constexpr int WAIT_LIMIT = 1 << 24;
+
+// Shared-memory address of swizzle block a (0..8) of an own tile whose ring A
+// / ring VO slots start at ra / rv, for the CTA owning value half c: blocks
+// 4c..4c+3 are in ring VO, the others in ring A in ascending order.
+__device__ __forceinline__ uint32_t kv_block(uint32_t ra, uint32_t rv, int c, int a) {
+  if ((a >> 2) == c && a < 8) return rv + (uint32_t)(a & 3) * KV_BLOCK_BYTES;
   const int pa = (c == 0) ? a - 4 : (a == 8 ? 4 : a);
   return ra + (uint32_t)pa * KV_BLOCK_BYTES;
 }
-
-constexpr int WAIT_LIMIT = 1 << 24;
 
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
@@ -123,6 +150,13 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, 
       "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+// commit whose mbarrier arrival lands at the same offset in the CTAs of `mask`
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n" ::"r"(bar), "h"(mask)
+      : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
@@ -227,8 +261,65 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
-    k_attn_umma(const char *__restrict__ q, const char *__restrict__ kv, int64_t n_kv,
+
+// ---- cluster helpers --------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+// address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t peer_addr(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
+                   : "memory");
+}
+// 16 / 4 bytes into the peer's shared memory; the peer's mbarrier `rbar`
+// counts the bytes when they land
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d, uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(
+          addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];\n" ::"r"(addr),
+               "r"(v), "r"(rbar)
+               : "memory");
+}
+// this thread's arrival plus the bytes still to come in the current phase
+__device__ __forceinline__ void arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+// bounded wait on a barrier that the peer CTA completes (cluster-scope acquire)
+__device__ __forceinline__ bool bar_wait_cluster(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  for (int i = 0; i < WAIT_LIMIT; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > (1ll << 31)) break;
+  }
+  return false;
+}
+__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, bar_wait_cluster(bar, parity));
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    k_attn_pair(const char *__restrict__ q, const char *__restrict__ kv, int64_t n_kv,
                 const int32_t *__restrict__ idx, int32_t H, int32_t K, float scale_log2,
                 __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, uint32_t *status) {
   extern __shared__ unsigned char smem_raw[];
@@ -237,29 +328,47 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(sm);
   const uint32_t bars = sbase + BAR_OFF;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + BAR_OFF + B_COUNT * 8);
+  volatile uint32_t *s_redo = tmem_slot + 1;
   auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = (int)cluster_rank();                // value half; own tiles t = c mod 2
+  const uint32_t peer = (uint32_t)(c ^ 1);
   const int n_hg = (H + HG - 1) / HG;
-  const int c = blockIdx.x & 1;                     // value half
   const int rg = blockIdx.x >> 1;
   const int r = rg / n_hg;
   const int h0 = (rg % n_hg) * HG;
   const int T = (K + NK - 1) / NK;
+  const int n_own = T > c ? (T - c + 1) / 2 : 0;
   const int32_t *idx_row = idx + (int64_t)r * K;
 
   if (tid == 0) {
     for (int s = 0; s < RA_SLOTS; ++s) {
-      bar_init(bar(B_FULL + s), NPROD);
+      bar_init(bar(B_FULLA + s), NPROD);
       bar_init(bar(B_EMPTYA + s), 1);
     }
-    for (int s = 0; s < RB_SLOTS; ++s) bar_init(bar(B_EMPTYB + s), 1);
+    for (int s = 0; s < VO_SLOTS; ++s) bar_init(bar(B_EMPTYVO + s), 1);
+    for (int s = 0; s < VP_SLOTS; ++s) {
+      bar_init(bar(B_FULLVP + s), NPROD);
+      bar_init(bar(B_EMPTYVP + s), 1);
+    }
     for (int b = 0; b < NSB; ++b) {
       bar_init(bar(B_SFULL + b), 1);
       bar_init(bar(B_SFREE + b), 1);
       bar_init(bar(B_PFULL + b), 4);
     }
-    bar_init(bar(B_OFULL), 1);
+    for (int s = 0; s < XP_SLOTS; ++s) {
+      bar_init(bar(B_XPFULL + s), 1);
+      bar_init(bar(B_XPFREE + s), 1);
+    }
+    bar_init(bar(B_XMAX), 1);
+    for (int p = 0; p < 2; ++p) {
+      bar_init(bar(B_XEND + p), 1);
+      bar_init(bar(B_OFULL + p), 1);
+    }
+    bar_init(bar(B_VOTE), 4);
+    bar_init(bar(B_DECIDE), 1);
+    *s_redo = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) {
@@ -268,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
 
-  // Q dims 320..575 -> SMEM (four 64-dim swizzle blocks), all threads
+  // Q dims 384..575 -> SMEM (three 64-dim swizzle blocks), all threads
   for (int i = tid; i < HG * QS_BLOCKS * 8; i += THREADS) {
     const int hr = i / (QS_BLOCKS * 8), rem = i % (QS_BLOCKS * 8);
     const int j = rem / 8, cc = rem % 8;
@@ -285,12 +394,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    // Q dims 0..319 -> TMEM columns [256, 416): lane = head, column j holds
+    // Q dims 0..383 -> TMEM columns [256, 448): lane = head, column j holds
     // dims 2j, 2j+1
     const int h = h0 + tid;
     const uint4 *qrow = reinterpret_cast<const uint4 *>(q + ((int64_t)r * H + (h < H ? h : 0)) * ROWB);
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-#pragma unroll
+#pragma unroll 1
     for (int part = 0; part < QT_DIMS / 64; ++part) {
       uint32_t v[32];
 #pragma unroll
@@ -306,7 +415,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   cp_async_wait<0>();
   fence_proxy_async();
   fence_before();
-  __syncthreads();
+  cluster_sync();          // both CTAs' barriers exist before any remote operation
   fence_after();
 
   bool timed_out = false;
@@ -316,175 +425,273 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int p = tid - 128;          // 0..127
     const int key = p >> 2;           // 32 keys per tile, 4 threads per key
     const int sub = p & 3;            // chunks sub, sub+4, ..., 18 per thread
-    // this thread's key index for tiles t and t+1 is loaded two tiles ahead so
-    // the index load never sits between a stage becoming free and its refill
     auto load_id = [&](int t) -> int32_t {
       const int j = t * NK + key;
       return (t < T && j < K) ? __ldg(idx_row + j) : -1;
     };
-    int32_t id0 = load_id(0), id1 = load_id(1);
-    for (int t = 0; t < T && !timed_out; ++t) {
-      const int sa = t % RA_SLOTS, sbv = t % RB_SLOTS;
-      const int32_t id = id0;
-      id0 = id1;
-      id1 = load_id(t + 2);
-      if (t >= RA_SLOTS && !bar_wait(bar(B_EMPTYA + sa), ((t / RA_SLOTS) - 1) & 1)) {
-        timed_out = true;
-        break;
+    int ig = 0, jg = 0;               // own / peer tiles issued, over both passes
+    for (int pass = 0; pass < 2 && !timed_out; ++pass) {
+      if (pass == 1) {
+        if (!bar_wait(bar(B_DECIDE), 0)) { timed_out = true; break; }
+        if (!*s_redo) break;
       }
-      if (t >= RB_SLOTS && !bar_wait(bar(B_EMPTYB + sbv), ((t / RB_SLOTS) - 1) & 1)) {
-        timed_out = true;
-        break;
-      }
-      const bool v = id >= 0 && id < n_kv;
-      const char *src = kv + (v ? (int64_t)id * ROWB : 0);
-      const uint32_t ra = sbase + RA_OFF + sa * RA_SLOT_BYTES;
-      const uint32_t rb = sbase + RB_OFF + sbv * RB_SLOT_BYTES;
-      // copy k of this thread is chunk sub + 4k: swizzle block k / 2, chunk
-      // sub + 4 (k & 1) within the block's 128-byte row
+      int32_t id0 = load_id(0), id1 = load_id(1);
+      for (int t = 0; t < T; ++t) {
+        const int32_t id = id0;
+        id0 = id1;
+        id1 = load_id(t + 2);
+        const bool v = id >= 0 && id < n_kv;
+        const char *src = kv + (v ? (int64_t)id * ROWB : 0);
+        if ((t & 1) == c) {
+          const int sa = ig % RA_SLOTS, so = ig % VO_SLOTS;
+          if (ig >= RA_SLOTS && !bar_wait(bar(B_EMPTYA + sa), ((ig / RA_SLOTS) - 1) & 1)) {
+            timed_out = true;
+            break;
+          }
+          if (ig >= VO_SLOTS && !bar_wait(bar(B_EMPTYVO + so), ((ig / VO_SLOTS) - 1) & 1)) {
+            timed_out = true;
+            break;
+          }
+          const uint32_t ra = sbase + RA_OFF + sa * RA_SLOT_BYTES;
+          const uint32_t rv = sbase + VO_OFF + so * V_SLOT_BYTES;
+          // copy k of this thread is chunk sub + 4k: swizzle block k / 2,
+          // chunk sub + 4 (k & 1) within the block's 128-byte row
 #pragma unroll
-      for (int k = 0; k < NCH / 4; ++k) {
-        const int ch = sub + 4 * k;
-        cp_async16(kv_block(ra, rb, c, k >> 1) + sw128(key, ch & 7), v ? src + ch * 16 : q, v);
+          for (int k = 0; k < NCH / 4; ++k) {
+            const int ch = sub + 4 * k;
+            cp_async16(kv_block(ra, rv, c, k >> 1) + sw128(key, ch & 7), v ? src + ch * 16 : q, v);
+          }
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar(B_FULLA + sa))
+                       : "memory");
+          ++ig;
+        } else {
+          const int sp = jg % VP_SLOTS;
+          if (jg >= VP_SLOTS && !bar_wait(bar(B_EMPTYVP + sp), ((jg / VP_SLOTS) - 1) & 1)) {
+            timed_out = true;
+            break;
+          }
+          const uint32_t rv = sbase + VP_OFF + sp * V_SLOT_BYTES;
+          // only this CTA's value half: copies k = 8c .. 8c + 7 of the 18
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int ch = sub + 4 * (8 * c + k);
+            cp_async16(rv + (k >> 1) * KV_BLOCK_BYTES + sw128(key, ch & 7), v ? src + ch * 16 : q, v);
+          }
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar(B_FULLVP + sp))
+                       : "memory");
+          ++jg;
+        }
       }
-      // the tile's barrier gets this thread's arrival when its copies land
-      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(
-                       bar(B_FULL + sa))
-                   : "memory");
     }
     cp_async_wait<0>();
   } else if (warp >= 8 && warp < 8 + NSB) {
-    // ------------------------------------------ Q K^T issuers (3 warps) ----
-    // warp 8 + b issues tiles t = b, b + 3, ... into S buffer b, so three
-    // 36-instruction chains are in flight at once
+    // ------------------------------------- Q K^T issuers (own tiles) ----
+    // warp 8 + b issues own tiles ig = b, b + 2, ... into S buffer b
     if (lane == 0) {
       const uint32_t qs0 = sbase + QS_OFF;
-      const int sb = warp - 8;
+      const int b = warp - 8;
       bool ok = true;
-      for (int t = sb; t < T && ok; t += NSB) {
-        const int sa = t % RA_SLOTS;
-        ok = bar_wait(bar(B_FULL + sa), (t / RA_SLOTS) & 1);
-        if (ok && t >= NSB) ok = bar_wait(bar(B_SFREE + sb), ((t / NSB) - 1) & 1);
-        if (!ok) break;
-        fence_after();
-        fence_proxy_async();   // the tile was written by cp.async (generic proxy)
-        const uint32_t ra = sbase + RA_OFF + sa * RA_SLOT_BYTES;
-        const uint32_t rb = sbase + RB_OFF + (t % RB_SLOTS) * RB_SLOT_BYTES;
-        const uint32_t sd = tmem + COL_S + sb * NK;
-#pragma unroll
-        for (int kk = 0; kk < QT_DIMS / 16; ++kk)
-          mma_ts(sd, tmem + COL_Q + kk * 8,
-                 sdesc(kv_block(ra, rb, c, kk >> 2) + (kk & 3) * 32, 16, 1024), IDESC_QK, kk > 0);
-#pragma unroll
-        for (int kk = QT_DIMS / 16; kk < D / 16; ++kk) {
-          const int qk = kk - QT_DIMS / 16;
-          mma_ss(sd, sdesc(qs0 + (qk >> 2) * (HG * 128) + (qk & 3) * 32, 16, 1024),
-                 sdesc(kv_block(ra, rb, c, kk >> 2) + (kk & 3) * 32, 16, 1024), IDESC_QK, 1);
+      for (int pass = 0; pass < 2 && ok; ++pass) {
+        if (pass == 1) {
+          ok = bar_wait(bar(B_DECIDE), 0);
+          if (!ok || !*s_redo) break;
         }
-        mma_commit(bar(B_SFULL + sb));
-        mma_commit(bar(B_EMPTYA + sa));   // ring A slot: Q K^T was its last reader
+        for (int il = 0; il < n_own && ok; ++il) {
+          const int ig = pass * n_own + il;
+          if (ig % NSB != b) continue;
+          const int sa = ig % RA_SLOTS;
+          ok = bar_wait(bar(B_FULLA + sa), (ig / RA_SLOTS) & 1);
+          if (ok && ig >= NSB) ok = bar_wait(bar(B_SFREE + b), ((ig / NSB) - 1) & 1);
+          if (!ok) break;
+          fence_after();
+          fence_proxy_async();   // the tile was written by cp.async (generic proxy)
+          const uint32_t ra = sbase + RA_OFF + sa * RA_SLOT_BYTES;
+          const uint32_t rv = sbase + VO_OFF + (ig % VO_SLOTS) * V_SLOT_BYTES;
+          const uint32_t sd = tmem + COL_S + b * NK;
+#pragma unroll
+          for (int kk = 0; kk < QT_DIMS / 16; ++kk)
+            mma_ts(sd, tmem + COL_Q + kk * 8,
+                   sdesc(kv_block(ra, rv, c, kk >> 2) + (kk & 3) * 32, 16, 1024), IDESC_QK, kk > 0);
+#pragma unroll
+          for (int kk = QT_DIMS / 16; kk < D / 16; ++kk) {
+            const int qk = kk - QT_DIMS / 16;
+            mma_ss(sd, sdesc(qs0 + (qk >> 2) * (HG * 128) + (qk & 3) * 32, 16, 1024),
+                   sdesc(kv_block(ra, rv, c, kk >> 2) + (kk & 3) * 32, 16, 1024), IDESC_QK, 1);
+          }
+          mma_commit(bar(B_SFULL + b));
+          mma_commit(bar(B_EMPTYA + sa));   // ring A slot: Q K^T was its last reader
+        }
       }
       timed_out = !ok;
     }
   } else if (warp == 8 + NSB) {
-    // --------------------------------------------------- P V issuer ----
+    // ------------------------------------ P V issuer (every tile, in order) ----
     if (lane == 0) {
       bool ok = true;
-      for (int u = 0; u < T && ok; ++u) {
-        const int sb = u % NSB, sbv = u % RB_SLOTS;
-        ok = bar_wait(bar(B_PFULL + sb), (u / NSB) & 1);
-        if (!ok) break;
-        fence_after();
-        const uint32_t vbase = sbase + RB_OFF + sbv * RB_SLOT_BYTES;
+      int ig = 0, jg = 0;
+      for (int pass = 0; pass < 2 && ok; ++pass) {
+        if (pass == 1) {
+          ok = bar_wait(bar(B_DECIDE), 0);
+          if (!ok || !*s_redo) break;
+        }
+        for (int t = 0; t < T && ok; ++t) {
+          if ((t & 1) == c) {
+            const int sb = ig % NSB, so = ig % VO_SLOTS;
+            ok = bar_wait(bar(B_PFULL + sb), (ig / NSB) & 1);
+            if (!ok) break;
+            fence_after();
+            const uint32_t vb = sbase + VO_OFF + so * V_SLOT_BYTES;
 #pragma unroll
-        for (int ks = 0; ks < NK / 16; ++ks)
-          mma_ts(tmem + COL_O, tmem + COL_S + sb * NK + ks * 8,
-                 sdesc(vbase + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (u > 0 || ks > 0));
-        mma_commit(bar(B_SFREE + sb));    // S/P buffer may take tile u + 3
-        mma_commit(bar(B_EMPTYB + sbv));  // ring B slot may take tile u + 5
+            for (int ks = 0; ks < NK / 16; ++ks)
+              mma_ts(tmem + COL_O, tmem + COL_S + sb * NK + ks * 8,
+                     sdesc(vb + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (t > 0 || ks > 0));
+            mma_commit(bar(B_SFREE + sb));    // S / P buffer may take own tile ig + 2
+            mma_commit(bar(B_EMPTYVO + so));
+            ++ig;
+          } else {
+            const int sp = jg % VP_SLOTS, xs = jg % XP_SLOTS;
+            ok = bar_wait(bar(B_FULLVP + sp), (jg / VP_SLOTS) & 1);
+            if (ok) {
+              arrive_expect_tx(bar(B_XPFULL + xs), HG * 64);
+              ok = bar_wait_cluster(bar(B_XPFULL + xs), (jg / XP_SLOTS) & 1);
+            }
+            if (!ok) break;
+            fence_after();
+            fence_proxy_async();   // V by cp.async, P by st.async
+            const uint32_t vb = sbase + VP_OFF + sp * V_SLOT_BYTES;
+#pragma unroll
+            for (int ks = 0; ks < NK / 16; ++ks)
+              mma_ss(tmem + COL_O, sdesc(sbase + XP_OFF + xs * 64 + ks * 32, 16, 1024),
+                     sdesc(vb + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (t > 0 || ks > 0));
+            mma_commit(bar(B_EMPTYVP + sp));
+            mma_commit_multicast(bar(B_XPFREE + xs), (uint16_t)(1u << peer));   // the peer may refill
+            ++jg;
+          }
+        }
+        if (ok && T > 0) mma_commit(bar(B_OFULL + pass));
       }
-      if (ok && T > 0) mma_commit(bar(B_OFULL));
       timed_out = !ok;
     }
-  } else {
-    // ---------------------------------------------- softmax (warps 0-3) ----
+  } else if (warp < 4) {
+    // -------------------------------- softmax + P exchange (warps 0-3) ----
     const int hrow = tid;                          // head row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    float m_used = -INFINITY, l = 0.f;
-    // index of key `lane` of tile t, loaded a tile ahead
+    const uint32_t peer_xp = peer_addr(sbase + XP_OFF, peer) + (uint32_t)hrow * 128;
+    float ref = 0.f, l = 0.f, l_peer = 0.f, m_ex = -INFINITY;
+    bool flag = false, ref_unset = false, decided = false;
+    int ig = 0, last_pass = 0;
     auto load_id = [&](int t) -> int32_t {
       return (t < T && t * NK + lane < K) ? __ldg(idx_row + t * NK + lane) : -1;
     };
-    int32_t my_id = load_id(0);
-    for (int t = 0; t < T; ++t) {
-      const int sb = t % NSB;
-      if (!warp_wait(bar(B_SFULL + sb), (t / NSB) & 1)) { timed_out = true; break; }
-      fence_after();
-      uint32_t sr[NK];
-      TMEM_LD32(lane_base + COL_S + sb * NK, sr);
-      tmem_wait_ld();
-
-      // invalid keys -> -inf in place (warp-uniform skip when all are valid)
-      const uint32_t vmask = __ballot_sync(0xffffffffu, my_id >= 0 && my_id < n_kv);
-      my_id = load_id(t + 1);
-      if (vmask != 0xffffffffu) {
-#pragma unroll
-        for (int k = 0; k < NK; ++k)
-          if (!((vmask >> k) & 1u)) sr[k] = 0xff800000u;
+    // the peer's first-tile maxima, taken once
+    auto agree_ref = [&](float mt) -> bool {
+      st_async_b32(peer_addr(sbase + XMAX_OFF, peer) + hrow * 4, __float_as_uint(mt),
+                   peer_addr(bar(B_XMAX), peer));
+      if (!warp_wait_cluster(bar(B_XMAX), 0)) return false;
+      const float pm = reinterpret_cast<volatile float *>(sm + XMAX_OFF)[hrow];
+      ref = fmaxf(mt, pm);
+      if (ref == -INFINITY) {   // neither first tile has a valid key
+        ref = 0.f;
+        ref_unset = true;
       }
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      return true;
+    };
+    if (tid == 0) arrive_expect_tx(bar(B_XMAX), HG * 4);
+    for (int pass = 0; pass < 2 && !timed_out; ++pass) {
+      if (tid == 0) arrive_expect_tx(bar(B_XEND + pass), HG * 16);
+      int32_t my_id = load_id(c);
+      for (int il = 0; il < n_own; ++il, ++ig) {
+        const int t = 2 * il + c;
+        const int sb = ig % NSB;
+        if (!warp_wait(bar(B_SFULL + sb), (ig / NSB) & 1)) { timed_out = true; break; }
+        fence_after();
+        uint32_t sr[NK];
+        TMEM_LD32(lane_base + COL_S + sb * NK, sr);
+        tmem_wait_ld();
+
+        // invalid keys -> -inf in place (warp-uniform skip when all are valid)
+        const uint32_t vmask = __ballot_sync(0xffffffffu, my_id >= 0 && my_id < n_kv);
+        my_id = load_id(t + 2);
+        if (vmask != 0xffffffffu) {
 #pragma unroll
-      for (int k = 0; k < NK; ++k) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(sr[k]));
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
-      // lazy rescale: only when the running max grows by more than 8 (log2)
-      const bool grow = mt > m_used + 8.0f;
-      const bool need_o = grow && m_used != -INFINITY;
-      if (__any_sync(0xffffffffu, need_o)) {
-        // O must hold every PV issued so far before it is rescaled
-        if (t >= 1 && !warp_wait(bar(B_SFREE + (t - 1) % NSB), ((t - 1) / NSB) & 1)) {
+          for (int k = 0; k < NK; ++k)
+            if (!((vmask >> k) & 1u)) sr[k] = 0xff800000u;
+        }
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int k = 0; k < NK; ++k) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(sr[k]));
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+        if (pass == 0) {
+          m_ex = fmaxf(m_ex, mt);
+          if (il == 0 && !agree_ref(mt)) { timed_out = true; break; }
+          if (ref_unset ? (mt != -INFINITY) : (mt > ref + REF_SLACK)) flag = true;
+        }
+
+        // P = exp2(s * scale - ref) as bf16 pairs over the first 16 columns
+        // of the S buffer (P V reads it from TMEM as its A operand)
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < NK / 2; ++k) {
+          const float a = ex2(fmaf(__uint_as_float(sr[2 * k]), scale_log2, -ref));
+          const float b = ex2(fmaf(__uint_as_float(sr[2 * k + 1]), scale_log2, -ref));
+          ps[k & 3] += a + b;
+          sr[k] = pack_bf16(a, b);          // in place: pair k of P
+        }
+        l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        TMEM_ST16(lane_base + COL_S + sb * NK, sr);
+        tmem_wait_st();
+        fence_before();
+        __syncwarp();
+        if (lane == 0) bar_arrive(bar(B_PFULL + sb));
+
+        // the same P to the peer: slot ig % 2 of its P buffer, 128-byte
+        // swizzled K-major rows (the A operand layout of its P V)
+        const int xs = ig % XP_SLOTS;
+        if (ig >= XP_SLOTS && !warp_wait_cluster(bar(B_XPFREE + xs), ((ig / XP_SLOTS) - 1) & 1)) {
           timed_out = true;
           break;
         }
-        fence_after();
-        const float alpha = need_o ? ex2(m_used - mt) : 1.0f;
-#pragma unroll 1
-        for (int part = 0; part < 256 / 32; ++part) {
-          uint32_t o[32];
-          TMEM_LD32(lane_base + COL_O + part * 32, o);
-          tmem_wait_ld();
+        const uint32_t rbar = peer_addr(bar(B_XPFULL + xs), peer);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-          TMEM_ST32(lane_base + COL_O + part * 32, o);
-        }
-        tmem_wait_st();
-        if (need_o) l *= alpha;
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_async_v4(peer_xp + ((uint32_t)((xs * 4 + q4) ^ (hrow & 7)) << 4), sr[4 * q4],
+                      sr[4 * q4 + 1], sr[4 * q4 + 2], sr[4 * q4 + 3], rbar);
       }
-      if (grow) m_used = mt;
+      if (timed_out) break;
+      if (pass == 0 && n_own == 0 && !agree_ref(-INFINITY)) { timed_out = true; break; }
 
-      // P = exp2(s * scale - m) as bf16 over the first 16 columns of the same
-      // buffer (P V reads it from TMEM as its A operand)
-      const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int k = 0; k < NK / 2; ++k) {
-        const float a = ex2(fmaf(__uint_as_float(sr[2 * k]), scale_log2, -mu));
-        const float b = ex2(fmaf(__uint_as_float(sr[2 * k + 1]), scale_log2, -mu));
-        ps[k & 3] += a + b;
-        sr[k] = pack_bf16(a, b);          // in place: pair k of P
-      }
-      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      TMEM_ST16(lane_base + COL_S + sb * NK, sr);
-      tmem_wait_st();
-      fence_before();
+      // end of pass: (l, running max, flag) to the peer, the peer's back
+      st_async_v4(peer_addr(sbase + XEND_OFF + pass * HG * 16, peer) + hrow * 16, __float_as_uint(l),
+                  __float_as_uint(m_ex), flag ? 1u : 0u, 0u, peer_addr(bar(B_XEND + pass), peer));
+      if (!warp_wait_cluster(bar(B_XEND + pass), 0)) { timed_out = true; break; }
+      const volatile uint32_t *pe =
+          reinterpret_cast<const volatile uint32_t *>(sm + XEND_OFF + pass * HG * 16) + hrow * 4;
+      l_peer = __uint_as_float(pe[0]);
+      const float m_peer = __uint_as_float(pe[1]);
+      const bool f_peer = pe[2] != 0u;
+      last_pass = pass;
+      if (pass == 1) break;
+      // second pass iff any head of either CTA was marked
+      if (__any_sync(0xffffffffu, flag || f_peer) && lane == 0) atomicOr((uint32_t *)s_redo, 1u);
       __syncwarp();
-      if (lane == 0) bar_arrive(bar(B_PFULL + sb));
+      if (lane == 0) bar_arrive(bar(B_VOTE));
+      if (!warp_wait(bar(B_VOTE), 0)) { timed_out = true; break; }
+      const bool redo = *s_redo != 0u;
+      if (tid == 0) bar_arrive(bar(B_DECIDE));
+      decided = true;
+      if (!redo) break;
+      ref = fmaxf(m_ex, m_peer);
+      if (ref == -INFINITY) ref = 0.f;
+      l = 0.f;
     }
+    if (!decided && tid == 0) bar_arrive(bar(B_DECIDE));   // lets the other roles wind down
 
     // ---------------------------------------------------------- epilogue --
     const int h = h0 + hrow;
-    if (!timed_out && T > 0 && !warp_wait(bar(B_OFULL), 0)) timed_out = true;
+    const float lt = l + l_peer;
+    if (!timed_out && T > 0 && !warp_wait(bar(B_OFULL + last_pass), 0)) timed_out = true;
     fence_after();
-    const float inv = l > 0.f ? 1.0f / l : 0.f;
+    const float inv = lt > 0.f ? 1.0f / lt : 0.f;
     __nv_bfloat16 *orow = out + ((int64_t)r * H + (h < H ? h : 0)) * DV + 256 * c;
 #pragma unroll 1
     for (int part = 0; part < 256 / 32; ++part) {
@@ -507,12 +714,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     if (lse && c == 0 && h < H)
-      lse[(int64_t)r * H + h] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+      lse[(int64_t)r * H + h] = lt > 0.f ? (ref + log2f(lt)) * 0.69314718055994530942f : -INFINITY;
+
+    // every P sent must have been consumed by the peer (its multicast commit
+    // arrives here) before this CTA's shared memory goes away
+    if (tid == 0 && !timed_out) {
+      for (int xs = 0; xs < XP_SLOTS; ++xs) {
+        const int uses = ig > xs ? (ig - xs + XP_SLOTS - 1) / XP_SLOTS : 0;
+        if (uses > 0 && !bar_wait_cluster(bar(B_XPFREE + xs), (uses - 1) & 1)) timed_out = true;
+      }
+    }
   }
 
   if (timed_out && status) atomicOr(status, 4u);
   fence_before();
-  __syncthreads();
+  cluster_sync();          // the peer writes into this CTA's shared memory until here
   if (warp == 0) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem));
@@ -538,15 +754,15 @@ extern "C" int hs_sparse_attn_decode(const void *q, const void *kv, int64_t n_kv
   HS_CUDA_TRY(cudaGetDevice(&dev));
   static bool attr_done[64] = {false};
   if (dev >= 64 || !attr_done[dev]) {
-    HS_CUDA_TRY(cudaFuncSetAttribute(k_attn_umma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    HS_CUDA_TRY(cudaFuncSetAttribute(k_attn_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      SMEM_ALLOC));
     if (dev < 64) attr_done[dev] = true;
   }
   const int64_t blocks = (int64_t)R * ((H + HG - 1) / HG) * 2;
   if (blocks > INT32_MAX) return hs_set_error(HS_ERR_UNSUPPORTED, "R*H too large");
-  k_attn_umma<<<(unsigned)blocks, THREADS, SMEM_ALLOC, stream>>>(
+  k_attn_pair<<<(unsigned)blocks, THREADS, SMEM_ALLOC, stream>>>(
       reinterpret_cast<const char *>(q), reinterpret_cast<const char *>(kv), n_kv_rows, idx, H,
       K, scale * 1.4426950408889634f, reinterpret_cast<__nv_bfloat16 *>(out), lse, status);
-  HS_LAUNCH_CHECK("k_attn_umma");
+  HS_LAUNCH_CHECK("k_attn_pair");
   return HS_OK;
 }

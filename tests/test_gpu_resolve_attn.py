@@ -86,7 +86,10 @@ def test_attention_single_valid_key_is_exact():
     assert torch.equal(out[1].cpu(), kv[3, :512].expand(128, 512))
 
 
-def test_attention_planted_dominant_key():
+@pytest.mark.parametrize("pos", [17, 250])
+def test_attention_planted_dominant_key(pos):
+    # at 17 the key is in the first tile; at 250 it is far above every score
+    # seen before it, so the kernel must switch to its exact-maximum pass
     hs = lib()
     g = np.random.default_rng(4)
     H, K, N = 128, 300, 400
@@ -96,7 +99,8 @@ def test_attention_planted_dominant_key():
     kv[:, 0] = 0.0
     kv[123, 0] = 60.0                           # logit >= 50 above all others (scale 1)
     idx = g.permutation(N)[:K].astype(np.int32)
-    idx[17] = 123
+    idx[idx == 123] = idx[pos]
+    idx[pos] = 123
     q, kv = _bf16(q), _bf16(kv)
     out = torch.empty((1, H, 512), dtype=torch.bfloat16, device=DEV)
     hs.hs_sparse_attn_decode(q.to(DEV), kv.to(DEV), torch.as_tensor(idx[None], device=DEV),
@@ -106,6 +110,24 @@ def test_attention_planted_dominant_key():
     want = kv[123, :512].float().expand(H, 512)
     ulp = torch.abs(want) * 2.0 ** -7 + 1e-30
     assert ((got - want).abs() <= ulp).all()
+
+
+@pytest.mark.parametrize("lead", [64, 96])
+def test_attention_leading_padding(lead):
+    # rows whose first `lead` entries are padding: no score to take the softmax
+    # reference from until later tiles
+    hs = lib()
+    R, H, K, N = 3, 128, 300, 1000
+    q, kv, idx = _attn_case(lead, R, H, K, N, sharp=True)
+    idx[:, :lead] = -1
+    scale = 1.0 / 24
+    ref, ref_lse = O.sparse_attn_decode(q, kv, idx, scale)
+    out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((R, H), dtype=torch.float32, device=DEV)
+    hs.hs_sparse_attn_decode(q.to(DEV), kv.to(DEV), torch.as_tensor(idx, device=DEV), scale,
+                             out, lse)
+    torch.cuda.synchronize()
+    check_attn(out, ref, lse, ref_lse)
 
 
 def test_workload2_full_size():
