@@ -383,16 +383,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
 
-  // Q dims 384..575 -> SMEM (three 64-dim swizzle blocks), all threads
-  for (int i = tid; i < HG * QS_BLOCKS * 8; i += THREADS) {
-    const int hr = i / (QS_BLOCKS * 8), rem = i % (QS_BLOCKS * 8);
-    const int j = rem / 8, cc = rem % 8;
+  // Q in one round of copies by all threads: dims 384..575 -> SMEM (three
+  // 64-dim swizzle blocks, the MMA's A operand), dims 0..383 -> a staging
+  // area in the (still empty) KV rings, 768 B per head with its 16-byte
+  // chunks permuted within groups of 8 so that the per-head reads below do
+  // not collide on banks
+  constexpr int QT_CH = QT_DIMS / 8;                       // 48 chunks per head
+  static_assert(HG * QT_CH * 16 <= VP_OFF - RA_OFF, "Q staging fits rings A and VO");
+  for (int i = tid; i < HG * (QS_BLOCKS * 8 + QT_CH); i += THREADS) {
+    const int hr = i / (QS_BLOCKS * 8 + QT_CH), rem = i % (QS_BLOCKS * 8 + QT_CH);
     const int h = h0 + hr;
     const bool v = h < H;
-    const char *src = v ? q + ((int64_t)r * H + h) * ROWB + (QT_DIMS + 64 * j) * 2 + cc * 16 : q;
-    cp_async16(sbase + QS_OFF + j * (HG * 128) + sw128(hr, cc), src, v);
+    const char *qrow = q + ((int64_t)r * H + (v ? h : 0)) * ROWB;
+    if (rem < QT_CH) {
+      cp_async16(sbase + RA_OFF + hr * (QT_CH * 16) + ((rem ^ (hr & 7)) << 4), v ? qrow + rem * 16 : q, v);
+    } else {
+      const int j = (rem - QT_CH) / 8, cc = (rem - QT_CH) % 8;
+      cp_async16(sbase + QS_OFF + j * (HG * 128) + sw128(hr, cc),
+                 v ? qrow + (QT_DIMS + 64 * j) * 2 + cc * 16 : q, v);
+    }
   }
   cp_async_commit();
+  cp_async_wait<0>();
 
   fence_before();
   __syncthreads();
@@ -400,28 +412,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    // Q dims 0..383 -> TMEM columns [256, 448): lane = head, column j holds
-    // dims 2j, 2j+1
-    const int h = h0 + tid;
-    const uint4 *qrow = reinterpret_cast<const uint4 *>(q + ((int64_t)r * H + (h < H ? h : 0)) * ROWB);
+    // staged Q dims 0..383 -> TMEM columns [256, 448): lane = head, column j
+    // holds dims 2j, 2j+1
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const unsigned char *stage = sm + RA_OFF + tid * (QT_CH * 16);
 #pragma unroll 1
     for (int part = 0; part < QT_DIMS / 64; ++part) {
       uint32_t v[32];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (h < H) w = qrow[part * 8 + k];
+        const int ch = part * 8 + k;
+        const uint4 w = *reinterpret_cast<const uint4 *>(stage + ((ch ^ (tid & 7)) << 4));
         v[4 * k] = w.x; v[4 * k + 1] = w.y; v[4 * k + 2] = w.z; v[4 * k + 3] = w.w;
       }
       TMEM_ST32(lane_base + COL_Q + part * 32, v);
     }
     tmem_wait_st();
   }
-  cp_async_wait<0>();
   fence_proxy_async();
   fence_before();
-  cluster_sync();          // both CTAs' barriers exist before any remote operation
+  cluster_sync();          // both CTAs' barriers exist before any remote operation,
+                           // and the Q staging area is free for KV tiles
   fence_after();
 
   bool timed_out = false;
