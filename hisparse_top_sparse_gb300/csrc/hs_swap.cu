@@ -34,7 +34,7 @@ namespace {
 
 constexpr int SW_THREADS = 1024;
 constexpr int ROW_CHUNK = 1024;   // rows of one request handled per pass
-constexpr int PB = 4;             // entries per thread per probe / table round
+constexpr int PB = 8;             // entries per thread per probe / table round
 
 struct SwapArgs {
   const int32_t *req_id, *clen, *kv_len, *topk;
@@ -80,13 +80,28 @@ __host__ __device__ inline int pow2_ceil(int x) {
   return p;
 }
 
-// Shared-memory layout (bytes): mkey[nS] i32 (misses, sorted) | ord[S] i32
-// (LRU order) | vict[S] i32 (victim slots) | hit / touched bitmap [S/32] u32 |
-// rows[ROW_CHUNK] i32 | row valid counts [ROW_CHUNK] i32
-__host__ __device__ inline size_t swap_smem_bytes(int S) {
-  const int nS = pow2_ceil(S);
-  return (size_t)nS * 4 + (size_t)S * 8 + (size_t)((S + 31) / 32) * 4 + ROW_CHUNK * 8;
+// Misses are put in ascending position order by rank in a bitmap of the
+// request's committed positions (one bit per position, a prefix count per
+// 32-bit word) when that fits in shared memory, else by a bitonic sort.
+constexpr int RANK_MAX_WORDS = 8192;   // positions < 262144
+
+__host__ __device__ inline int rank_words(int max_ctx) {
+  const int w = (max_ctx + 31) / 32;
+  return w <= RANK_MAX_WORDS ? w : 0;
 }
+
+// Shared-memory layout (bytes): mkey[nS] i32 (misses) | ord[S] i32 (LRU
+// order) | vict[S] i32 (victim slots) | hit / touched bitmap [S/32] u32 |
+// rows[ROW_CHUNK] i32 | row valid counts [ROW_CHUNK] i32 | miss bitmap [W]
+// u32 | its word prefix counts [W] i32 | needed-position bitmap [W] u32
+// (W = rank_words(max_ctx); with W = 0 the claims go through pos_mark and the
+// misses are sorted)
+__host__ __device__ inline size_t swap_smem_bytes(int S, int max_ctx) {
+  const int nS = pow2_ceil(S);
+  return (size_t)nS * 4 + (size_t)S * 8 + (size_t)((S + 31) / 32) * 4 + ROW_CHUNK * 8 +
+         (size_t)rank_words(max_ctx) * 12;
+}
+constexpr int ORD_REGS = HS_MAX_SLOTS / SW_THREADS;   // LRU order entries a thread prefetches
 
 __device__ __forceinline__ bool bit_of(const uint32_t *bm, int s) { return (bm[s >> 5] >> (s & 31)) & 1u; }
 
@@ -147,6 +162,10 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
   uint32_t *hitmap = reinterpret_cast<uint32_t *>(vict + a.S);
   int32_t *rows = reinterpret_cast<int32_t *>(hitmap + (a.S + 31) / 32);
   int32_t *rvalid = rows + ROW_CHUNK;
+  const int nW = rank_words(a.max_ctx);
+  uint32_t *pbm = reinterpret_cast<uint32_t *>(rvalid + ROW_CHUNK);
+  int32_t *pwp = reinterpret_cast<int32_t *>(pbm + nW);
+  uint32_t *pneed = reinterpret_cast<uint32_t *>(pwp + nW);
   __shared__ int s_need, s_miss, s_cnt, s_any, s_bad;
   __shared__ int scan_tmp[33];
   const int lane = threadIdx.x & 31;
@@ -158,15 +177,35 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
   const int32_t L = a.kv_len[b];
   const int64_t cbase = (int64_t)b * a.max_ctx;
   const int64_t sbase = (int64_t)b * a.S;
+  // the request's LRU order, loaded now and put in shared memory after the
+  // probe, so its latency hides behind the probe
+  int32_t ordv[ORD_REGS];
+#pragma unroll
+  for (int u = 0; u < ORD_REGS; ++u) {
+    const int i = u * SW_THREADS + (int)threadIdx.x;
+    ordv[u] = i < a.S ? a.lru_order[sbase + i] : 0;
+  }
+  // a position is claimed once per call: first setter of its bit in the
+  // needed-position bitmap (or of its pos_mark epoch when that does not fit)
+  const bool use_bm = nW > 0;
+  if (use_bm)
+    for (int w = threadIdx.x; w < (L + 31) / 32; w += SW_THREADS) pneed[w] = 0u;
+  __syncthreads();
+  // a request whose entries take one probe round keeps them in registers for
+  // the table
+  int32_t keep_t[PB], keep_clen[PB];
+  bool single = false;
 
   // ---- probe ----------------------------------------------------------------
   for (int from = 0; from < a.R;) {
     int next;
+    const int first_chunk = from == 0;
     const int n = collect_rows(a, b, from, rows, &next, &s_cnt);
     from = next;
     if (n == 0) break;
     if (threadIdx.x == 0) s_any = 1;
     const int items = n * a.K;
+    single = first_chunk && next >= a.R && items <= SW_THREADS * PB;
     // PB entries per thread per round: their loads, claims and lookups are all
     // in flight together (each is a dependent global access)
     for (int base = 0; base < items; base += SW_THREADS * PB) {
@@ -185,8 +224,15 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
       }
 #pragma unroll
       for (int u = 0; u < PB; ++u) {
+        keep_t[u] = t[u];
+        keep_clen[u] = clen[u];
         const bool committed = t[u] >= 0 && t[u] < clen[u] && t[u] < L && t[u] < a.max_ctx;
-        first[u] = committed && atomicExch(&a.pos_mark[cbase + t[u]], a.epoch) != a.epoch;
+        if (use_bm) {
+          const uint32_t bit = 1u << (committed ? (t[u] & 31) : 0);
+          first[u] = committed && !(atomicOr(&pneed[committed ? (t[u] >> 5) : 0], bit) & bit);
+        } else {
+          first[u] = committed && atomicExch(&a.pos_mark[cbase + t[u]], a.epoch) != a.epoch;
+        }
       }
 #pragma unroll
       for (int u = 0; u < PB; ++u) sl[u] = first[u] ? a.token_slot[cbase + t[u]] : -1;
@@ -230,7 +276,11 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
     // victims: the first nm slots of the LRU order (ascending (ts, slot)) that
     // hold no position needed in this call
     int32_t *lru = a.lru_order + sbase;
-    for (int i = threadIdx.x; i < a.S; i += SW_THREADS) ord[i] = lru[i];
+#pragma unroll
+    for (int u = 0; u < ORD_REGS; ++u) {
+      const int i = u * SW_THREADS + (int)threadIdx.x;
+      if (i < a.S) ord[i] = ordv[u];
+    }
     __syncthreads();
     {
       const int E = (a.S + SW_THREADS - 1) / SW_THREADS;
@@ -251,16 +301,38 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
     for (int sl = threadIdx.x; sl < a.S; sl += SW_THREADS)
       if (bit_of(hitmap, sl)) a.slot_ts[sbase + sl] = a.now;
     if (nm > 0) {
-      // misses in ascending position order take the victims in order
-      const int nM = pow2_ceil(nm);
-      for (int i = nm + threadIdx.x; i < nM; i += SW_THREADS) mkey[i] = INT32_MAX;
-      __syncthreads();
-      block_bitonic_sort(mkey, nM);
+      // misses in ascending position order take the victims in order: the
+      // i-th smallest miss position gets vict[i]
+      const bool by_rank = nW > 0 && L <= nW * 32;
+      if (by_rank) {
+        const int W = (L + 31) / 32;
+        for (int w = threadIdx.x; w < W; w += SW_THREADS) pbm[w] = 0u;
+        __syncthreads();
+        for (int i = threadIdx.x; i < nm; i += SW_THREADS)
+          atomicOr(&pbm[mkey[i] >> 5], 1u << (mkey[i] & 31));
+        __syncthreads();
+        const int E = (W + SW_THREADS - 1) / SW_THREADS;
+        const int lo = threadIdx.x * E, hi = min(W, lo + E);
+        int cnt = 0;
+        for (int w = lo; w < hi; ++w) cnt += __popc(pbm[w]);
+        int tot;
+        int k = hs_block_exscan(cnt, scan_tmp, &tot);
+        for (int w = lo; w < hi; ++w) { pwp[w] = k; k += __popc(pbm[w]); }
+        __syncthreads();
+      } else {
+        const int nM = pow2_ceil(nm);
+        for (int i = nm + threadIdx.x; i < nM; i += SW_THREADS) mkey[i] = INT32_MAX;
+        __syncthreads();
+        block_bitonic_sort(mkey, nM);
+      }
+      auto rank_of = [&](int i, int32_t t) -> int {
+        return by_rank ? pwp[t >> 5] + __popc(pbm[t >> 5] & ((1u << (t & 31)) - 1u)) : i;
+      };
       const int32_t *hbt_row = a.hbt + (int64_t)b * a.hbt_stride;
       uint64_t *desc = a.copy_desc + sbase;
       for (int i = threadIdx.x; i < nm; i += SW_THREADS) {
         const int32_t t = mkey[i];
-        const int32_t sl = vict[i];
+        const int32_t sl = vict[rank_of(i, t)];
         const int32_t old = a.slot_token[sbase + sl];
         if (old >= 0 && old < a.max_ctx) a.token_slot[cbase + old] = -1;   // not needed now
         a.slot_token[sbase + sl] = t;
@@ -284,8 +356,9 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
   const int32_t *ts_row = a.token_slot + cbase;
   for (int from = 0; from < a.R;) {
     int next;
-    const int n = collect_rows(a, b, from, rows, &next, &s_cnt);
-    from = next;
+    // with `single`, rows[] still holds the request's only chunk from the probe
+    const int n = single ? s_cnt : collect_rows(a, b, from, rows, &next, &s_cnt);
+    from = single ? a.R : next;
     if (n == 0) break;
     for (int i = threadIdx.x; i < n; i += SW_THREADS) rvalid[i] = 0;
     __syncthreads();
@@ -301,8 +374,8 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
         ri[u] = -1;
         if (i < items) {
           ri[u] = i / a.K;
-          t[u] = a.topk[(int64_t)rows[ri[u]] * a.K + i % a.K];
-          clen[u] = a.clen[rows[ri[u]]];
+          t[u] = single ? keep_t[u] : a.topk[(int64_t)rows[ri[u]] * a.K + i % a.K];
+          clen[u] = single ? keep_clen[u] : a.clen[rows[ri[u]]];
         }
       }
 #pragma unroll
@@ -450,11 +523,11 @@ extern "C" int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
   a.epoch = (uint32_t)buf->clock;
   a.now = buf->clock;
 
-  const size_t smem = swap_smem_bytes(buf->S);
+  const size_t smem = swap_smem_bytes(buf->S, buf->max_ctx);
   static bool attr_set[64] = {false};
   if (buf->device >= 64 || !attr_set[buf->device]) {
     HS_CUDA_TRY(cudaFuncSetAttribute(k_swap_request, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)swap_smem_bytes(HS_MAX_SLOTS)));
+                                     (int)swap_smem_bytes(HS_MAX_SLOTS, RANK_MAX_WORDS * 32)));
     HS_CUDA_TRY(cudaFuncSetAttribute(k_swap_gather, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)((HS_MAX_REQS + 1) * sizeof(int))));
     if (buf->device < 64) attr_set[buf->device] = true;
