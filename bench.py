@@ -229,7 +229,7 @@ def run_ours(args):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "traffic": _traffic(), "peak_kind": peak_kind,
-                "kernel": "k_attn_umma", "algorithmic_bytes_per_launch": alg_bytes,
+                "kernel": "k_attn_pair", "algorithmic_bytes_per_launch": alg_bytes,
                 "attn_ms": round(t_attn * 1e3, 4),
                 "tensor_floor_ms": round(R * H * K * 2 * (576 + 512) / (peaks["bf16_tflops"] * 1e12)
                                          * 1e3, 4)}
@@ -373,7 +373,7 @@ def run_swap_bench(hs, dev, args):
             "cold_step_gbs": round(miss[0] * ROW_BYTES / (swap_ms[0] * 1e-3) / 1e9, 2),
             "attn_ms_per_step_mean": round(statistics.mean(attn_ms[1:]), 4),
             "query_rows_per_s_attention": round(cfg.R / (statistics.mean(attn_ms[1:]) * 1e-3), 1),
-            "status": st, "gpu_launches_per_step": 4}
+            "status": st, "gpu_launches_per_step": 2}
 
 
 def cpu_baseline(cfg, rc, budget_s: float = 12.0):

@@ -10,21 +10,24 @@
 // Two launches. k_swap_request: one 1024-thread block per request that has
 // rows in the call works through that request alone:
 //   probe   every entry of the request's rows: classify it, claim each needed
-//           committed position once per call (epoch-stamped marks), record hit
-//           slots in a shared-memory bitmap, compact misses with
+//           committed position once per call (a shared-memory bitmap of the
+//           request's positions, or epoch-stamped marks when it does not fit),
+//           record hit slots in a shared-memory bitmap, compact misses with
 //           __ballot_sync / __popc into a shared-memory list
 //   assign  capacity check; the victims are the first slots of the request's
 //           LRU order (a persistent array kept in ascending (ts, slot) order)
 //           that hold no needed position (one block prefix scan); the misses,
-//           sorted ascending (bitonic, shared memory), take them in order; hits
-//           and victims take the current time and move to the end of the order
-//           in slot order (two prefix scans) -- no sort over all S slots
-//   table   the hot-row index of every entry and the valid count of every row
+//           in ascending position order (their ranks in a bitmap of miss
+//           positions), take them in order; hits and victims take the current
+//           time and move to the end of the order in slot order (two prefix
+//           scans) -- no sort over all S slots
 //   publish (host pool row, hot slot) of every miss
 // k_swap_gather: every SM copies a share of every request's missed 1152-byte
 // rows from the device-mapped page-locked host pool with 16-byte loads (four
 // in flight per thread): reads over the host link need requests in flight
-// from all SMs to reach the link's bandwidth.
+// from all SMs to reach the link's bandwidth. While those loads are in
+// flight, the same threads write the slot table: the hot-row index of every
+// entry of every row and the valid count of every row.
 // Rows are found by scanning the row descriptors, 1024 rows of the request at
 // a time.
 
@@ -191,21 +194,17 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
   if (use_bm)
     for (int w = threadIdx.x; w < (L + 31) / 32; w += SW_THREADS) pneed[w] = 0u;
   __syncthreads();
-  // a request whose entries take one probe round keeps them in registers for
-  // the table
-  int32_t keep_t[PB], keep_clen[PB];
-  bool single = false;
 
   // ---- probe ----------------------------------------------------------------
   for (int from = 0; from < a.R;) {
     int next;
-    const int first_chunk = from == 0;
     const int n = collect_rows(a, b, from, rows, &next, &s_cnt);
     from = next;
     if (n == 0) break;
     if (threadIdx.x == 0) s_any = 1;
+    if (out_valid)   // counted by the gather's table pass
+      for (int i = threadIdx.x; i < n; i += SW_THREADS) out_valid[rows[i]] = 0;
     const int items = n * a.K;
-    single = first_chunk && next >= a.R && items <= SW_THREADS * PB;
     // PB entries per thread per round: their loads, claims and lookups are all
     // in flight together (each is a dependent global access)
     for (int base = 0; base < items; base += SW_THREADS * PB) {
@@ -224,8 +223,6 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
       }
 #pragma unroll
       for (int u = 0; u < PB; ++u) {
-        keep_t[u] = t[u];
-        keep_clen[u] = clen[u];
         const bool committed = t[u] >= 0 && t[u] < clen[u] && t[u] < L && t[u] < a.max_ctx;
         if (use_bm) {
           const uint32_t bit = 1u << (committed ? (t[u] & 31) : 0);
@@ -267,7 +264,10 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
   const int need = s_need, nm = s_miss;
   const bool failed = need > a.S;
   if (failed) {
-    if (threadIdx.x == 0) atomicOr(a.status, HS_STATUS_CAPACITY);
+    if (threadIdx.x == 0) {
+      atomicOr(a.status, HS_STATUS_CAPACITY);
+      a.copy_cnt[b] = -1;   // the table gives the request's committed entries -1
+    }
   } else {
     if (threadIdx.x == 0 && a.stats) {
       atomicAdd((unsigned long long *)&a.stats[0], (unsigned long long)(need - nm));
@@ -351,75 +351,59 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
   }
   __syncthreads();
 
-  // ---- table: hot-row index of every entry, valid count of every row -------
-  const int32_t row0 = b * a.S_tot;
-  const int32_t *ts_row = a.token_slot + cbase;
-  for (int from = 0; from < a.R;) {
-    int next;
-    // with `single`, rows[] still holds the request's only chunk from the probe
-    const int n = single ? s_cnt : collect_rows(a, b, from, rows, &next, &s_cnt);
-    from = single ? a.R : next;
-    if (n == 0) break;
-    for (int i = threadIdx.x; i < n; i += SW_THREADS) rvalid[i] = 0;
-    __syncthreads();
-    const int items = n * a.K;
-    for (int base = 0; base < items; base += SW_THREADS * PB) {
-      int32_t t[PB], clen[PB], sl[PB];
-      int ri[PB];
-#pragma unroll
-      for (int u = 0; u < PB; ++u) {
-        const int i = base + u * SW_THREADS + (int)threadIdx.x;
-        t[u] = -1;
-        clen[u] = 0;
-        ri[u] = -1;
-        if (i < items) {
-          ri[u] = i / a.K;
-          t[u] = single ? keep_t[u] : a.topk[(int64_t)rows[ri[u]] * a.K + i % a.K];
-          clen[u] = single ? keep_clen[u] : a.clen[rows[ri[u]]];
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < PB; ++u)
-        sl[u] = (!failed && t[u] >= 0 && t[u] < clen[u] && t[u] < L && t[u] < a.max_ctx)
-                    ? ts_row[t[u]] : -1;
-#pragma unroll
-      for (int u = 0; u < PB; ++u) {
-        if (ri[u] < 0) continue;
-        const int32_t tt = t[u];
-        int32_t v = -1;
-        if (tt >= 0 && tt < clen[u]) {
-          if (tt >= L) {
-            if (tt - L < a.S_tot - a.S) v = row0 + a.S + (tt - L);
-          } else if (sl[u] >= 0) {
-            v = row0 + sl[u];
-          }
-        }
-        const int i = base + u * SW_THREADS + (int)threadIdx.x;
-        out[(int64_t)rows[ri[u]] * a.K + i % a.K] = v;
-        if (v >= 0) atomicAdd(&rvalid[ri[u]], 1);
+}
+
+// Arguments of the slot-table pass run inside the gather.
+struct TableArgs {
+  const int32_t *req_id, *clen, *kv_len, *topk, *token_slot, *copy_cnt;
+  int32_t R, K, max_reqs, S, S_tot, max_ctx;
+  int32_t *out, *out_valid;
+  uint32_t *status;
+};
+
+// Entry e = r * K + j of the slot table: the hot-row index of topk[r][j]
+// (-1 for padding, an index error, a refused request or a bad request id).
+__device__ __forceinline__ void table_entry(const TableArgs &ta, int64_t e) {
+  const int r = (int)(e / ta.K), j = (int)(e - (int64_t)r * ta.K);
+  const int32_t b = ta.req_id[r];
+  int32_t v = -1;
+  if (b < 0 || b >= ta.max_reqs) {
+    if (j == 0) {
+      if (ta.out_valid) ta.out_valid[r] = 0;
+      atomicOr(ta.status, HS_STATUS_INDEX);
+    }
+  } else {
+    const int32_t t = ta.topk[e], n = ta.clen[r], L = ta.kv_len[b];
+    if (t >= 0 && t < n) {
+      if (t >= L) {
+        if (t - L < ta.S_tot - ta.S) v = b * ta.S_tot + ta.S + (t - L);
+      } else if (t < ta.max_ctx && ta.copy_cnt[b] >= 0) {
+        const int32_t sl = ta.token_slot[(int64_t)b * ta.max_ctx + t];
+        if (sl >= 0) v = b * ta.S_tot + sl;
       }
     }
-    __syncthreads();
-    if (out_valid)
-      for (int i = threadIdx.x; i < n; i += SW_THREADS) out_valid[rows[i]] = rvalid[i];
-    __syncthreads();
   }
+  ta.out[e] = v;
+  if (v >= 0 && ta.out_valid) atomicAdd(&ta.out_valid[r], 1);
 }
 
 // Chunks of every request's misses are numbered consecutively (a prefix sum
 // over the per-request counts, computed by every block in shared memory) and
-// spread over the whole grid, four 16-byte loads in flight per thread.
+// spread over the whole grid, four 16-byte loads in flight per thread; the
+// slot table's entries are spread the same way and worked on while the
+// loads over the host link are in flight.
 __global__ void __launch_bounds__(256) k_swap_gather(const int32_t *__restrict__ copy_cnt,
                                                      const uint64_t *__restrict__ copy_desc,
                                                      int32_t max_reqs, int32_t S, int32_t S_tot,
                                                      const uint4 *__restrict__ pool,
-                                                     uint4 *__restrict__ hot) {
+                                                     uint4 *__restrict__ hot, TableArgs ta) {
   extern __shared__ int pre[];                     // [max_reqs + 1] chunk offsets
   __shared__ int part[256];
   const int tid = threadIdx.x;
   const int seg = (max_reqs + 255) / 256;
+  auto cnt_of = [&](int i) -> int { const int c = copy_cnt[i]; return c > 0 ? c : 0; };
   int sum = 0;
-  for (int i = tid * seg; i < (tid + 1) * seg && i < max_reqs; ++i) sum += copy_cnt[i] * HS_ROW_VEC16;
+  for (int i = tid * seg; i < (tid + 1) * seg && i < max_reqs; ++i) sum += cnt_of(i) * HS_ROW_VEC16;
   part[tid] = sum;
   __syncthreads();
   if (tid < 32) {                                  // exclusive scan of the 256 partial sums
@@ -440,19 +424,25 @@ __global__ void __launch_bounds__(256) k_swap_gather(const int32_t *__restrict__
     int acc = part[tid];
     for (int i = tid * seg; i < (tid + 1) * seg && i < max_reqs; ++i) {
       pre[i] = acc;
-      acc += copy_cnt[i] * HS_ROW_VEC16;
+      acc += cnt_of(i) * HS_ROW_VEC16;
     }
     if (tid == 255) pre[max_reqs] = acc;
   }
   __syncthreads();
   const int total = pre[max_reqs];
+  const int64_t n_entries = (int64_t)ta.R * ta.K;
   const int step = gridDim.x * blockDim.x;
-  for (int e = blockIdx.x * blockDim.x + tid; e < total; e += 4 * step) {
+  constexpr int TE = 2;                            // table entries per thread per round
+  const int g = blockIdx.x * blockDim.x + tid;
+  for (int it = 0;; ++it) {
+    const int64_t e = (int64_t)g + (int64_t)it * 4 * step;
+    const int64_t te = (int64_t)g + (int64_t)it * TE * step;
+    if (e >= total && te >= n_entries) break;
     uint4 v[4];
     int64_t dst[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int k = e + u * step;
+      const int64_t k = e + (int64_t)u * step;
       dst[u] = -1;
       if (k < total) {
         int lo = 0, hi = max_reqs;                 // request b with pre[b] <= k < pre[b+1]
@@ -460,7 +450,7 @@ __global__ void __launch_bounds__(256) k_swap_gather(const int32_t *__restrict__
           const int mid = (lo + hi) >> 1;
           if (pre[mid] <= k) lo = mid; else hi = mid;
         }
-        const int rel = k - pre[lo];
+        const int rel = (int)k - pre[lo];
         const int i = rel / HS_ROW_VEC16, c = rel % HS_ROW_VEC16;
         const uint64_t d = copy_desc[(int64_t)lo * S + i];
         if (d != ~0ull) {
@@ -469,22 +459,15 @@ __global__ void __launch_bounds__(256) k_swap_gather(const int32_t *__restrict__
         }
       }
     }
+    // slot-table entries while the host reads are in flight
+#pragma unroll
+    for (int u = 0; u < TE; ++u) {
+      const int64_t en = te + (int64_t)u * step;
+      if (en < n_entries) table_entry(ta, en);
+    }
 #pragma unroll
     for (int u = 0; u < 4; ++u)
       if (dst[u] >= 0) hot[dst[u]] = v[u];
-  }
-}
-
-// Rows whose request id is outside the buffer: every entry -1, index status.
-__global__ void k_swap_bad_rows(const int32_t *req_id, int32_t R, int32_t K, int32_t max_reqs,
-                                int32_t *out, int32_t *out_valid, uint32_t *status) {
-  const int r = blockIdx.x;
-  const int32_t b = req_id[r];
-  if (b >= 0 && b < max_reqs) return;
-  for (int j = threadIdx.x; j < K; j += blockDim.x) out[(int64_t)r * K + j] = -1;
-  if (threadIdx.x == 0) {
-    if (out_valid) out_valid[r] = 0;
-    if (K > 0) atomicOr(status, HS_STATUS_INDEX);
   }
 }
 
@@ -540,12 +523,15 @@ extern "C" int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
     HS_CUDA_TRY(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, buf->device));
     if (buf->device < 64) sms[buf->device] = nsm;
   }
+  TableArgs ta;
+  ta.req_id = req_id_per_row; ta.clen = row_causal_len; ta.kv_len = kv_len; ta.topk = topk;
+  ta.token_slot = buf->token_slot; ta.copy_cnt = buf->copy_cnt;
+  ta.R = R; ta.K = K; ta.max_reqs = buf->max_reqs; ta.S = buf->S; ta.S_tot = buf->S_tot;
+  ta.max_ctx = buf->max_ctx;
+  ta.out = out_slot_idx; ta.out_valid = out_valid; ta.status = buf->status;
   const size_t gsmem = (size_t)(buf->max_reqs + 1) * sizeof(int);
   k_swap_gather<<<nsm * 8, 256, gsmem, stream>>>(buf->copy_cnt, buf->copy_desc, buf->max_reqs,
-                                                 buf->S, buf->S_tot, a.pool, a.hot);
+                                                 buf->S, buf->S_tot, a.pool, a.hot, ta);
   HS_LAUNCH_CHECK("k_swap_gather");
-  k_swap_bad_rows<<<R, 128, 0, stream>>>(req_id_per_row, R, K, buf->max_reqs, out_slot_idx,
-                                         out_valid, buf->status);
-  HS_LAUNCH_CHECK("k_swap_bad_rows");
   return HS_OK;
 }
