@@ -43,6 +43,8 @@
 // Every mbarrier wait is bounded; a wait that gives up sets HS_STATUS_TIMEOUT
 // in the caller's status word and the CTA winds down.
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 
 #include "hs_internal.cuh"
@@ -104,7 +106,8 @@ enum {
   B_VOTE = B_XEND + 2,                // the four softmax warps have voted for a second pass
   B_DECIDE = B_VOTE + 1,              // softmax -> other roles: second pass or not
   B_OFULL = B_DECIDE + 1,             // all P V of a pass done (one per pass)
-  B_COUNT = B_OFULL + 2
+  B_QLOAD = B_OFULL + 2,              // Q landed (9 x 16 KB by tensor copies)
+  B_COUNT = B_QLOAD + 1
 };
 static_assert(B_COUNT * 8 + 8 <= 512, "barrier area");
 
@@ -212,9 +215,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool v
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                "r"(valid ? 16 : 0)
                : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -325,9 +325,10 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity)
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-    k_attn_pair(const char *__restrict__ q, const char *__restrict__ kv, int64_t n_kv,
-                const int32_t *__restrict__ idx, int32_t H, int32_t K, float scale_log2,
-                __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, uint32_t *status) {
+    k_attn_pair(const __grid_constant__ CUtensorMap tmap_q, const char *__restrict__ q,
+                const char *__restrict__ kv, int64_t n_kv, const int32_t *__restrict__ idx,
+                int32_t H, int32_t K, float scale_log2, __nv_bfloat16 *__restrict__ out,
+                float *__restrict__ lse, uint32_t *status) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -374,6 +375,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
     bar_init(bar(B_VOTE), 4);
     bar_init(bar(B_DECIDE), 1);
+    bar_init(bar(B_QLOAD), 1);
     *s_redo = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -383,59 +385,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
 
-  // Q in one round of copies by all threads: dims 384..575 -> SMEM (three
-  // 64-dim swizzle blocks, the MMA's A operand), dims 0..383 -> a staging
-  // area in the (still empty) KV rings, 768 B per head with its 16-byte
-  // chunks permuted within groups of 8 so that the per-head reads below do
-  // not collide on banks
-  constexpr int QT_CH = QT_DIMS / 8;                       // 48 chunks per head
-  static_assert(HG * QT_CH * 16 <= VP_OFF - RA_OFF, "Q staging fits rings A and VO");
-  for (int i = tid; i < HG * (QS_BLOCKS * 8 + QT_CH); i += THREADS) {
-    const int hr = i / (QS_BLOCKS * 8 + QT_CH), rem = i % (QS_BLOCKS * 8 + QT_CH);
-    const int h = h0 + hr;
-    const bool v = h < H;
-    const char *qrow = q + ((int64_t)r * H + (v ? h : 0)) * ROWB;
-    if (rem < QT_CH) {
-      cp_async16(sbase + RA_OFF + hr * (QT_CH * 16) + ((rem ^ (hr & 7)) << 4), v ? qrow + rem * 16 : q, v);
-    } else {
-      const int j = (rem - QT_CH) / 8, cc = (rem - QT_CH) % 8;
-      cp_async16(sbase + QS_OFF + j * (HG * 128) + sw128(hr, cc),
-                 v ? qrow + (QT_DIMS + 64 * j) * 2 + cc * 16 : q, v);
-    }
-  }
-  cp_async_commit();
-  cp_async_wait<0>();
-
+  // Q by nine tensor copies of 128 heads x 64 dims (16 KB, 128-byte swizzle,
+  // rows past H filled with zeros), each issued by one CTA of the pair and
+  // multicast to both: dims 384..575 land in SMEM as the MMA's A operand,
+  // dims 0..383 in a staging area in the (still empty) KV rings, from where
+  // each head's thread moves them into TMEM
+  static_assert(6 * HG * 128 <= VP_OFF - RA_OFF, "Q staging fits rings A and VO");
   fence_before();
-  __syncthreads();
+  cluster_sync();          // both CTAs' barriers exist before any remote operation
   fence_after();
   const uint32_t tmem = *tmem_slot;
-
+  if (tid == 0) {
+    arrive_expect_tx(bar(B_QLOAD), 9 * HG * 128);
+    for (int a = c; a < D / 64; a += 2) {
+      const uint32_t dst = a < 6 ? sbase + RA_OFF + a * (HG * 128) : sbase + QS_OFF + (a - 6) * (HG * 128);
+      asm volatile(
+          "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+          ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;\n" ::"r"(dst),
+          "l"(reinterpret_cast<uint64_t>(&tmap_q)), "r"(64 * a), "r"(h0), "r"(r), "r"(bar(B_QLOAD)),
+          "h"((uint16_t)3)
+          : "memory");
+    }
+  }
+  bool timed_out = false;
   if (warp < 4) {
     // staged Q dims 0..383 -> TMEM columns [256, 448): lane = head, column j
     // holds dims 2j, 2j+1
+    if (!warp_wait_cluster(bar(B_QLOAD), 0)) timed_out = true;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const unsigned char *stage = sm + RA_OFF + tid * (QT_CH * 16);
 #pragma unroll 1
     for (int part = 0; part < QT_DIMS / 64; ++part) {
+      const unsigned char *blk = sm + RA_OFF + part * (HG * 128) + tid * 128;
       uint32_t v[32];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const int ch = part * 8 + k;
-        const uint4 w = *reinterpret_cast<const uint4 *>(stage + ((ch ^ (tid & 7)) << 4));
+        const uint4 w = *reinterpret_cast<const uint4 *>(blk + ((k ^ (tid & 7)) << 4));
         v[4 * k] = w.x; v[4 * k + 1] = w.y; v[4 * k + 2] = w.z; v[4 * k + 3] = w.w;
       }
       TMEM_ST32(lane_base + COL_Q + part * 32, v);
     }
     tmem_wait_st();
   }
-  fence_proxy_async();
   fence_before();
-  cluster_sync();          // both CTAs' barriers exist before any remote operation,
-                           // and the Q staging area is free for KV tiles
+  __syncthreads();         // Q is in place; the staging area is free for KV tiles
   fence_after();
 
-  bool timed_out = false;
 
   if (warp >= 4 && warp < 8) {
     // ------------------------------------------------ gather producers ----
@@ -778,8 +772,29 @@ extern "C" int hs_sparse_attn_decode(const void *q, const void *kv, int64_t n_kv
   }
   const int64_t blocks = (int64_t)R * ((H + HG - 1) / HG) * 2;
   if (blocks > INT32_MAX) return hs_set_error(HS_ERR_UNSUPPORTED, "R*H too large");
+  // q as a [R][H][576] bf16 tensor for the prologue's tensor copies
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult qr;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess || !fn)
+      return hs_set_error(HS_ERR_CUDA, "cuTensorMapEncodeTiled not available");
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  alignas(64) CUtensorMap tmap;
+  const cuuint64_t gdim[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)R};
+  const cuuint64_t gstride[2] = {(cuuint64_t)ROWB, (cuuint64_t)H * ROWB};
+  const cuuint32_t box[3] = {64, HG, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult er = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), gdim,
+                             gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (er != CUDA_SUCCESS) return hs_set_error(HS_ERR_CUDA, "tensor map of q failed (%d)", (int)er);
   k_attn_pair<<<(unsigned)blocks, THREADS, SMEM_ALLOC, stream>>>(
-      reinterpret_cast<const char *>(q), reinterpret_cast<const char *>(kv), n_kv_rows, idx, H,
+      tmap, reinterpret_cast<const char *>(q), reinterpret_cast<const char *>(kv), n_kv_rows, idx, H,
       K, scale * 1.4426950408889634f, reinterpret_cast<__nv_bfloat16 *>(out), lse, status);
   HS_LAUNCH_CHECK("k_attn_pair");
   return HS_OK;
