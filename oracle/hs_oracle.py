@@ -183,6 +183,7 @@ class HotBuffer:
         self.token_slot = [dict() for _ in range(max_reqs)]
         self.hot = np.zeros((max_reqs * self.S_tot, LATENT_DIM), dtype=np.uint16)
         self.now = 0
+        self.last_plan = []
 
     # -- queries ---------------------------------------------------------
     def token_slot_array(self, b: int) -> np.ndarray:
@@ -254,6 +255,7 @@ class HotBuffer:
 
         failed = set()
         hits = misses = 0
+        self.last_plan = []       # (request, slot, position) of every copy made
         for b in sorted(needed):
             need = needed[b]
             if len(need) > self.S:
@@ -276,6 +278,7 @@ class HotBuffer:
                 # a4: copy the host row into the hot slot
                 self.hot[self.hot_row(b, s)] = self.host_pool[
                     host_row(self.hbt, b, t, self.block_size)]
+                self.last_plan.append((b, s, t))
             misses += len(missing)
 
         # a5: slot index table
@@ -442,3 +445,55 @@ def verify_finalize(buf: HotBuffer, logits, drafts, step_kv, kv_len):
         else:
             status |= STATUS_CAPACITY
     return acc, nxt, L.astype(np.int32), status
+
+
+# ---------------------------------------------------------------------------
+# next-1: one swap plan applied to follower caches
+# ---------------------------------------------------------------------------
+
+def apply_plan(plan, follower_hot, follower_pool, hbt, block_size: int, S_tot: int,
+               row_offset: int = 0) -> None:
+    """A follower cache repeats the leader's latest swap-in ("vllm 分析(十二)
+    HiSparse 下篇", ``HiSparseCacheHandle.resolve_topk``: a handle with a leader
+    calls ``runtime.apply_plan`` with ``plan_row_offset`` instead of
+    ``swap_in``; the leader's ``swap_in`` is asked to ``produce_plan``).
+
+    ``plan`` is ``HotBuffer.last_plan``: the (request b, slot s, position t)
+    of every row the leader copied. The follower has the same hot-buffer
+    geometry and the same paged host pool, so each copy is repeated from the
+    follower's pool into the follower's buffer (reading R14):
+    ``follower_hot[row_offset + b * S_tot + s] = follower_pool[host_row(b, t)]``.
+    The leader's slot table then indexes the follower's buffer unchanged.
+    ``follower_hot`` and ``follower_pool`` are uint16 row arrays (bf16 bits),
+    updated in place.
+    """
+    h = _np_i64(hbt)
+    for (b, s, t) in plan:
+        follower_hot[row_offset + b * S_tot + s] = follower_pool[host_row(h, b, t, block_size)]
+
+
+# ---------------------------------------------------------------------------
+# next-2: backup of device pages to the host caches
+# ---------------------------------------------------------------------------
+
+def backup_pages(src_layers, dst_layers, src_blocks, dst_blocks, page_offsets,
+                 blocks_per_kv_block: int, block_rows: int) -> None:
+    """Copy whole pages of several layers' device caches to their host caches
+    ("vllm 分析(十二) HiSparse 下篇", section 数据 back up:
+    ``HiSparseWorker._enqueue_transfers`` and ``hisparse_backup_layers``).
+
+    For transfer ``i`` and layer ``l`` (reading R15): rows
+    ``src_blocks[l][i] * block_rows + o`` of ``src_layers[l]`` go to rows
+    ``(dst_blocks[i] * blocks_per_kv_block + page_offsets[i]) * block_rows + o``
+    of ``dst_layers[l]``, for ``o = 0 .. block_rows - 1``: the source row uses
+    the layer's own resident block, the host page is shared by the layers.
+    Row arrays are numpy arrays of raw row contents, updated in place.
+    """
+    sb = _np_i64(src_blocks)
+    db = _np_i64(dst_blocks)
+    po = _np_i64(page_offsets)
+    for l in range(len(src_layers)):
+        for i in range(len(db)):
+            host_page = int(db[i]) * blocks_per_kv_block + int(po[i])
+            for o in range(block_rows):
+                dst_layers[l][host_page * block_rows + o] = src_layers[l][int(sb[l][i]) * block_rows + o]
