@@ -37,7 +37,7 @@ EXPORTS = (
     "hs_buffer_create", "hs_buffer_destroy", "hs_request_reset", "hs_get_status",
     "hs_buffer_dump", "hs_buffer_clock", "hs_last_error_string", "hs_resolve_topk",
     "hs_swap_in", "hs_sparse_attn_decode", "hs_verify_finalize", "hs_read_probe",
-    "hs_verify_accept_noalloc",
+    "hs_verify_accept_noalloc", "hs_swap_apply_plan", "hs_backup_pages",
 )
 
 
@@ -87,6 +87,8 @@ def lib() -> ctypes.CDLL:
             "hs_verify_finalize": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
             "hs_read_probe": (_I, [_P, ctypes.c_size_t, _P, _I, _P]),
             "hs_verify_accept_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
+            "hs_swap_apply_plan": (_I, [_P, _I, _P, _P, _I64, _P]),
+            "hs_backup_pages": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _I64, _P, _P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -295,3 +297,46 @@ def hs_read_probe(src: torch.Tensor, sink: torch.Tensor, blocks: int, stream=Non
     _check(lib().hs_read_probe(src.data_ptr(), nbytes,
                                _ptr(sink, "sink", torch.int64, (blocks,)), blocks,
                                _stream(stream)), "hs_read_probe")
+
+def _ptr_array(tensors, name, dtype, device):
+    """A ctypes array of the tensors' data pointers (checked like _ptr)."""
+    arr = (ctypes.c_void_p * len(tensors))()
+    for i, t in enumerate(tensors):
+        arr[i] = _ptr(t, f"{name}[{i}]", dtype, device=device)
+    return arr
+
+
+def hs_swap_apply_plan(buf: "HsBuffer", hot_kv_layers, host_pool_layers, row_offset: int = 0,
+                       stream=None) -> None:
+    """Repeat buf's latest swap-in copies for follower caches (one per layer)."""
+    if len(hot_kv_layers) != len(host_pool_layers):
+        raise ValueError("one host pool per follower cache")
+    hot = _ptr_array(hot_kv_layers, "hot_kv", torch.bfloat16, True)
+    pools = _ptr_array(host_pool_layers, "host_pools", torch.bfloat16, False)
+    _check(lib().hs_swap_apply_plan(buf.handle, len(hot_kv_layers), hot, pools, int(row_offset),
+                                    _stream(stream)), "hs_swap_apply_plan")
+
+
+def hs_backup_pages(src_caches, dst_caches, src_blocks, dst_blocks, page_offsets,
+                    block_rows: int, blocks_per_kv_block: int, status=None, stream=None) -> None:
+    """Copy pages of several layers' device caches ([rows][...] tensors) to
+    their host caches; row size from the tensors."""
+    if len(src_caches) != len(dst_caches):
+        raise ValueError("one host cache per layer")
+    n = len(src_caches)
+    if n == 0:
+        return
+    row_bytes = src_caches[0][0].numel() * src_caches[0].element_size()
+    for t in list(src_caches) + list(dst_caches):
+        if t[0].numel() * t.element_size() != row_bytes:
+            raise ValueError("all caches must have the same row size")
+    nt = dst_blocks.shape[0]
+    src = _ptr_array(src_caches, "src_caches", None, True)
+    dst = _ptr_array(dst_caches, "dst_caches", None, False)
+    _check(lib().hs_backup_pages(
+        n, src, dst, _ptr(src_blocks, "src_blocks", torch.int32, (n, nt)),
+        _ptr(dst_blocks, "dst_blocks", torch.int32, (nt,)),
+        _ptr(page_offsets, "page_offsets", torch.int32, (nt,)), nt, int(block_rows),
+        int(blocks_per_kv_block), int(row_bytes), src_caches[0].shape[0], dst_caches[0].shape[0],
+        _ptr(status, "status", torch.int32, (1,), allow_none=True), _stream(stream)),
+        "hs_backup_pages")

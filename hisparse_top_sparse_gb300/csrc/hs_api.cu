@@ -33,6 +33,21 @@ int hs_check_device_ptr(const void *p, const char *name, bool allow_null) {
   return HS_OK;
 }
 
+int hs_device_alias(const void *p, const void **out, const char *name) {
+  if (!p) return hs_set_error(HS_ERR_INVALID_ARG, "%s is NULL", name);
+  if ((uintptr_t)p & 15) return hs_set_error(HS_ERR_INVALID_ARG, "%s must be 16-byte aligned", name);
+  cudaPointerAttributes attr;
+  HS_CUDA_TRY(cudaPointerGetAttributes(&attr, p));
+  *out = nullptr;
+  if (attr.type == cudaMemoryTypeHost || attr.type == cudaMemoryTypeDevice ||
+      attr.type == cudaMemoryTypeManaged)
+    *out = attr.devicePointer;
+  if (!*out)
+    return hs_set_error(HS_ERR_INVALID_ARG,
+                        "%s is not page-locked mapped host memory or device memory", name);
+  return HS_OK;
+}
+
 int hs_check_buffer(const hs_buffer *buf) {
   if (!buf) return hs_set_error(HS_ERR_INVALID_ARG, "buffer is NULL");
   int dev = -1;

@@ -12,6 +12,7 @@
 #define HS_MAX_SLOTS 8192                  // S limit (the LRU sort runs in SMEM)
 #define HS_MAX_STEP 16
 #define HS_MAX_REQS 16384                  // requests per buffer (swap-in gather prefix in SMEM)
+#define HS_MAX_LAYERS 64                   // caches per hs_swap_apply_plan / hs_backup_pages call
 
 // Host-side state of a hot buffer. Device arrays are owned by the library.
 struct hs_buffer {
@@ -58,6 +59,9 @@ int hs_set_error(int code, const char *fmt, ...);
   } while (0)
 
 int hs_check_device_ptr(const void *p, const char *name, bool allow_null);
+// The device-accessible alias of p (device memory, or page-locked host memory
+// mapped into the device's address space); 16-byte alignment required.
+int hs_device_alias(const void *p, const void **out, const char *name);
 
 // ---- block helpers shared by the swap-in and commit kernels -----------------
 

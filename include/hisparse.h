@@ -245,6 +245,61 @@ int hs_sparse_attn_decode(const void *q, const void *kv, int64_t n_kv_rows,
                           hs_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* next-1: one swap plan for follower caches ([VLLM] resolve_topk:           */
+/*         runtime.apply_plan, produce_plan, plan_row_offset)                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Repeats the copies of buf's latest hs_swap_in (the "plan": every missed
+ * position's host row and the slot it went to) for n_layers follower caches,
+ * e.g. the other layers of the same requests: for each copy (request b, slot
+ * s, host row h) and layer l,
+ *   hot_kv[l][row_offset + b * (S + step_slots) + s] = host_pools[l][h].
+ * The slot table returned by that hs_swap_in indexes every follower cache
+ * the same way (plus row_offset). Followers have the leader's geometry: at
+ * least row_offset + max_reqs * (S + step_slots) rows of 576 bf16 in hot_kv[l],
+ * and host pools paged like the leader's (at least host_pool_rows rows).
+ *   hot_kv      host array of n_layers device pointers, 16-byte aligned
+ *   host_pools  host array of n_layers pointers to page-locked mapped host
+ *               memory (or device memory), 16-byte aligned
+ *   row_offset  rows added to every destination (>= 0)
+ * Call it after the hs_swap_in whose plan it repeats and before the next one
+ * (same stream, or ordered). Requirements: 0 <= n_layers <= 64.
+ */
+int hs_swap_apply_plan(hs_buffer *buf, int32_t n_layers, void *const *hot_kv,
+                       const void *const *host_pools, int64_t row_offset, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* next-2: page backup of several layers to host ([VLLM] 数据 back up:        */
+/*         HiSparseWorker._enqueue_transfers, hisparse_backup_layers)         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For transfer i and layer l, rows src_blocks[l][i] * block_rows + o of
+ * src_caches[l] go to rows
+ *   (dst_blocks[i] * blocks_per_kv_block + page_offsets[i]) * block_rows + o
+ * of dst_caches[l], o = 0 .. block_rows - 1 (each layer's own resident block,
+ * one host page shared by the layers). Rows of row_bytes bytes.
+ *   src_caches    host array of n_layers device pointers (resident caches)
+ *   dst_caches    host array of n_layers pointers to page-locked mapped host
+ *                 memory (or device memory)
+ *   src_blocks    device int32 [n_layers][n_transfers]
+ *   dst_blocks, page_offsets  device int32 [n_transfers]
+ *   src_rows, dst_rows        rows in each source / destination cache: a
+ *                 transfer reaching outside them (or a negative block) is
+ *                 skipped and sets HS_STATUS_INDEX in status (device uint32
+ *                 or NULL)
+ * Requirements: 0 <= n_layers <= 64, n_transfers >= 0, block_rows >= 1,
+ * blocks_per_kv_block >= 1, row_bytes a multiple of 16, pointers 16-byte
+ * aligned.
+ */
+int hs_backup_pages(int32_t n_layers, const void *const *src_caches, void *const *dst_caches,
+                    const int32_t *src_blocks, const int32_t *dst_blocks,
+                    const int32_t *page_offsets, int32_t n_transfers, int32_t block_rows,
+                    int32_t blocks_per_kv_block, int32_t row_bytes, int64_t src_rows,
+                    int64_t dst_rows, uint32_t *status, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* a7-a8: greedy verify and commit of the accepted prefix ([KVF] ④-⑥)       */
 /* ------------------------------------------------------------------------ */
 
