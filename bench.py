@@ -346,8 +346,13 @@ def run_swap_bench(hs, dev, args):
     stats = torch.zeros(2, dtype=torch.int64, device=dev)
     q = W.step_q(cfg, 0, device=dev)
     o = torch.empty((cfg.R, cfg.H, 512), dtype=torch.bfloat16, device=dev)
-    a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-    swap_ms, attn_ms, miss = [], [], []
+    # two follower layers (next row 1): their own hot buffers and host pools,
+    # filled by repeating each step's plan
+    n_follow = 2
+    f_hot = [torch.empty_like(hb["hot"]) for _ in range(n_follow)]
+    f_pool = [W.host_pool_tensor(hb["pool"].shape[0], 900 + i, device=dev) for i in range(n_follow)]
+    a, b, c, d = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+    swap_ms, attn_ms, apply_ms, miss = [], [], [], []
     for s in range(cfg.steps):
         stats.zero_()
         a.record()
@@ -355,13 +360,17 @@ def run_swap_bench(hs, dev, args):
         b.record()
         hs.hs_sparse_attn_decode(q, hb["hot"], out, cfg.scale, o)
         c.record()
-        c.synchronize()
+        hs.hs_swap_apply_plan(buf, f_hot, f_pool)
+        d.record()
+        d.synchronize()
         swap_ms.append(a.elapsed_time(b))
         attn_ms.append(b.elapsed_time(c))
+        apply_ms.append(c.elapsed_time(d))
         miss.append(int(stats[1].item()))
     st = hs.hs_get_status(buf)
     buf.close()
-    del hb
+    del hb, f_hot, f_pool
+    backup = run_backup_bench(hs, dev)
     link = measure_link(hs, dev)
     steady = range(1, cfg.steps)
     bytes_ss = sum(miss[s] for s in steady) * ROW_BYTES
@@ -373,7 +382,52 @@ def run_swap_bench(hs, dev, args):
             "cold_step_gbs": round(miss[0] * ROW_BYTES / (swap_ms[0] * 1e-3) / 1e9, 2),
             "attn_ms_per_step_mean": round(statistics.mean(attn_ms[1:]), 4),
             "query_rows_per_s_attention": round(cfg.R / (statistics.mean(attn_ms[1:]) * 1e-3), 1),
+            "follower_apply": {
+                "layers": n_follow,
+                "gbs": round(n_follow * bytes_ss / (sum(apply_ms[s] for s in steady) * 1e-3) / 1e9, 2),
+                "frac_of_link": round(n_follow * bytes_ss / (sum(apply_ms[s] for s in steady) * 1e-3)
+                                      / 1e9 / link["peak_gbs"], 4),
+                "ms_per_step": [round(x, 4) for x in apply_ms]},
+            "backup": backup,
             "status": st, "gpu_launches_per_step": 2}
+
+
+def run_backup_bench(hs, dev, layers=4, pages=512, block_rows=64):
+    """Next row 2: pages of several layers' device caches to their host caches
+    (pinned, mapped), device -> host GB/s against a 1 GiB device -> host copy."""
+    rows = pages * block_rows
+    g = np.random.default_rng(9)
+    src = [W.bf16_normal((rows, 576), W.KV_SCALE, 10 + l, "backup", 0, device=dev) for l in range(layers)]
+    dst = [torch.empty((rows * 2, 576), dtype=torch.bfloat16).pin_memory() for _ in range(layers)]
+    src_blocks = torch.as_tensor(np.stack([g.permutation(pages) for _ in range(layers)]).astype(np.int32),
+                                 device=dev)
+    dst_blocks = torch.as_tensor(g.permutation(pages).astype(np.int32), device=dev)
+    offs = torch.as_tensor(g.integers(0, 2, size=pages).astype(np.int32), device=dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ms = []
+    for _ in range(6):
+        a.record()
+        hs.hs_backup_pages(src, dst, src_blocks, dst_blocks, offs, block_rows, 2)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    byt = layers * rows * ROW_BYTES
+    best = min(ms[1:])
+    n = 1 << 30
+    host = torch.empty(n, dtype=torch.uint8).pin_memory()
+    dsrc = torch.empty(n, dtype=torch.uint8, device=dev)
+    best_copy = 0.0
+    for _ in range(3):
+        a.record()
+        host.copy_(dsrc, non_blocking=True)
+        b.record()
+        b.synchronize()
+        best_copy = max(best_copy, n / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del host, dsrc, src, dst
+    gbs = byt / (best * 1e-3) / 1e9
+    return {"layers": layers, "pages": pages, "block_rows": block_rows, "bytes": byt,
+            "ms": round(best, 4), "gbs": round(gbs, 2), "d2h_link_gbs": round(best_copy, 1),
+            "frac_of_link": round(gbs / best_copy, 4)}
 
 
 def cpu_baseline(cfg, rc, budget_s: float = 12.0):
