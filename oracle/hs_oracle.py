@@ -384,6 +384,82 @@ def sparse_attn_decode_rows(q, kv_rows_of, idx, scale: float, rows):
 
 
 # --------------------------------------------------------------------------
+# next-3: reclaim of resident pages and a batch mixing both kinds of request
+#     ("vllm 分析(十二) HiSparse 下篇": reclaim_resident_blocks with
+#      reclaimable_pages / release_resident_page, and the fully_resident flag
+#      that HiSparseCacheHandle.resolve_topk branches on)
+# --------------------------------------------------------------------------
+
+def reclaimable_pages(block_table, n_blocks) -> list:
+    """``(request, logical block)`` of every page a reclaim may release: the
+    pages each request still holds (entry >= 0) except its last two logical
+    blocks, listed request by request, blocks ascending (reading R16)."""
+    bt = _np_i64(block_table)
+    nb = _np_i64(n_blocks)
+    out = []
+    for b in range(bt.shape[0]):
+        n = min(max(int(nb[b]), 0), bt.shape[1])
+        for i in range(n - 2):
+            if bt[b, i] >= 0:
+                out.append((b, i))
+    return out
+
+
+def reclaim_resident(block_table, n_blocks, need: int):
+    """Release the first ``need`` reclaimable pages: each one's entry becomes
+    -1 (release_resident_page) and its block id is handed back. A request that
+    lost a page is no longer fully resident.
+
+    Returns ``(table int32 [B][stride], freed int32 [need] (-1 past the last
+    release), fully_resident int32 [B], n_freed)``."""
+    bt = _np_i64(block_table).copy()
+    nb = _np_i64(n_blocks)
+    freed = np.full(need, -1, dtype=np.int32)
+    take = reclaimable_pages(bt, nb)[:need]
+    for k, (b, i) in enumerate(take):
+        freed[k] = bt[b, i]
+        bt[b, i] = -1
+    fully = np.zeros(bt.shape[0], dtype=np.int32)
+    for b in range(bt.shape[0]):
+        n = min(max(int(nb[b]), 0), bt.shape[1])
+        fully[b] = int(all(bt[b, i] >= 0 for i in range(n)))
+    return bt.astype(np.int32), freed, fully, len(take)
+
+
+def sparse_attn_decode_mixed(q, kv_resident, kv_hot, row_req, fully_resident, idx,
+                             scale: float):
+    """``sparse_attn_decode`` for a batch mixing both kinds of request: row
+    ``r`` reads ``kv_resident`` while its request is fully resident
+    (``fully_resident[row_req[r]] != 0``) and ``kv_hot`` otherwise, each
+    row's entries valid within its own cache (reading R17). A request id
+    outside the flags leaves the row with no valid entry. ``row_req`` None
+    indexes the flags by row; ``fully_resident`` None sends every row to
+    ``kv_resident``."""
+    qb = _rows_u16(q) if not isinstance(q, np.ndarray) else q
+    as_f64 = lambda kv: kv if (isinstance(kv, np.ndarray) and kv.dtype == np.float64) \
+        else bf16_bits_to_f64(kv)
+    kv_resident = as_f64(kv_resident)
+    kv_hot = as_f64(kv_hot) if fully_resident is not None else None
+    ix = _np_i64(idx)
+    R = ix.shape[0]
+    H = qb.shape[1]
+    out = np.zeros((R, H, VALUE_DIM), dtype=np.float64)
+    lse = np.full((R, H), -np.inf, dtype=np.float64)
+    for r in range(R):
+        if fully_resident is None:
+            kv = kv_resident
+        else:
+            fr = _np_i64(fully_resident)
+            b = int(_np_i64(row_req)[r]) if row_req is not None else r
+            if not 0 <= b < fr.shape[0]:
+                continue
+            kv = kv_resident if fr[b] != 0 else kv_hot
+        o, l = sparse_attn_decode(qb[r:r + 1], kv, ix[r:r + 1], scale)
+        out[r], lse[r] = o[0], l[0]
+    return out, lse
+
+
+# --------------------------------------------------------------------------
 # a7-a8: greedy verify and commit of the accepted prefix
 #     ("投机解码的 KV 流转", sections ④-⑥ and the closing table)
 # --------------------------------------------------------------------------
