@@ -37,7 +37,8 @@ EXPORTS = (
     "hs_buffer_create", "hs_buffer_destroy", "hs_request_reset", "hs_get_status",
     "hs_buffer_dump", "hs_buffer_clock", "hs_last_error_string", "hs_resolve_topk",
     "hs_swap_in", "hs_sparse_attn_decode", "hs_verify_finalize", "hs_read_probe",
-    "hs_verify_accept_noalloc", "hs_swap_apply_plan", "hs_backup_pages",
+    "hs_verify_accept_noalloc", "hs_swap_apply_plan", "hs_backup_pages", "hs_reclaim_resident",
+    "hs_sparse_attn_decode_mixed",
 )
 
 
@@ -84,6 +85,9 @@ def lib() -> ctypes.CDLL:
             "hs_swap_in": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P]),
             "hs_sparse_attn_decode": (_I, [_P, _P, _I64, _P, _I, _I, _I, ctypes.c_float,
                                            _P, _P, _P, _P]),
+            "hs_sparse_attn_decode_mixed": (_I, [_P, _P, _I64, _P, _I64, _P, _P, _I, _P, _I, _I,
+                                                 _I, ctypes.c_float, _P, _P, _P, _P]),
+            "hs_reclaim_resident": (_I, [_P, _I, _I, _P, _I, _P, _P, _P, _P]),
             "hs_verify_finalize": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
             "hs_read_probe": (_I, [_P, ctypes.c_size_t, _P, _I, _P]),
             "hs_verify_accept_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
@@ -247,6 +251,42 @@ def hs_sparse_attn_decode(q, kv, idx, scale: float, out, lse=None, status=None,
         _ptr(lse, "lse", torch.float32, (R, H), allow_none=True),
         _ptr(status, "status", torch.int32, (1,), allow_none=True),
         _stream(stream)), "hs_sparse_attn_decode")
+
+
+def hs_sparse_attn_decode_mixed(q, kv_resident, kv_hot, row_req, fully_resident, idx,
+                                scale: float, out, lse=None, status=None, stream=None) -> None:
+    """Row r reads kv_resident while fully_resident[row_req[r]] != 0, else
+    kv_hot (row_req None: the flags are indexed by row)."""
+    R, H, D = q.shape
+    if D != LATENT_DIM:
+        raise ValueError("q must be [R][H][576]")
+    K = idx.shape[1]
+    n_reqs = fully_resident.numel() if fully_resident is not None else 0
+    _check(lib().hs_sparse_attn_decode_mixed(
+        _ptr(q, "q", torch.bfloat16),
+        _ptr(kv_resident, "kv_resident", torch.bfloat16), kv_resident.shape[0],
+        _ptr(kv_hot, "kv_hot", torch.bfloat16), kv_hot.shape[0],
+        _ptr(row_req, "row_req", torch.int32, (R,), allow_none=True),
+        _ptr(fully_resident, "fully_resident", torch.int32, allow_none=True), n_reqs,
+        _ptr(idx, "idx", torch.int32, (R, K)), R, H, K, float(scale),
+        _ptr(out, "out", torch.bfloat16, (R, H, VALUE_DIM)),
+        _ptr(lse, "lse", torch.float32, (R, H), allow_none=True),
+        _ptr(status, "status", torch.int32, (1,), allow_none=True),
+        _stream(stream)), "hs_sparse_attn_decode_mixed")
+
+
+def hs_reclaim_resident(block_table, n_blocks, need: int, freed=None, fully_resident=None,
+                        n_freed=None, stream=None) -> None:
+    """Releases up to `need` resident pages (all but each request's last two,
+    scan order) in the device block table."""
+    B, stride = block_table.shape
+    _check(lib().hs_reclaim_resident(
+        _ptr(block_table, "block_table", torch.int32), B, stride,
+        _ptr(n_blocks, "n_blocks", torch.int32, (B,)), int(need),
+        _ptr(freed, "freed", torch.int32, (int(need),), allow_none=True),
+        _ptr(fully_resident, "fully_resident", torch.int32, (B,), allow_none=True),
+        _ptr(n_freed, "n_freed", torch.int32, (1,), allow_none=True),
+        _stream(stream)), "hs_reclaim_resident")
 
 
 def hs_verify_finalize(buf: HsBuffer, logits, draft_tokens, step_kv, kv_len, accept_len,

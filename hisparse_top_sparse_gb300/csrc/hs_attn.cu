@@ -326,9 +326,11 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity)
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     k_attn_pair(const __grid_constant__ CUtensorMap tmap_q, const char *__restrict__ q,
-                const char *__restrict__ kv, int64_t n_kv, const int32_t *__restrict__ idx,
-                int32_t H, int32_t K, float scale_log2, __nv_bfloat16 *__restrict__ out,
-                float *__restrict__ lse, uint32_t *status) {
+                const char *__restrict__ kv_res, int64_t n_res, const char *__restrict__ kv_hot,
+                int64_t n_hot, const int32_t *__restrict__ row_req,
+                const int32_t *__restrict__ fully_resident, int32_t n_reqs,
+                const int32_t *__restrict__ idx, int32_t H, int32_t K, float scale_log2,
+                __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, uint32_t *status) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -348,6 +350,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int T = (K + NK - 1) / NK;
   const int n_own = T > c ? (T - c + 1) / 2 : 0;
   const int32_t *idx_row = idx + (int64_t)r * K;
+  // the row's cache: the paged resident cache while its request is fully
+  // resident, else the hot buffer its swap-in indices address
+  // (a request id outside [0, n_reqs) leaves the row without a valid entry)
+  const int32_t req = fully_resident ? (row_req ? __ldg(row_req + r) : r) : 0;
+  const bool req_ok = !fully_resident || (req >= 0 && req < n_reqs);
+  const bool hot = req_ok && fully_resident && __ldg(fully_resident + req) == 0;
+  const char *kv = hot ? kv_hot : kv_res;
+  const int64_t n_kv = !req_ok ? 0 : hot ? n_hot : n_res;
+  if (!req_ok && status && tid == 0 && c == 0) atomicOr(status, HS_STATUS_INDEX);
 
   if (tid == 0) {
     for (int s = 0; s < RA_SLOTS; ++s) {
@@ -749,17 +760,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 }  // namespace
 
-extern "C" int hs_sparse_attn_decode(const void *q, const void *kv, int64_t n_kv_rows,
-                                     const int32_t *idx, int32_t R, int32_t H, int32_t K,
-                                     float scale, void *out, float *lse, uint32_t *status,
-                                     hs_stream_t stream) {
-  if (R < 0 || H < 1 || H > 1024 || K < 0 || n_kv_rows < 0)
-    return hs_set_error(HS_ERR_INVALID_ARG, "bad sizes R=%d H=%d (1..1024) K=%d n_kv_rows=%lld",
-                        R, H, K, (long long)n_kv_rows);
+extern "C" int hs_sparse_attn_decode_mixed(const void *q, const void *kv_resident,
+                                           int64_t n_resident, const void *kv_hot, int64_t n_hot,
+                                           const int32_t *row_req, const int32_t *fully_resident,
+                                           int32_t n_reqs, const int32_t *idx, int32_t R,
+                                           int32_t H, int32_t K,
+                                           float scale, void *out, float *lse, uint32_t *status,
+                                           hs_stream_t stream) {
+  if (R < 0 || H < 1 || H > 1024 || K < 0 || n_resident < 0 || n_hot < 0 ||
+      (fully_resident && n_reqs < 0))
+    return hs_set_error(HS_ERR_INVALID_ARG, "bad sizes R=%d H=%d (1..1024) K=%d n_kv=%lld/%lld",
+                        R, H, K, (long long)n_resident, (long long)n_hot);
   if (R == 0) return HS_OK;
-  if (!q || !out || (K > 0 && (!idx || (!kv && n_kv_rows > 0))))
+  if (!q || !out ||
+      (K > 0 && (!idx || (!kv_resident && n_resident > 0) || (!kv_hot && n_hot > 0))))
     return hs_set_error(HS_ERR_INVALID_ARG, "NULL q/kv/idx/out");
-  if (((uintptr_t)q & 15) || ((uintptr_t)kv & 15) || ((uintptr_t)out & 15))
+  if (((uintptr_t)q & 15) || ((uintptr_t)kv_resident & 15) || ((uintptr_t)kv_hot & 15) ||
+      ((uintptr_t)out & 15))
     return hs_set_error(HS_ERR_INVALID_ARG, "q, kv and out must be 16-byte aligned");
   if (!(scale == scale)) return hs_set_error(HS_ERR_INVALID_ARG, "scale is NaN");
   int dev = 0;
@@ -794,8 +811,18 @@ extern "C" int hs_sparse_attn_decode(const void *q, const void *kv, int64_t n_kv
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (er != CUDA_SUCCESS) return hs_set_error(HS_ERR_CUDA, "tensor map of q failed (%d)", (int)er);
   k_attn_pair<<<(unsigned)blocks, THREADS, SMEM_ALLOC, stream>>>(
-      tmap, reinterpret_cast<const char *>(q), reinterpret_cast<const char *>(kv), n_kv_rows, idx, H,
-      K, scale * 1.4426950408889634f, reinterpret_cast<__nv_bfloat16 *>(out), lse, status);
+      tmap, reinterpret_cast<const char *>(q), reinterpret_cast<const char *>(kv_resident),
+      n_resident, reinterpret_cast<const char *>(kv_hot), n_hot, row_req, fully_resident, n_reqs, idx,
+      H, K,
+      scale * 1.4426950408889634f, reinterpret_cast<__nv_bfloat16 *>(out), lse, status);
   HS_LAUNCH_CHECK("k_attn_pair");
   return HS_OK;
+}
+
+extern "C" int hs_sparse_attn_decode(const void *q, const void *kv, int64_t n_kv_rows,
+                                     const int32_t *idx, int32_t R, int32_t H, int32_t K,
+                                     float scale, void *out, float *lse, uint32_t *status,
+                                     hs_stream_t stream) {
+  return hs_sparse_attn_decode_mixed(q, kv, n_kv_rows, nullptr, 0, nullptr, nullptr, 0, idx, R,
+                                     H, K, scale, out, lse, status, stream);
 }

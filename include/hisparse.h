@@ -245,6 +245,61 @@ int hs_sparse_attn_decode(const void *q, const void *kv, int64_t n_kv_rows,
                           hs_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* next-3: a batch mixing fully-resident and host-backed requests            */
+/*         ("hiSparse-MTP" page: reclaim_resident_blocks, the fully_resident */
+/*          flag and HiSparseCacheHandle.resolve_topk)                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Releases resident pages when the paged cache runs short of blocks. Scanning
+ * requests 0..B-1 and, within each, logical blocks 0 .. n_blocks[b] - 3 (every
+ * page but the request's last two, which are still being written), it takes
+ * the first `need` entries that are still held (>= 0): each one's physical
+ * block id goes to freed[k] in that order and its entry becomes -1. Then
+ * fully_resident[b] = 1 if entries 0 .. n_blocks[b] - 1 are all >= 0, else 0.
+ * The pages leave the choice among reclaimable pages to a priority rule they
+ * do not give; this call takes them in scan order, oldest pages first.
+ *   block_table     device int32 [B][stride], updated in place
+ *   n_blocks        device int32 [B]: logical blocks each request holds
+ *                   (clamped to 0..stride)
+ *   need            pages wanted (>= 0)
+ *   freed           device int32 [need] or NULL: released block ids, -1 past
+ *                   the last release
+ *   fully_resident  device int32 [B] or NULL
+ *   n_freed         device int32 or NULL: pages released (min(need, held))
+ */
+int hs_reclaim_resident(int32_t *block_table, int32_t B, int32_t stride,
+                        const int32_t *n_blocks, int32_t need, int32_t *freed,
+                        int32_t *fully_resident, int32_t *n_freed, hs_stream_t stream);
+
+/*
+ * hs_sparse_attn_decode for a batch that mixes both kinds of request: row r
+ * reads kv_resident (its indices come from hs_resolve_topk) while its request
+ * is fully resident, i.e. fully_resident[row_req[r]] != 0, and kv_hot (its
+ * indices come from hs_swap_in) otherwise; each row's entries are valid within
+ * its own cache's row count. The pages route a whole batch one way (resident
+ * only when every request is); the per-row choice keeps the resident requests
+ * off the swap-in path. Output, lse and requirements as hs_sparse_attn_decode.
+ *   kv_resident, kv_hot  device bf16 [n_resident][576] / [n_hot][576],
+ *                  16-byte aligned; either may be NULL when its count is 0
+ *   row_req        device int32 [R]: request of each row, or NULL (the flags
+ *                  are then indexed by row)
+ *   fully_resident device int32 [n_reqs] (as hs_reclaim_resident writes it),
+ *                  or NULL: every row reads kv_resident
+ *   status         as hs_sparse_attn_decode; in addition HS_STATUS_INDEX when
+ *                  a row's request is outside [0, n_reqs) -- that row then has
+ *                  no valid entry
+ * hs_sparse_attn_decode(q, kv, n, ...) is this call with kv_resident = kv,
+ * n_resident = n and fully_resident = NULL.
+ */
+int hs_sparse_attn_decode_mixed(const void *q, const void *kv_resident, int64_t n_resident,
+                                const void *kv_hot, int64_t n_hot, const int32_t *row_req,
+                                const int32_t *fully_resident, int32_t n_reqs,
+                                const int32_t *idx, int32_t R, int32_t H, int32_t K,
+                                float scale, void *out, float *lse, uint32_t *status,
+                                hs_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* next-1: one swap plan for follower caches ([VLLM] resolve_topk:           */
 /*         runtime.apply_plan, produce_plan, plan_row_offset)                */
 /* ------------------------------------------------------------------------ */

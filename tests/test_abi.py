@@ -40,3 +40,16 @@ def test_argument_errors_return_without_a_gpu():
     assert L.hs_buffer_create(None, None) == hs.HS_ERR_INVALID_ARG
     assert L.hs_swap_in(None, None, None, None, None, 0, 0, None, None, None,
                         None) == hs.HS_ERR_INVALID_ARG
+    # mixed batch: negative cache sizes, a negative request count with flags
+    assert L.hs_sparse_attn_decode_mixed(None, None, -1, None, 0, None, None, 0, None, 1, 1, 1,
+                                         ctypes.c_float(1.0), None, None, None,
+                                         None) == hs.HS_ERR_INVALID_ARG
+    flags = ctypes.c_int32(1)
+    assert L.hs_sparse_attn_decode_mixed(None, None, 0, None, 0, None, ctypes.byref(flags), -1,
+                                         None, 1, 1, 1, ctypes.c_float(1.0), None, None, None,
+                                         None) == hs.HS_ERR_INVALID_ARG
+    assert L.hs_reclaim_resident(None, -1, 4, None, 1, None, None, None,
+                                 None) == hs.HS_ERR_INVALID_ARG
+    assert L.hs_reclaim_resident(None, 2, 4, None, 1, None, None, None,
+                                 None) == hs.HS_ERR_INVALID_ARG
+    assert b"NULL" in L.hs_last_error_string()
