@@ -540,8 +540,8 @@ def apply_plan(plan, follower_hot, follower_pool, hbt, block_size: int, S_tot: i
     follower's pool into the follower's buffer (reading R14):
     ``follower_hot[row_offset + b * S_tot + s] = follower_pool[host_row(b, t)]``.
     The leader's slot table then indexes the follower's buffer unchanged.
-    ``follower_hot`` and ``follower_pool`` are uint16 row arrays (bf16 bits),
-    updated in place.
+    ``follower_hot`` and ``follower_pool`` are row arrays of any row format
+    (bf16 bits, or the raw bytes of an FP8 / FP4 row), updated in place.
     """
     h = _np_i64(hbt)
     for (b, s, t) in plan:
@@ -573,3 +573,52 @@ def backup_pages(src_layers, dst_layers, src_blocks, dst_blocks, page_offsets,
             host_page = int(db[i]) * blocks_per_kv_block + int(po[i])
             for o in range(block_rows):
                 dst_layers[l][host_page * block_rows + o] = src_layers[l][int(sb[l][i]) * block_rows + o]
+
+
+# ---------------------------------------------------------------------------
+# next-4: row backup by slot mapping and the indexer cache's host slots
+#     ("vllm 分析(十二) HiSparse 下篇", section c4a kv cache 写入:
+#      runtime.backup_rows, compress_hisparse_slot_mapping,
+#      hisparse_backup_indexer with its token_stride)
+# ---------------------------------------------------------------------------
+
+def backup_rows(src_layers, dst_layers, src_slots, dst_slots) -> int:
+    """Copy the rows a step wrote to the host caches: for every entry ``i``
+    whose two slots are non-negative and every layer ``l``,
+    ``dst_layers[l][dst_slots[i]] = src_layers[l][src_slots[i]]``. A row is
+    one token's entry of ``token_stride`` bytes (reading R19), here one row of
+    a numpy array of raw bytes. A negative slot means "no entry"; a slot past
+    the end of its array is skipped and reported. Returns the status bits."""
+    ss = _np_i64(src_slots)
+    ds = _np_i64(dst_slots)
+    status = 0
+    for i in range(len(ss)):
+        s, d = int(ss[i]), int(ds[i])
+        if s < 0 or d < 0:
+            continue
+        if s >= len(src_layers[0]) or d >= len(dst_layers[0]):
+            status |= STATUS_INDEX
+            continue
+        for l in range(len(src_layers)):
+            dst_layers[l][d] = src_layers[l][s]
+    return status
+
+
+def compress_slot_mapping(host_slots, positions, storage_block_size: int,
+                          compress_ratio: int) -> np.ndarray:
+    """Host row of each token in the indexer's compressed host cache (reading
+    R18): a logical block of ``storage_block_size * compress_ratio`` token
+    slots is stored as one block of ``storage_block_size`` entries, one entry
+    per ``compress_ratio`` consecutive positions, so the token at ``position``
+    with logical host slot ``slot`` lands in entry
+    ``(position mod logical block size) // compress_ratio`` of storage block
+    ``slot // logical block size``. Negative inputs give -1."""
+    lbs = storage_block_size * compress_ratio
+    out = np.full(len(host_slots), -1, dtype=np.int64)
+    for i, (s, p) in enumerate(zip(_np_i64(host_slots), _np_i64(positions))):
+        if s < 0 or p < 0:
+            continue
+        block = int(s) // lbs
+        entry = (int(p) % lbs) // compress_ratio
+        out[i] = block * storage_block_size + entry
+    return out
