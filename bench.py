@@ -425,9 +425,56 @@ def run_backup_bench(hs, dev, layers=4, pages=512, block_rows=64):
         best_copy = max(best_copy, n / (a.elapsed_time(b) * 1e-3) / 1e9)
     del host, dsrc, src, dst
     gbs = byt / (best * 1e-3) / 1e9
+
+    def timed(fn):
+        ts = []
+        for _ in range(6):
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return min(ts[1:])
+
+    # next row 4: rows by slot mapping (a prefill's scattered 1152-byte rows),
+    # and the indexer cache's 132-byte entries (one per 4 tokens) to their
+    # compressed host slots
+    n_rows = rows // 2
+    r_src = [W.bf16_normal((rows, 576), W.KV_SCALE, 20 + l, "backup", 0, device=dev)
+             for l in range(layers)]
+    r_dst = [torch.empty((rows, 576), dtype=torch.bfloat16).pin_memory() for _ in range(layers)]
+    s_slots = torch.as_tensor(g.permutation(rows)[:n_rows].astype(np.int32), device=dev)
+    d_slots = torch.as_tensor(g.permutation(rows)[:n_rows].astype(np.int32), device=dev)
+    r_ms = timed(lambda: hs.hs_backup_rows(r_src, r_dst, s_slots, d_slots))
+    r_bytes = layers * n_rows * ROW_BYTES
+    del r_src, r_dst
+    ratio, sbs, width = 4, 64, 132
+    n_tok = rows * 4
+    lbs = sbs * ratio
+    i_src = [torch.randint(0, 256, (n_tok // ratio, width), dtype=torch.uint8, device=dev)
+             for _ in range(layers)]
+    i_dst = [torch.empty((n_tok // ratio, width), dtype=torch.uint8).pin_memory()
+             for _ in range(layers)]
+    pos = np.arange(n_tok) % (64 * lbs)                        # requests of 64 blocks
+    hblk = g.permutation(n_tok // lbs)
+    h_slots = (hblk[np.arange(n_tok) // lbs] * lbs + pos % lbs).astype(np.int32)
+    e_src = np.where(pos % ratio == ratio - 1, np.arange(n_tok) // ratio, -1).astype(np.int32)
+    t_src, t_host, t_pos = (torch.as_tensor(x.astype(np.int32), device=dev)
+                            for x in (e_src, h_slots, pos))
+    i_ms = timed(lambda: hs.hs_backup_indexer(i_src, i_dst, t_src, t_host, t_pos, sbs, ratio))
+    i_bytes = layers * (n_tok // ratio) * width
+    del i_src, i_dst
     return {"layers": layers, "pages": pages, "block_rows": block_rows, "bytes": byt,
             "ms": round(best, 4), "gbs": round(gbs, 2), "d2h_link_gbs": round(best_copy, 1),
-            "frac_of_link": round(gbs / best_copy, 4)}
+            "frac_of_link": round(gbs / best_copy, 4),
+            "rows": {"rows_per_layer": n_rows, "row_bytes": ROW_BYTES, "bytes": r_bytes,
+                     "ms": round(r_ms, 4), "gbs": round(r_bytes / (r_ms * 1e-3) / 1e9, 2),
+                     "frac_of_link": round(r_bytes / (r_ms * 1e-3) / 1e9 / best_copy, 4)},
+            "indexer": {"tokens_per_layer": n_tok, "entries_per_layer": n_tok // ratio,
+                        "entry_bytes": width, "compress_ratio": ratio,
+                        "storage_block_size": sbs, "bytes": i_bytes, "ms": round(i_ms, 4),
+                        "gbs": round(i_bytes / (i_ms * 1e-3) / 1e9, 2),
+                        "frac_of_link": round(i_bytes / (i_ms * 1e-3) / 1e9 / best_copy, 4)}}
 
 
 def cpu_baseline(cfg, rc, budget_s: float = 12.0):

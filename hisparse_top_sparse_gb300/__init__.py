@@ -38,7 +38,7 @@ EXPORTS = (
     "hs_buffer_dump", "hs_buffer_clock", "hs_last_error_string", "hs_resolve_topk",
     "hs_swap_in", "hs_sparse_attn_decode", "hs_verify_finalize", "hs_read_probe",
     "hs_verify_accept_noalloc", "hs_swap_apply_plan", "hs_backup_pages", "hs_reclaim_resident",
-    "hs_sparse_attn_decode_mixed",
+    "hs_sparse_attn_decode_mixed", "hs_backup_rows", "hs_backup_indexer",
 )
 
 
@@ -91,7 +91,10 @@ def lib() -> ctypes.CDLL:
             "hs_verify_finalize": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
             "hs_read_probe": (_I, [_P, ctypes.c_size_t, _P, _I, _P]),
             "hs_verify_accept_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
-            "hs_swap_apply_plan": (_I, [_P, _I, _P, _P, _I64, _P]),
+            "hs_swap_apply_plan": (_I, [_P, _I, _P, _P, _I64, _I, _P]),
+            "hs_backup_rows": (_I, [_I, _P, _P, _P, _P, _I, _I, _I64, _I64, _P, _P]),
+            "hs_backup_indexer": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _I64, _P,
+                                       _P]),
             "hs_backup_pages": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _I64, _P, _P]),
         }
         for name, (res, args) in sig.items():
@@ -348,13 +351,25 @@ def _ptr_array(tensors, name, dtype, device):
 
 def hs_swap_apply_plan(buf: "HsBuffer", hot_kv_layers, host_pool_layers, row_offset: int = 0,
                        stream=None) -> None:
-    """Repeat buf's latest swap-in copies for follower caches (one per layer)."""
+    """Repeat buf's latest swap-in copies for follower caches (one per layer;
+    [rows][...] tensors of any dtype, the row size taken from them)."""
     if len(hot_kv_layers) != len(host_pool_layers):
         raise ValueError("one host pool per follower cache")
-    hot = _ptr_array(hot_kv_layers, "hot_kv", torch.bfloat16, True)
-    pools = _ptr_array(host_pool_layers, "host_pools", torch.bfloat16, False)
-    _check(lib().hs_swap_apply_plan(buf.handle, len(hot_kv_layers), hot, pools, int(row_offset),
+    n = len(hot_kv_layers)
+    row_bytes = _row_bytes(list(hot_kv_layers) + list(host_pool_layers)) if n else 4
+    hot = _ptr_array(hot_kv_layers, "hot_kv", None, True)
+    pools = _ptr_array(host_pool_layers, "host_pools", None, False)
+    _check(lib().hs_swap_apply_plan(buf.handle, n, hot, pools, int(row_offset), row_bytes,
                                     _stream(stream)), "hs_swap_apply_plan")
+
+
+def _row_bytes(tensors) -> int:
+    """Bytes per row (dim 0) shared by all the tensors."""
+    rb = tensors[0][0].numel() * tensors[0].element_size()
+    for t in tensors:
+        if t.dim() < 2 or t[0].numel() * t.element_size() != rb:
+            raise ValueError("all caches must be [rows][...] with the same row size")
+    return rb
 
 
 def hs_backup_pages(src_caches, dst_caches, src_blocks, dst_blocks, page_offsets,
@@ -380,3 +395,46 @@ def hs_backup_pages(src_caches, dst_caches, src_blocks, dst_blocks, page_offsets
         int(blocks_per_kv_block), int(row_bytes), src_caches[0].shape[0], dst_caches[0].shape[0],
         _ptr(status, "status", torch.int32, (1,), allow_none=True), _stream(stream)),
         "hs_backup_pages")
+
+
+def hs_backup_rows(src_caches, dst_caches, src_slots, dst_slots, status=None,
+                   stream=None) -> None:
+    """Row dst_slots[i] of every host cache = row src_slots[i] of its device
+    cache ([rows][...] tensors, one row = one token's entry)."""
+    if len(src_caches) != len(dst_caches):
+        raise ValueError("one host cache per layer")
+    n_l = len(src_caches)
+    if n_l == 0:
+        return
+    tb = _row_bytes(list(src_caches) + list(dst_caches))
+    n = src_slots.shape[0]
+    _check(lib().hs_backup_rows(
+        n_l, _ptr_array(src_caches, "src_caches", None, True),
+        _ptr_array(dst_caches, "dst_caches", None, False),
+        _ptr(src_slots, "src_slots", torch.int32, (n,)),
+        _ptr(dst_slots, "dst_slots", torch.int32, (n,)), n, tb, src_caches[0].shape[0],
+        dst_caches[0].shape[0], _ptr(status, "status", torch.int32, (1,), allow_none=True),
+        _stream(stream)), "hs_backup_rows")
+
+
+def hs_backup_indexer(src_caches, dst_caches, src_slots, host_slots, positions,
+                      storage_block_size: int, compress_ratio: int, status=None,
+                      stream=None) -> None:
+    """hs_backup_rows into the indexer's compressed host cache: the host row
+    comes from the logical host slot and the position."""
+    if len(src_caches) != len(dst_caches):
+        raise ValueError("one host cache per layer")
+    n_l = len(src_caches)
+    if n_l == 0:
+        return
+    tb = _row_bytes(list(src_caches) + list(dst_caches))
+    n = src_slots.shape[0]
+    _check(lib().hs_backup_indexer(
+        n_l, _ptr_array(src_caches, "src_caches", None, True),
+        _ptr_array(dst_caches, "dst_caches", None, False),
+        _ptr(src_slots, "src_slots", torch.int32, (n,)),
+        _ptr(host_slots, "host_slots", torch.int32, (n,)),
+        _ptr(positions, "positions", torch.int32, (n,)), n, int(storage_block_size),
+        int(compress_ratio), tb, src_caches[0].shape[0], dst_caches[0].shape[0],
+        _ptr(status, "status", torch.int32, (1,), allow_none=True), _stream(stream)),
+        "hs_backup_indexer")

@@ -33,9 +33,10 @@ int hs_check_device_ptr(const void *p, const char *name, bool allow_null) {
   return HS_OK;
 }
 
-int hs_device_alias(const void *p, const void **out, const char *name) {
+int hs_device_alias(const void *p, const void **out, const char *name, int align) {
   if (!p) return hs_set_error(HS_ERR_INVALID_ARG, "%s is NULL", name);
-  if ((uintptr_t)p & 15) return hs_set_error(HS_ERR_INVALID_ARG, "%s must be 16-byte aligned", name);
+  if ((uintptr_t)p % (uintptr_t)align)
+    return hs_set_error(HS_ERR_INVALID_ARG, "%s must be %d-byte aligned", name, align);
   cudaPointerAttributes attr;
   HS_CUDA_TRY(cudaPointerGetAttributes(&attr, p));
   *out = nullptr;

@@ -10,6 +10,15 @@
 // device-mapped page-locked host caches, four loads in flight per thread; the
 // row arithmetic is done per chunk in the kernel.
 
+// next-4: the same data movement row by row ("vllm 分析(十二) HiSparse 下篇",
+// section c4a kv cache 写入): after the compressor writes a step's entries,
+// runtime.backup_rows copies each written row of the cache to its host slot,
+// and for the 128-dim indexer cache hisparse_backup_indexer copies token_stride
+// bytes per entry to a host cache whose slots are the source slots compressed
+// by compress_hisparse_slot_mapping. One kernel serves both: per (layer,
+// entry, unit) a 16- or 4-byte copy, the destination slot computed in the
+// kernel when a compression ratio is given.
+
 #include "hs_internal.cuh"
 
 namespace {
@@ -64,6 +73,128 @@ __global__ void __launch_bounds__(256) k_backup_pages(const __grid_constant__ Ba
   if (bad && status) atomicOr(status, HS_STATUS_INDEX);
 }
 
+struct RowLayers {
+  const char *src[HS_MAX_LAYERS];
+  char *dst[HS_MAX_LAYERS];
+};
+
+// Host row of entry i: dst_slots[i], or with ratio > 0 the compressed slot
+// (dst_slots[i] / (sbs * ratio)) * sbs + (positions[i] % (sbs * ratio)) / ratio.
+//
+// Each row is copied by `tpr` threads of a block (tpr = min(units per row,
+// 256), so a block holds rows_per_block = 256 / tpr rows side by side); a
+// thread resolves the slots of TB tokens once and then copies its units of
+// those TB rows for every layer, TB loads in flight. Tokens without an entry
+// cost one slot load.
+constexpr int BR_THREADS = 256;
+constexpr int BR_TB = 8;
+
+template <typename U>
+__global__ void __launch_bounds__(BR_THREADS) k_backup_rows(const __grid_constant__ RowLayers rl,
+                                                            int32_t n_layers,
+                                                            const int32_t *__restrict__ src_slots,
+                                                            const int32_t *__restrict__ dst_slots,
+                                                            const int32_t *__restrict__ positions,
+                                                            int32_t n, int32_t vec, int32_t tpr,
+                                                            int32_t sbs, int32_t ratio,
+                                                            int64_t src_rows, int64_t dst_rows,
+                                                            uint32_t *status) {
+  const int rows_per_block = BR_THREADS / tpr;
+  const int c0 = threadIdx.x % tpr, rloc = threadIdx.x / tpr;
+  if (rloc >= rows_per_block) return;              // the block's spare threads (no barriers)
+  const int64_t row_stride = (int64_t)gridDim.x * rows_per_block;
+  const int lbs = sbs * ratio;
+  bool bad = false;
+  for (int64_t base = (int64_t)blockIdx.x * rows_per_block + rloc; base < n;
+       base += row_stride * BR_TB) {
+    int64_t so[BR_TB], dof[BR_TB];                 // unit offsets of the rows, -1 = none
+#pragma unroll
+    for (int t = 0; t < BR_TB; ++t) {
+      const int64_t i = base + t * row_stride;
+      so[t] = -1;
+      dof[t] = 0;
+      if (i < n) {
+        const int sr = __ldg(src_slots + i);
+        int dr = __ldg(dst_slots + i);
+        if (ratio > 0) {
+          const int p = __ldg(positions + i);
+          dr = (dr < 0 || p < 0) ? -1 : (dr / lbs) * sbs + (p % lbs) / ratio;
+        }
+        if (sr >= 0 && dr >= 0) {
+          if (sr < src_rows && dr < dst_rows) {
+            so[t] = (int64_t)sr * vec;
+            dof[t] = (int64_t)dr * vec;
+          } else {
+            bad = true;
+          }
+        }
+      }
+    }
+    for (int l = 0; l < n_layers; ++l) {
+      const U *src = reinterpret_cast<const U *>(rl.src[l]);
+      U *dst = reinterpret_cast<U *>(rl.dst[l]);
+      for (int c = c0; c < vec; c += tpr) {
+        U v[BR_TB];
+#pragma unroll
+        for (int t = 0; t < BR_TB; ++t)
+          if (so[t] >= 0) v[t] = src[so[t] + c];
+#pragma unroll
+        for (int t = 0; t < BR_TB; ++t)
+          if (so[t] >= 0) dst[dof[t] + c] = v[t];
+      }
+    }
+  }
+  if (bad && status) atomicOr(status, HS_STATUS_INDEX);
+}
+
+int backup_rows_impl(int32_t n_layers, const void *const *src_caches, void *const *dst_caches,
+                     const int32_t *src_slots, const int32_t *dst_slots,
+                     const int32_t *positions, int32_t n, int32_t sbs, int32_t ratio,
+                     int32_t token_stride, int64_t src_rows, int64_t dst_rows, uint32_t *status,
+                     hs_stream_t stream) {
+  if (n_layers < 0 || n_layers > HS_MAX_LAYERS)
+    return hs_set_error(HS_ERR_INVALID_ARG, "n_layers %d not in 0..%d", n_layers, HS_MAX_LAYERS);
+  if (n < 0 || src_rows < 0 || dst_rows < 0)
+    return hs_set_error(HS_ERR_INVALID_ARG, "bad sizes n=%d src_rows=%lld dst_rows=%lld", n,
+                        (long long)src_rows, (long long)dst_rows);
+  if (token_stride < 4 || token_stride % 4 || token_stride > (1 << 20))
+    return hs_set_error(HS_ERR_INVALID_ARG,
+                        "token_stride %d must be a multiple of 4 in 4..2^20", token_stride);
+  if (n_layers == 0 || n == 0) return HS_OK;
+  if (!src_caches || !dst_caches || !src_slots || !dst_slots || (ratio > 0 && !positions))
+    return hs_set_error(HS_ERR_INVALID_ARG, "NULL argument");
+  RowLayers rl;
+  bool wide = token_stride % 16 == 0;
+  int rc;
+  for (int l = 0; l < n_layers; ++l) {
+    const void *sp = nullptr, *dp = nullptr;
+    if ((rc = hs_device_alias(src_caches[l], &sp, "src_caches[l]", 4))) return rc;
+    if ((rc = hs_device_alias(dst_caches[l], &dp, "dst_caches[l]", 4))) return rc;
+    if (((uintptr_t)sp & 15) || ((uintptr_t)dp & 15)) wide = false;
+    rl.src[l] = reinterpret_cast<const char *>(sp);
+    rl.dst[l] = reinterpret_cast<char *>(const_cast<void *>(dp));
+  }
+  const int vec = wide ? token_stride / 16 : token_stride / 4;
+  const int tpr = vec < BR_THREADS ? vec : BR_THREADS;
+  const int rows_per_block = BR_THREADS / tpr;
+  int dev = 0, nsm = 0;
+  HS_CUDA_TRY(cudaGetDevice(&dev));
+  HS_CUDA_TRY(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t want = ((int64_t)n + (int64_t)rows_per_block * BR_TB - 1) /
+                       ((int64_t)rows_per_block * BR_TB);
+  const int grid = (int)(want < (int64_t)nsm * 8 ? want : (int64_t)nsm * 8);
+  if (wide)
+    k_backup_rows<uint4><<<grid, BR_THREADS, 0, stream>>>(rl, n_layers, src_slots, dst_slots,
+                                                          positions, n, vec, tpr, sbs, ratio,
+                                                          src_rows, dst_rows, status);
+  else
+    k_backup_rows<uint32_t><<<grid, BR_THREADS, 0, stream>>>(rl, n_layers, src_slots, dst_slots,
+                                                             positions, n, vec, tpr, sbs, ratio,
+                                                             src_rows, dst_rows, status);
+  HS_LAUNCH_CHECK("k_backup_rows");
+  return HS_OK;
+}
+
 }  // namespace
 
 extern "C" int hs_backup_pages(int32_t n_layers, const void *const *src_caches,
@@ -102,4 +233,28 @@ extern "C" int hs_backup_pages(int32_t n_layers, const void *const *src_caches,
                                            row_bytes / 16, src_rows, dst_rows, status);
   HS_LAUNCH_CHECK("k_backup_pages");
   return HS_OK;
+}
+
+extern "C" int hs_backup_rows(int32_t n_layers, const void *const *src_caches,
+                              void *const *dst_caches, const int32_t *src_slots,
+                              const int32_t *dst_slots, int32_t n, int32_t token_stride,
+                              int64_t src_rows, int64_t dst_rows, uint32_t *status,
+                              hs_stream_t stream) {
+  return backup_rows_impl(n_layers, src_caches, dst_caches, src_slots, dst_slots, nullptr, n, 0,
+                          0, token_stride, src_rows, dst_rows, status, stream);
+}
+
+extern "C" int hs_backup_indexer(int32_t n_layers, const void *const *src_caches,
+                                 void *const *dst_caches, const int32_t *src_slots,
+                                 const int32_t *host_slots, const int32_t *positions, int32_t n,
+                                 int32_t storage_block_size, int32_t compress_ratio,
+                                 int32_t token_stride, int64_t src_rows, int64_t dst_rows,
+                                 uint32_t *status, hs_stream_t stream) {
+  if (storage_block_size < 1 || compress_ratio < 1 ||
+      (int64_t)storage_block_size * compress_ratio > INT32_MAX)
+    return hs_set_error(HS_ERR_INVALID_ARG, "bad storage_block_size %d / compress_ratio %d",
+                        storage_block_size, compress_ratio);
+  return backup_rows_impl(n_layers, src_caches, dst_caches, src_slots, host_slots, positions, n,
+                          storage_block_size, compress_ratio, token_stride, src_rows, dst_rows,
+                          status, stream);
 }

@@ -60,8 +60,8 @@ int hs_set_error(int code, const char *fmt, ...);
 
 int hs_check_device_ptr(const void *p, const char *name, bool allow_null);
 // The device-accessible alias of p (device memory, or page-locked host memory
-// mapped into the device's address space); 16-byte alignment required.
-int hs_device_alias(const void *p, const void **out, const char *name);
+// mapped into the device's address space); `align`-byte alignment required.
+int hs_device_alias(const void *p, const void **out, const char *name, int align = 16);
 
 // ---- block helpers shared by the swap-in and commit kernels -----------------
 

@@ -473,24 +473,28 @@ __global__ void __launch_bounds__(256) k_swap_gather(const int32_t *__restrict__
 
 // The follower caches of one hs_swap_apply_plan call.
 struct PlanLayers {
-  uint4 *hot[HS_MAX_LAYERS];
-  const uint4 *pool[HS_MAX_LAYERS];
+  char *hot[HS_MAX_LAYERS];
+  const char *pool[HS_MAX_LAYERS];
 };
 
 // The leader's latest copy list, repeated for n_layers follower caches: the
-// same chunk numbering as k_swap_gather, with the layer as the outer index.
+// same numbering as k_swap_gather (request, copy, unit of the row), with the
+// layer as the outer index. A row is `vec` units of type U (16 or 4 bytes), so
+// follower caches may hold rows of another format than the leader's.
+template <typename U>
 __global__ void __launch_bounds__(256) k_swap_apply(const int32_t *__restrict__ copy_cnt,
                                                     const uint64_t *__restrict__ copy_desc,
                                                     int32_t max_reqs, int32_t S, int32_t S_tot,
                                                     int64_t row_offset, int32_t n_layers,
+                                                    int32_t vec,
                                                     const __grid_constant__ PlanLayers pl) {
-  extern __shared__ int pre[];                     // [max_reqs + 1] chunk offsets
+  extern __shared__ int pre[];                     // [max_reqs + 1] unit offsets
   __shared__ int part[256];
   const int tid = threadIdx.x;
   const int seg = (max_reqs + 255) / 256;
   auto cnt_of = [&](int i) -> int { const int c = copy_cnt[i]; return c > 0 ? c : 0; };
   int sum = 0;
-  for (int i = tid * seg; i < (tid + 1) * seg && i < max_reqs; ++i) sum += cnt_of(i) * HS_ROW_VEC16;
+  for (int i = tid * seg; i < (tid + 1) * seg && i < max_reqs; ++i) sum += cnt_of(i) * vec;
   part[tid] = sum;
   __syncthreads();
   if (tid < 32) {
@@ -511,7 +515,7 @@ __global__ void __launch_bounds__(256) k_swap_apply(const int32_t *__restrict__ 
     int acc = part[tid];
     for (int i = tid * seg; i < (tid + 1) * seg && i < max_reqs; ++i) {
       pre[i] = acc;
-      acc += cnt_of(i) * HS_ROW_VEC16;
+      acc += cnt_of(i) * vec;
     }
     if (tid == 255) pre[max_reqs] = acc;
   }
@@ -520,8 +524,8 @@ __global__ void __launch_bounds__(256) k_swap_apply(const int32_t *__restrict__ 
   const int64_t total = per_layer * n_layers;
   const int64_t step = (int64_t)gridDim.x * blockDim.x;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + tid; e < total; e += 4 * step) {
-    uint4 v[4];
-    uint4 *dst[4];
+    U v[4];
+    U *dst[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int64_t k = e + u * step;
@@ -535,11 +539,12 @@ __global__ void __launch_bounds__(256) k_swap_apply(const int32_t *__restrict__ 
           if (pre[mid] <= kk) lo = mid; else hi = mid;
         }
         const int rel = kk - pre[lo];
-        const int i = rel / HS_ROW_VEC16, c = rel % HS_ROW_VEC16;
+        const int i = rel / vec, c = rel - i * vec;
         const uint64_t d = copy_desc[(int64_t)lo * S + i];
         if (d != ~0ull) {
-          v[u] = pl.pool[l][(int64_t)(d >> 16) * HS_ROW_VEC16 + c];
-          dst[u] = pl.hot[l] + (row_offset + (int64_t)lo * S_tot + (int64_t)(d & 0xFFFF)) * HS_ROW_VEC16 + c;
+          v[u] = reinterpret_cast<const U *>(pl.pool[l])[(int64_t)(d >> 16) * vec + c];
+          dst[u] = reinterpret_cast<U *>(pl.hot[l]) +
+                   (row_offset + (int64_t)lo * S_tot + (int64_t)(d & 0xFFFF)) * vec + c;
         }
       }
     }
@@ -616,33 +621,50 @@ extern "C" int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
 
 extern "C" int hs_swap_apply_plan(hs_buffer *buf, int32_t n_layers, void *const *hot_kv,
                                   const void *const *host_pools, int64_t row_offset,
-                                  hs_stream_t stream) {
+                                  int32_t row_bytes, hs_stream_t stream) {
   int rc = hs_check_buffer(buf);
   if (rc) return rc;
   if (n_layers < 0 || n_layers > HS_MAX_LAYERS)
     return hs_set_error(HS_ERR_INVALID_ARG, "n_layers %d not in 0..%d", n_layers, HS_MAX_LAYERS);
   if (row_offset < 0) return hs_set_error(HS_ERR_INVALID_ARG, "negative row_offset");
+  if (row_bytes < 4 || row_bytes % 4 || row_bytes > (1 << 20))
+    return hs_set_error(HS_ERR_INVALID_ARG, "row_bytes %d must be a multiple of 4 in 4..2^20",
+                        row_bytes);
   if (n_layers == 0) return HS_OK;
   if (!hot_kv || !host_pools) return hs_set_error(HS_ERR_INVALID_ARG, "NULL layer arrays");
   PlanLayers pl;
+  bool wide = row_bytes % 16 == 0;
   for (int l = 0; l < n_layers; ++l) {
     const void *h = nullptr, *p = nullptr;
-    if ((rc = hs_device_alias(hot_kv[l], &h, "hot_kv[l]"))) return rc;
-    if ((rc = hs_device_alias(host_pools[l], &p, "host_pools[l]"))) return rc;
-    pl.hot[l] = reinterpret_cast<uint4 *>(const_cast<void *>(h));
-    pl.pool[l] = reinterpret_cast<const uint4 *>(p);
+    if (!hot_kv[l] || !host_pools[l] || ((uintptr_t)hot_kv[l] & 3) || ((uintptr_t)host_pools[l] & 3))
+      return hs_set_error(HS_ERR_INVALID_ARG, "hot_kv[%d] / host_pools[%d] NULL or not 4-byte aligned", l, l);
+    if (((uintptr_t)hot_kv[l] & 15) || ((uintptr_t)host_pools[l] & 15)) wide = false;
+    if ((rc = hs_device_alias(hot_kv[l], &h, "hot_kv[l]", 4))) return rc;
+    if ((rc = hs_device_alias(host_pools[l], &p, "host_pools[l]", 4))) return rc;
+    pl.hot[l] = reinterpret_cast<char *>(const_cast<void *>(h));
+    pl.pool[l] = reinterpret_cast<const char *>(p);
   }
-  static bool attr_set[64] = {false};
-  if (buf->device >= 64 || !attr_set[buf->device]) {
-    HS_CUDA_TRY(cudaFuncSetAttribute(k_swap_apply, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const int vec = wide ? row_bytes / 16 : row_bytes / 4;
+  if ((int64_t)buf->max_reqs * buf->S * vec > INT32_MAX)
+    return hs_set_error(HS_ERR_UNSUPPORTED, "max_reqs * slots_per_req * row units exceeds int32");
+  static bool attr_set[2][64] = {{false}};
+  if (buf->device >= 64 || !attr_set[wide][buf->device]) {
+    HS_CUDA_TRY(cudaFuncSetAttribute(wide ? k_swap_apply<uint4> : k_swap_apply<uint32_t>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)((HS_MAX_REQS + 1) * sizeof(int))));
-    if (buf->device < 64) attr_set[buf->device] = true;
+    if (buf->device < 64) attr_set[wide][buf->device] = true;
   }
   int nsm = 0;
   HS_CUDA_TRY(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, buf->device));
   const size_t gsmem = (size_t)(buf->max_reqs + 1) * sizeof(int);
-  k_swap_apply<<<nsm * 8, 256, gsmem, stream>>>(buf->copy_cnt, buf->copy_desc, buf->max_reqs,
-                                                buf->S, buf->S_tot, row_offset, n_layers, pl);
+  if (wide)
+    k_swap_apply<uint4><<<nsm * 8, 256, gsmem, stream>>>(buf->copy_cnt, buf->copy_desc,
+                                                         buf->max_reqs, buf->S, buf->S_tot,
+                                                         row_offset, n_layers, vec, pl);
+  else
+    k_swap_apply<uint32_t><<<nsm * 8, 256, gsmem, stream>>>(buf->copy_cnt, buf->copy_desc,
+                                                            buf->max_reqs, buf->S, buf->S_tot,
+                                                            row_offset, n_layers, vec, pl);
   HS_LAUNCH_CHECK("k_swap_apply");
   return HS_OK;
 }

@@ -311,18 +311,25 @@ int hs_sparse_attn_decode_mixed(const void *q, const void *kv_resident, int64_t 
  * s, host row h) and layer l,
  *   hot_kv[l][row_offset + b * (S + step_slots) + s] = host_pools[l][h].
  * The slot table returned by that hs_swap_in indexes every follower cache
- * the same way (plus row_offset). Followers have the leader's geometry: at
- * least row_offset + max_reqs * (S + step_slots) rows of 576 bf16 in hot_kv[l],
- * and host pools paged like the leader's (at least host_pool_rows rows).
- *   hot_kv      host array of n_layers device pointers, 16-byte aligned
+ * the same way (plus row_offset). Followers have the leader's geometry (at
+ * least row_offset + max_reqs * (S + step_slots) rows in hot_kv[l], host pools
+ * paged like the leader's with at least host_pool_rows rows) but their own row
+ * size: row_bytes per row, e.g. 1152 for a bf16 latent row like the leader's,
+ * or the row of an FP8 / FP4 cache format (next-4: a second kind of cache on
+ * the same plan).
+ *   hot_kv      host array of n_layers device pointers
  *   host_pools  host array of n_layers pointers to page-locked mapped host
- *               memory (or device memory), 16-byte aligned
+ *               memory (or device memory)
  *   row_offset  rows added to every destination (>= 0)
+ *   row_bytes   a multiple of 4 (copies are 16 bytes wide when it is a
+ *               multiple of 16 and every pointer is 16-byte aligned, else 4)
  * Call it after the hs_swap_in whose plan it repeats and before the next one
- * (same stream, or ordered). Requirements: 0 <= n_layers <= 64.
+ * (same stream, or ordered). Requirements: 0 <= n_layers <= 64, pointers
+ * 4-byte aligned, max_reqs * S * (row units) < 2^31.
  */
 int hs_swap_apply_plan(hs_buffer *buf, int32_t n_layers, void *const *hot_kv,
-                       const void *const *host_pools, int64_t row_offset, hs_stream_t stream);
+                       const void *const *host_pools, int64_t row_offset, int32_t row_bytes,
+                       hs_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* next-2: page backup of several layers to host ([VLLM] 数据 back up:        */
@@ -353,6 +360,52 @@ int hs_backup_pages(int32_t n_layers, const void *const *src_caches, void *const
                     const int32_t *page_offsets, int32_t n_transfers, int32_t block_rows,
                     int32_t blocks_per_kv_block, int32_t row_bytes, int64_t src_rows,
                     int64_t dst_rows, uint32_t *status, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* next-4: row backup by slot mapping, and the indexer cache's backup        */
+/*         ([VLLM] c4a kv cache 写入: runtime.backup_rows,                    */
+/*          compress_hisparse_slot_mapping, hisparse_backup_indexer)          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For every entry i with src_slots[i] >= 0 and dst_slots[i] >= 0 and every
+ * layer l: row dst_slots[i] of dst_caches[l] = row src_slots[i] of
+ * src_caches[l], token_stride bytes per row (a token's entry is one
+ * contiguous run of token_stride bytes on both sides). A negative slot means
+ * "no entry" and is skipped; a slot at or past src_rows / dst_rows is skipped
+ * and sets HS_STATUS_INDEX in status (device uint32 or NULL). Destination
+ * slots are distinct within a call (else which copy lands is unspecified).
+ *   src_caches  host array of n_layers device pointers
+ *   dst_caches  host array of n_layers pointers to page-locked mapped host
+ *               memory (or device memory)
+ *   src_slots, dst_slots  device int32 [n]
+ * Requirements: 0 <= n_layers <= 64, n >= 0, token_stride a multiple of 4 in
+ * 4..2^20, pointers 4-byte aligned (16-byte copies when token_stride and
+ * every pointer allow).
+ */
+int hs_backup_rows(int32_t n_layers, const void *const *src_caches, void *const *dst_caches,
+                   const int32_t *src_slots, const int32_t *dst_slots, int32_t n,
+                   int32_t token_stride, int64_t src_rows, int64_t dst_rows, uint32_t *status,
+                   hs_stream_t stream);
+
+/*
+ * hs_backup_rows for the indexer cache, whose host cache stores one entry per
+ * compress_ratio tokens in blocks of storage_block_size entries: the host row
+ * of entry i is computed from its logical host slot and position,
+ *   lbs = storage_block_size * compress_ratio,
+ *   dst = (host_slots[i] / lbs) * storage_block_size
+ *         + (positions[i] % lbs) / compress_ratio,
+ * (-1, skipped, when host_slots[i] or positions[i] is negative), and
+ * src_slots[i] < 0 marks a token that wrote no entry.
+ *   host_slots, positions  device int32 [n]
+ * Requirements as hs_backup_rows, plus storage_block_size >= 1,
+ * compress_ratio >= 1.
+ */
+int hs_backup_indexer(int32_t n_layers, const void *const *src_caches, void *const *dst_caches,
+                      const int32_t *src_slots, const int32_t *host_slots,
+                      const int32_t *positions, int32_t n, int32_t storage_block_size,
+                      int32_t compress_ratio, int32_t token_stride, int64_t src_rows,
+                      int64_t dst_rows, uint32_t *status, hs_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* a7-a8: greedy verify and commit of the accepted prefix ([KVF] ④-⑥)       */

@@ -53,3 +53,9 @@ def test_argument_errors_return_without_a_gpu():
     assert L.hs_reclaim_resident(None, 2, 4, None, 1, None, None, None,
                                  None) == hs.HS_ERR_INVALID_ARG
     assert b"NULL" in L.hs_last_error_string()
+    # row backups: bad token strides are refused before any device work
+    assert L.hs_backup_rows(1, None, None, None, None, 4, 6, 10, 10, None,
+                            None) == hs.HS_ERR_INVALID_ARG
+    assert b"token_stride" in L.hs_last_error_string()
+    assert L.hs_backup_indexer(1, None, None, None, None, None, 4, 0, 4, 16, 10, 10, None,
+                               None) == hs.HS_ERR_INVALID_ARG
