@@ -147,6 +147,78 @@ __global__ void __launch_bounds__(BR_THREADS) k_backup_rows(const __grid_constan
   if (bad && status) atomicOr(status, HS_STATUS_INDEX);
 }
 
+// Rows whose size (or whose host cache) is not a multiple of 16 bytes: each
+// row is cut into the 16-byte-aligned chunks of the destination it overlaps;
+// a chunk wholly inside the row is written with one 16-byte store (its four
+// words loaded one by one from the source), the partial chunks at the row's
+// two ends word by word. Stores over the host link stay mostly 16 bytes wide.
+template <int TB>
+__global__ void __launch_bounds__(BR_THREADS) k_backup_rows_narrow(
+    const __grid_constant__ RowLayers rl, int32_t n_layers, const int32_t *__restrict__ src_slots,
+    const int32_t *__restrict__ dst_slots, const int32_t *__restrict__ positions, int32_t n,
+    int32_t words, int32_t tpr, int32_t sbs, int32_t ratio, int64_t src_rows, int64_t dst_rows,
+    uint32_t *status) {
+  const int chunks = (words + 3) / 4 + 1;          // aligned chunks a row can touch
+  const int rows_per_block = BR_THREADS / tpr;
+  const int c0 = threadIdx.x % tpr, rloc = threadIdx.x / tpr;
+  if (rloc >= rows_per_block) return;              // the block's spare threads (no barriers)
+  const int64_t row_stride = (int64_t)gridDim.x * rows_per_block;
+  const int lbs = sbs * ratio;
+  bool bad = false;
+  for (int64_t base = (int64_t)blockIdx.x * rows_per_block + rloc; base < n;
+       base += row_stride * TB) {
+    int64_t so[TB], dof[TB];                       // word offsets of the rows, -1 = none
+#pragma unroll
+    for (int t = 0; t < TB; ++t) {
+      const int64_t i = base + t * row_stride;
+      so[t] = -1;
+      dof[t] = 0;
+      if (i < n) {
+        const int sr = __ldg(src_slots + i);
+        int dr = __ldg(dst_slots + i);
+        if (ratio > 0) {
+          const int p = __ldg(positions + i);
+          dr = (dr < 0 || p < 0) ? -1 : (dr / lbs) * sbs + (p % lbs) / ratio;
+        }
+        if (sr >= 0 && dr >= 0) {
+          if (sr < src_rows && dr < dst_rows) {
+            so[t] = (int64_t)sr * words;
+            dof[t] = (int64_t)dr * words;
+          } else {
+            bad = true;
+          }
+        }
+      }
+    }
+    for (int l = 0; l < n_layers; ++l) {
+      const uint32_t *src = reinterpret_cast<const uint32_t *>(rl.src[l]);
+      // word index 0 of `dst` is the 16-byte aligned address at or below the
+      // cache's start; `mis` words lie between the two
+      const int mis = (int)((reinterpret_cast<uintptr_t>(rl.dst[l]) >> 2) & 3);
+      uint32_t *dst = reinterpret_cast<uint32_t *>(reinterpret_cast<uintptr_t>(rl.dst[l]) & ~(uintptr_t)15);
+      for (int k = c0; k < chunks; k += tpr) {
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+          if (so[t] < 0) continue;
+          const int64_t d = dof[t] + mis;          // the row's first word, from dst
+          const int64_t c4 = (d & ~(int64_t)3) + 4 * k;
+          const int64_t w0 = c4 - d;               // row word at the chunk's start
+          if (w0 >= words) continue;
+          if (w0 >= 0 && w0 + 4 <= words) {
+            const uint32_t *sp = src + so[t] + w0;
+            *reinterpret_cast<uint4 *>(dst + c4) = make_uint4(sp[0], sp[1], sp[2], sp[3]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (w0 + e >= 0 && w0 + e < words) dst[c4 + e] = src[so[t] + w0 + e];
+          }
+        }
+      }
+    }
+  }
+  if (bad && status) atomicOr(status, HS_STATUS_INDEX);
+}
+
 int backup_rows_impl(int32_t n_layers, const void *const *src_caches, void *const *dst_caches,
                      const int32_t *src_slots, const int32_t *dst_slots,
                      const int32_t *positions, int32_t n, int32_t sbs, int32_t ratio,
@@ -175,18 +247,27 @@ int backup_rows_impl(int32_t n_layers, const void *const *src_caches, void *cons
     rl.dst[l] = reinterpret_cast<char *>(const_cast<void *>(dp));
   }
   const int vec = wide ? token_stride / 16 : token_stride / 4;
-  const int tpr = vec < BR_THREADS ? vec : BR_THREADS;
+  // narrow rows of 256 bytes and more go by 16-byte-aligned destination chunks
+  // (1152-byte rows at a 4-byte offset: 151 against 129 GB/s over the link);
+  // shorter ones a word per thread (132-byte rows: 87 against 65 GB/s)
+  const bool chunked = !wide && vec >= 64;
+  const int units = chunked ? vec / 4 + 2 : vec;
+  const int tpr = units < BR_THREADS ? units : BR_THREADS;
   const int rows_per_block = BR_THREADS / tpr;
   int dev = 0, nsm = 0;
   HS_CUDA_TRY(cudaGetDevice(&dev));
   HS_CUDA_TRY(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
-  const int64_t want = ((int64_t)n + (int64_t)rows_per_block * BR_TB - 1) /
-                       ((int64_t)rows_per_block * BR_TB);
+  const int tb = BR_TB;
+  const int64_t want = ((int64_t)n + (int64_t)rows_per_block * tb - 1) / ((int64_t)rows_per_block * tb);
   const int grid = (int)(want < (int64_t)nsm * 8 ? want : (int64_t)nsm * 8);
   if (wide)
     k_backup_rows<uint4><<<grid, BR_THREADS, 0, stream>>>(rl, n_layers, src_slots, dst_slots,
                                                           positions, n, vec, tpr, sbs, ratio,
                                                           src_rows, dst_rows, status);
+  else if (chunked)
+    k_backup_rows_narrow<BR_TB><<<grid, BR_THREADS, 0, stream>>>(rl, n_layers, src_slots, dst_slots,
+                                                                 positions, n, vec, tpr, sbs, ratio,
+                                                                 src_rows, dst_rows, status);
   else
     k_backup_rows<uint32_t><<<grid, BR_THREADS, 0, stream>>>(rl, n_layers, src_slots, dst_slots,
                                                              positions, n, vec, tpr, sbs, ratio,

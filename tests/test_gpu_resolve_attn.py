@@ -71,6 +71,23 @@ def test_attention_small(H, K, sharp):
     check_attn(out, ref, lse, ref_lse)
 
 
+@pytest.mark.parametrize("H,K", [(200, 96), (256, 130), (1024, 64)])
+def test_attention_several_head_groups(H, K):
+    """More than 128 heads: one CTA pair per group of 128 heads, the last
+    group ragged (rows past H are zero-filled by the Q copy and not written)."""
+    hs = lib()
+    R, N = 3, 2000
+    q, kv, idx = _attn_case(H + K, R, H, K, N)
+    scale = 1.0 / 24
+    ref, ref_lse = O.sparse_attn_decode(q, kv, idx, scale)
+    out = torch.full((R, H, 512), 7.0, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((R, H), dtype=torch.float32, device=DEV)
+    hs.hs_sparse_attn_decode(q.to(DEV), kv.to(DEV), torch.as_tensor(idx, device=DEV), scale,
+                             out, lse)
+    torch.cuda.synchronize()
+    check_attn(out, ref, lse, ref_lse)
+
+
 def test_attention_single_valid_key_is_exact():
     hs = lib()
     g = np.random.default_rng(3)
