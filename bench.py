@@ -283,14 +283,16 @@ def run_e2e(hs, cfg, rc, dev, args):
     d2h = h_out.numel() * h_out.element_size()
     n_ch = max(1, min(args.e2e_chunks, R))
     bounds = [(R * k // n_ch, R * (k + 1) // n_ch) for k in range(n_ch)]
-    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    s_cap, s_in, s_cmp, s_out = (torch.cuda.Stream() for _ in range(4))
+    ev_start = torch.cuda.Event()
     ev_in = [torch.cuda.Event() for _ in bounds]
     ev_cmp = [torch.cuda.Event() for _ in bounds]
-    ev_done = torch.cuda.Event()
-    ev_done.record(s_out)
+    ev_end = torch.cuda.Event()
 
-    def step():
-        s_in.wait_event(ev_done)
+    def step_ops():
+        # forks from and joins into the capturing stream s_cap
+        ev_start.record(s_cap)
+        s_in.wait_event(ev_start)
         for k, (r0, r1) in enumerate(bounds):
             with torch.cuda.stream(s_in):
                 d_q[r0:r1].copy_(h_q[r0:r1], non_blocking=True)
@@ -307,11 +309,23 @@ def run_e2e(hs, cfg, rc, dev, args):
             s_out.wait_event(ev_cmp[k])
             with torch.cuda.stream(s_out):
                 h_out[r0:r1].copy_(out[r0:r1], non_blocking=True)
-        ev_done.record(s_out)
+        ev_end.record(s_out)
+        s_cap.wait_event(ev_end)
 
-    for _ in range(max(3, args.warmup)):
-        step()
+    # one step = one replay of the captured copies and launches (the host
+    # issues a single graph launch per step); replays on s_cap run in order,
+    # so a step starts only after the previous step's output is in host memory
+    with torch.cuda.stream(s_cap):
+        step_ops()                       # eager once (kernel attributes, tensor maps)
     torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s_cap):
+        step_ops()
+
+    def step():
+        with torch.cuda.stream(s_cap):
+            graph.replay()
+
     # the chunked step gives the whole-batch result bit for bit
     idx_all = torch.empty_like(rc["topk"])
     out_all = torch.empty_like(out)
@@ -323,15 +337,15 @@ def run_e2e(hs, cfg, rc, dev, args):
         raise RuntimeError("end-to-end output differs from the whole-batch step")
     del idx_all, out_all
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(s_in)
+    a.record(s_cap)
     for _ in range(args.steps):
         step()
-    b.record(s_out)
+    b.record(s_cap)
     b.synchronize()
     ms = a.elapsed_time(b) / args.steps
     return {"value": round(R / (ms * 1e-3), 1), "unit": "query-rows/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "chunks_per_step": n_ch}
+            "chunks_per_step": n_ch, "cuda_graph": True}
 
 
 def measure_link(hs, dev):
