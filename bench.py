@@ -432,6 +432,8 @@ def run_swap_bench(hs, dev, args):
     buf.close()
     del hb, f_hot, f_pool
     backup = run_backup_bench(hs, dev)
+    verify = run_verify_bench(hs, dev, _peaks()[0]["hbm_gbs"])
+    overlap = run_overlap_bench(hs, dev)
     link = measure_link(hs, dev)
     steady = range(1, cfg.steps)
     bytes_ss = sum(miss[s] for s in steady) * ROW_BYTES
@@ -452,8 +454,135 @@ def run_swap_bench(hs, dev, args):
                 "frac_of_link": round(n_follow * bytes_ss / (sum(apply_ms[s] for s in steady) * 1e-3)
                                       / 1e9 / link["peak_gbs"], 4),
                 "ms_per_step": [round(x, 4) for x in apply_ms]},
-            "backup": backup,
+            "backup": backup, "verify": verify, "overlap_workload4": overlap,
             "status": st, "gpu_launches_per_step": 2}
+
+
+def run_verify_bench(hs, dev, peak_hbm):
+    """Workload 5: the greedy acceptance reads 256 x 4 x 129280 bf16 logits
+    (264.8 MB, more than L2); its GB/s against the measured HBM peak, then
+    one full hs_verify_finalize (acceptance + commit of the accepted prefix)
+    on a warm hot buffer."""
+    cfg = W.get_config(5)
+    logits, drafts, _ = W.planted_logits(cfg, device=dev)
+    t_drafts = torch.as_tensor(drafts, device=dev)
+    acc = torch.empty(cfg.B, dtype=torch.int32, device=dev)
+    nxt = torch.empty_like(acc)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        hs.hs_verify_accept_noalloc(logits, t_drafts, acc, nxt)
+    ms = []
+    for _ in range(10):
+        a.record()
+        hs.hs_verify_accept_noalloc(logits, t_drafts, acc, nxt)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    best = statistics.median(ms)
+    byt = logits.numel() * logits.element_size()
+    # one acceptance + commit on a buffer warmed by a swap-in of a 2048-set
+    req, ri = W.rows_of(cfg)
+    hb = W.host_backed_case(cfg, device=dev)
+    buf = hs.HsBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hb["hot"],
+                      hb["pool"], hb["hbt"])
+    sets = [W.locality_sets(cfg, cfg.L[r], r, 1) for r in range(cfg.B)]
+    topk = torch.as_tensor(W.topk_shared_sets(cfg, sets, 0), device=dev)
+    clen = torch.as_tensor(W.causal_lengths(cfg.L, req, ri), device=dev)
+    out_idx = torch.empty((cfg.R, cfg.K), dtype=torch.int32, device=dev)
+    hs.hs_swap_in(buf, torch.as_tensor(req, device=dev), clen, hb["kv_len"], topk, out_idx)
+    skv = W.step_kv(cfg, 0, device=dev)
+    a.record()
+    hs.hs_verify_finalize(buf, logits, t_drafts, skv, hb["kv_len"], acc, nxt)
+    b.record()
+    b.synchronize()
+    fin_ms = a.elapsed_time(b)
+    committed = int(acc.sum().item()) + cfg.B
+    st = hs.hs_get_status(buf)
+    buf.close()
+    del hb, logits
+    return {"workload": cfg.name, "accept_ms": round(best, 4),
+            "logits_gbs": round(byt / (best * 1e-3) / 1e9, 1),
+            "frac_of_hbm": round(byt / (best * 1e-3) / 1e9 / peak_hbm, 4),
+            "finalize_ms": round(fin_ms, 4), "rows_committed": committed, "status": st}
+
+
+def run_overlap_bench(hs, dev, steps=8):
+    """Workload 4 (128 requests, contexts 16K-128K, 90 % reuse): decode steps
+    of swap-in + attention, serial (one swap-in, then the attention) against
+    overlapped (requests in two halves: the second half's swap-in runs while
+    the first half's rows are attended on another stream). Both run on their
+    own empty hot buffer and must give the same output bit for bit."""
+    cfg = W.get_config(4)
+    req, ri = W.rows_of(cfg)
+    clen = W.causal_lengths(cfg.L, req, ri)
+    hb = W.host_backed_case(cfg, device=dev)
+    hot2 = torch.zeros_like(hb["hot"])
+    sets = [W.locality_sets(cfg, cfg.L[r], r, steps) for r in range(cfg.B)]
+    topks = [torch.as_tensor(W.topk_shared_sets(cfg, sets, st), device=dev) for st in range(steps)]
+    t_req, t_clen = torch.as_tensor(req, device=dev), torch.as_tensor(clen, device=dev)
+    # the first part: whole requests filling whole attention waves (one wave =
+    # one row per two-SM cluster slot), so that splitting adds no wave
+    slots = torch.cuda.get_device_properties(dev).multi_processor_count // 2
+    rows_per_req = cfg.d + 1
+    waves = (cfg.R + slots - 1) // slots
+    half = max(1, (waves + 1) // 2) * slots
+    half -= half % rows_per_req
+    half = min(half, cfg.R - rows_per_req)
+    assert (req[:half] < req[half]).all() and (req[half:] >= req[half]).all()
+    q = W.step_q(cfg, 0, device=dev)
+    out_s = torch.empty((cfg.R, cfg.H, 512), dtype=torch.bfloat16, device=dev)
+    out_o = torch.empty_like(out_s)
+    idx_s = torch.empty((cfg.R, cfg.K), dtype=torch.int32, device=dev)
+    idx_o = torch.empty_like(idx_s)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    e_swap = [torch.cuda.Event() for _ in range(2)]
+    e_done = torch.cuda.Event()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def serial(buf, st):
+        hs.hs_swap_in(buf, t_req, t_clen, hb["kv_len"], topks[st], idx_s, stream=s1)
+        hs.hs_sparse_attn_decode(q, hb["hot"], idx_s, cfg.scale, out_s, stream=s1)
+
+    def overlapped(buf, st):
+        for k, (r0, r1) in enumerate(((0, half), (half, cfg.R))):
+            hs.hs_swap_in(buf, t_req[r0:r1], t_clen[r0:r1], hb["kv_len"], topks[st][r0:r1],
+                          idx_o[r0:r1], stream=s1)
+            e_swap[k].record(s1)
+            s2.wait_event(e_swap[k])
+            hs.hs_sparse_attn_decode(q[r0:r1], hot2, idx_o[r0:r1], cfg.scale, out_o[r0:r1],
+                                     stream=s2)
+        e_done.record(s2)
+        s1.wait_event(e_done)
+
+    res = {}
+    variants = [("serial", serial, hb["hot"], 0)] + \
+        [(f"overlapped_copy_sms_{n}" if n else "overlapped", overlapped, hot2, n) for n in (0, 24)]
+    for name, fn, hot, n_sms in variants:
+        buf = hs.HsBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hot,
+                          hb["pool"], hb["hbt"])
+        hs.hs_buffer_set_copy_sms(buf, n_sms)
+        ms = []
+        for st in range(steps):
+            a.record(s1)
+            fn(buf, st)
+            b.record(s1)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        res[name] = {"ms_per_step": [round(x, 4) for x in ms],
+                     "steady_ms": round(statistics.mean(ms[1:]), 4),
+                     "status": hs.hs_get_status(buf)}
+        buf.close()
+        torch.cuda.synchronize()
+        if fn is overlapped and not torch.equal(out_s.view(torch.int16), out_o.view(torch.int16)):
+            raise RuntimeError("overlapped decode step differs from the serial one")
+    del hb, hot2
+    ser = res["serial"]["steady_ms"]
+    best = min((k for k in res if k != "serial"), key=lambda k: res[k]["steady_ms"])
+    return {"workload": cfg.name, "rows": cfg.R, "first_part_rows": half, "variants": res,
+            "best_overlapped": best,
+            "query_rows_per_s_serial": round(cfg.R / (ser * 1e-3), 1),
+            "query_rows_per_s_best": round(cfg.R / (min(ser, res[best]["steady_ms"]) * 1e-3), 1),
+            "speedup": round(ser / res[best]["steady_ms"], 3)}
 
 
 def run_backup_bench(hs, dev, layers=4, pages=512, block_rows=64):

@@ -39,6 +39,7 @@ EXPORTS = (
     "hs_swap_in", "hs_sparse_attn_decode", "hs_verify_finalize", "hs_read_probe",
     "hs_verify_accept_noalloc", "hs_swap_apply_plan", "hs_backup_pages", "hs_reclaim_resident",
     "hs_sparse_attn_decode_mixed", "hs_backup_rows", "hs_backup_indexer",
+    "hs_buffer_set_copy_sms",
 )
 
 
@@ -80,6 +81,7 @@ def lib() -> ctypes.CDLL:
             "hs_get_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
             "hs_buffer_dump": (_I, [_P, _P, _P, _P, _P]),
             "hs_buffer_clock": (_I64, [_P]),
+            "hs_buffer_set_copy_sms": (_I, [_P, _I]),
             "hs_last_error_string": (ctypes.c_char_p, []),
             "hs_resolve_topk": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
             "hs_swap_in": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P]),
@@ -201,6 +203,10 @@ def hs_buffer_destroy(buf: HsBuffer) -> None:
 
 def hs_request_reset(buf: HsBuffer, req: int, stream=None) -> None:
     _check(lib().hs_request_reset(buf.handle, int(req), _stream(stream)), "hs_request_reset")
+
+
+def hs_buffer_set_copy_sms(buf: HsBuffer, n_sms: int) -> None:
+    _check(lib().hs_buffer_set_copy_sms(buf.handle, int(n_sms)), "hs_buffer_set_copy_sms")
 
 
 def hs_get_status(buf: HsBuffer, stream=None) -> int:

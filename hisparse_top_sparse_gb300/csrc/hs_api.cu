@@ -172,6 +172,14 @@ extern "C" int hs_buffer_destroy(hs_buffer *buf) {
 
 extern "C" int64_t hs_buffer_clock(const hs_buffer *buf) { return buf ? buf->clock : -1; }
 
+extern "C" int hs_buffer_set_copy_sms(hs_buffer *buf, int32_t n_sms) {
+  int rc = hs_check_buffer(buf);
+  if (rc) return rc;
+  if (n_sms < 0) return hs_set_error(HS_ERR_INVALID_ARG, "n_sms %d < 0", n_sms);
+  buf->copy_sms = n_sms;
+  return HS_OK;
+}
+
 __global__ void k_request_reset(int32_t *token_slot, int32_t *slot_token, int64_t *slot_ts,
                                 int32_t *order, int32_t S, int32_t max_ctx, int32_t req) {
   for (int s = threadIdx.x; s < S; s += blockDim.x) {

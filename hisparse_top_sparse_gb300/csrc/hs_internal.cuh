@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "hisparse.h"
@@ -37,6 +38,7 @@ struct hs_buffer {
   uint32_t *status;      // device status word
 
   int64_t clock;         // LRU clock: swap-in and commit calls made so far
+  int32_t copy_sms;      // SMs the copy kernels may spread over (0 = all)
 };
 
 // error reporting (hs_api.cu)
@@ -118,3 +120,76 @@ __device__ __forceinline__ void hs_lru_reorder(const int32_t *order, const uint3
   }
 }
 int hs_check_buffer(const hs_buffer *buf);
+
+// ---- argmax of one logits row (greedy verify) -------------------------------
+
+#define HS_ARGMAX_THREADS 256   // a block per row: 8 per SM, every row of a call in one wave
+
+// The index of the largest of logits[0 .. V-1] (fp32 or bf16 as dtype says),
+// the lowest index among equals, for the block's thread 0 (others: unspecified).
+// 16-byte streaming loads over the aligned body, four in flight per thread;
+// scalar loads for the unaligned head and the tail. Every thread of the block
+// (HS_ARGMAX_THREADS of them) calls it.
+template <int DTYPE>
+__device__ __forceinline__ int32_t hs_row_argmax(const char *base, int32_t V) {
+  struct Best {
+    float v;
+    int32_t i;
+  };
+  auto take = [](Best &b, float v, int32_t i) {
+    if (v > b.v || (v == b.v && i < b.i)) { b.v = v; b.i = i; }
+  };
+  constexpr int NT = HS_ARGMAX_THREADS;
+  const int64_t elem = (DTYPE == HS_LOGITS_F32) ? 4 : 2;
+  const int per16 = 16 / (int)elem;
+  auto load = [&](int32_t i) -> float {
+    if (DTYPE == HS_LOGITS_F32) return reinterpret_cast<const float *>(base)[i];
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[i]);
+  };
+  auto take16 = [&](Best &b, const uint4 w, int32_t i0) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (DTYPE == HS_LOGITS_F32) {
+        take(b, __uint_as_float(ws[q]), i0 + q);
+      } else {
+        take(b, __uint_as_float(ws[q] << 16), i0 + 2 * q);
+        take(b, __uint_as_float(ws[q] & 0xFFFF0000u), i0 + 2 * q + 1);
+      }
+    }
+  };
+  Best best{-INFINITY, INT32_MAX};
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(base);
+  int head = (int)(((16 - (addr & 15)) & 15) / elem);
+  if ((addr & (elem - 1)) != 0) head = V;     // misaligned elements: all scalar
+  if (head > V) head = V;
+  const int nvec = (V - head) / per16;
+  for (int i = threadIdx.x; i < head; i += NT) take(best, load(i), i);
+  const uint4 *body = reinterpret_cast<const uint4 *>(base + (int64_t)head * elem);
+  int k = threadIdx.x;
+  for (; k + 3 * NT < nvec; k += 4 * NT) {
+    uint4 w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) w[u] = __ldcs(body + k + u * NT);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) take16(best, w[u], head + (k + u * NT) * per16);
+  }
+  for (; k < nvec; k += NT) take16(best, __ldcs(body + k), head + k * per16);
+  for (int i = head + nvec * per16 + threadIdx.x; i < V; i += NT) take(best, load(i), i);
+  for (int off = 16; off; off >>= 1) {
+    const float v = __shfl_xor_sync(0xffffffffu, best.v, off);
+    const int32_t i = __shfl_xor_sync(0xffffffffu, best.i, off);
+    take(best, v, i);
+  }
+  __shared__ float wv[NT / 32];
+  __shared__ int32_t wi[NT / 32];
+  if ((threadIdx.x & 31) == 0) {
+    wv[threadIdx.x >> 5] = best.v;
+    wi[threadIdx.x >> 5] = best.i;
+  }
+  __syncthreads();
+  Best b{-INFINITY, INT32_MAX};
+  if (threadIdx.x == 0)
+    for (int w = 0; w < NT / 32; ++w) take(b, wv[w], wi[w]);
+  return b.i;
+}

@@ -46,69 +46,17 @@ int scratch_for_current_device(int32_t **out) {
   return HS_OK;
 }
 
-struct Best {
-  float v;
-  int32_t i;
-};
-
-__device__ __forceinline__ void take(Best &b, float v, int32_t i) {
-  if (v > b.v || (v == b.v && i < b.i)) { b.v = v; b.i = i; }
-}
-
-__device__ __forceinline__ Best warp_best(Best b) {
-  for (int off = 16; off; off >>= 1) {
-    const float v = __shfl_xor_sync(0xffffffffu, b.v, off);
-    const int32_t i = __shfl_xor_sync(0xffffffffu, b.i, off);
-    take(b, v, i);
-  }
-  return b;
-}
-
 // Block per logits row: argmax with ties to the lowest index, written to
 // pred[row] (every row of the call is written, so nothing needs clearing).
 template <int DTYPE>
-__global__ void __launch_bounds__(512) k_accept_argmax(const void *__restrict__ logits,
-                                                       int32_t V, int32_t *__restrict__ pred) {
+__global__ void __launch_bounds__(HS_ARGMAX_THREADS) k_accept_argmax(const void *__restrict__ logits,
+                                                                    int32_t V,
+                                                                    int32_t *__restrict__ pred) {
   const int64_t row = blockIdx.x;
   const int64_t elem = (DTYPE == HS_LOGITS_F32) ? 4 : 2;
-  const char *base = reinterpret_cast<const char *>(logits) + row * (int64_t)V * elem;
-  auto load = [&](int32_t i) -> float {
-    if (DTYPE == HS_LOGITS_F32) return reinterpret_cast<const float *>(base)[i];
-    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[i]);
-  };
-  Best best{-INFINITY, INT32_MAX};
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(base);
-  const int per16 = 16 / (int)elem;
-  int head = (int)(((16 - (addr & 15)) & 15) / elem);
-  if ((addr & (elem - 1)) != 0) head = V;
-  if (head > V) head = V;
-  const int nvec = (V - head) / per16;
-  for (int i = threadIdx.x; i < head; i += blockDim.x) take(best, load(i), i);
-  const uint4 *body = reinterpret_cast<const uint4 *>(base + (int64_t)head * elem);
-  for (int k = threadIdx.x; k < nvec; k += blockDim.x) {
-    const uint4 w = __ldcs(body + k);
-    const int32_t i0 = head + k * per16;
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (DTYPE == HS_LOGITS_F32) {
-        take(best, __uint_as_float(ws[q]), i0 + q);
-      } else {
-        take(best, __uint_as_float(ws[q] << 16), i0 + 2 * q);
-        take(best, __uint_as_float(ws[q] & 0xFFFF0000u), i0 + 2 * q + 1);
-      }
-    }
-  }
-  for (int i = head + nvec * per16 + threadIdx.x; i < V; i += blockDim.x) take(best, load(i), i);
-  best = warp_best(best);
-  __shared__ Best wb[16];
-  if ((threadIdx.x & 31) == 0) wb[threadIdx.x >> 5] = best;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    Best b = (threadIdx.x < (blockDim.x >> 5)) ? wb[threadIdx.x] : Best{-INFINITY, INT32_MAX};
-    b = warp_best(b);
-    if (threadIdx.x == 0) pred[row] = b.i;
-  }
+  const int32_t best = hs_row_argmax<DTYPE>(
+      reinterpret_cast<const char *>(logits) + row * (int64_t)V * elem, V);
+  if (threadIdx.x == 0) pred[row] = best;
 }
 
 // Thread per request: longest agreeing prefix and the next token.
@@ -146,9 +94,9 @@ extern "C" int hs_verify_accept_noalloc(const void *logits, int32_t logits_dtype
   if (rc) return rc;
   const int rows = B * (d + 1);
   if (logits_dtype == HS_LOGITS_F32)
-    k_accept_argmax<HS_LOGITS_F32><<<rows, 512, 0, stream>>>(logits, V, pred);
+    k_accept_argmax<HS_LOGITS_F32><<<rows, HS_ARGMAX_THREADS, 0, stream>>>(logits, V, pred);
   else
-    k_accept_argmax<HS_LOGITS_BF16><<<rows, 512, 0, stream>>>(logits, V, pred);
+    k_accept_argmax<HS_LOGITS_BF16><<<rows, HS_ARGMAX_THREADS, 0, stream>>>(logits, V, pred);
   HS_LAUNCH_CHECK("k_accept_argmax");
   k_accept_prefix<<<(B + 127) / 128, 128, 0, stream>>>(pred, draft_tokens, B, d, accept_len,
                                                        next_token);

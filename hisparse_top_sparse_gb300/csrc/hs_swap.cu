@@ -613,6 +613,7 @@ extern "C" int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
   ta.max_ctx = buf->max_ctx;
   ta.out = out_slot_idx; ta.out_valid = out_valid; ta.status = buf->status;
   const size_t gsmem = (size_t)(buf->max_reqs + 1) * sizeof(int);
+  if (buf->copy_sms > 0 && buf->copy_sms < nsm) nsm = buf->copy_sms;
   k_swap_gather<<<nsm * 8, 256, gsmem, stream>>>(buf->copy_cnt, buf->copy_desc, buf->max_reqs,
                                                  buf->S, buf->S_tot, a.pool, a.hot, ta);
   HS_LAUNCH_CHECK("k_swap_gather");
@@ -656,6 +657,7 @@ extern "C" int hs_swap_apply_plan(hs_buffer *buf, int32_t n_layers, void *const 
   }
   int nsm = 0;
   HS_CUDA_TRY(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, buf->device));
+  if (buf->copy_sms > 0 && buf->copy_sms < nsm) nsm = buf->copy_sms;
   const size_t gsmem = (size_t)(buf->max_reqs + 1) * sizeof(int);
   if (wide)
     k_swap_apply<uint4><<<nsm * 8, 256, gsmem, stream>>>(buf->copy_cnt, buf->copy_desc,

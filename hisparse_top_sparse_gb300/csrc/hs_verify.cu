@@ -22,75 +22,18 @@
 
 namespace {
 
-struct Best {
-  float v;
-  int32_t i;
-};
-
-__device__ __forceinline__ void take(Best &b, float v, int32_t i) {
-  if (v > b.v || (v == b.v && i < b.i)) { b.v = v; b.i = i; }
-}
-
-__device__ __forceinline__ Best warp_best(Best b) {
-  for (int off = 16; off; off >>= 1) {
-    const float v = __shfl_xor_sync(0xffffffffu, b.v, off);
-    const int32_t i = __shfl_xor_sync(0xffffffffu, b.i, off);
-    take(b, v, i);
-  }
-  return b;
-}
-
 template <int DTYPE>
-__global__ void __launch_bounds__(512) k_verify_argmax(const void *__restrict__ logits,
-                                                       int32_t V, int32_t rows_per_req,
-                                                       int32_t n_step, int32_t *__restrict__ pred) {
+__global__ void __launch_bounds__(HS_ARGMAX_THREADS) k_verify_argmax(const void *__restrict__ logits,
+                                                                    int32_t V, int32_t rows_per_req,
+                                                                    int32_t n_step,
+                                                                    int32_t *__restrict__ pred) {
   const int64_t row = blockIdx.x;
-  Best best{-INFINITY, INT32_MAX};
   const int64_t elem = (DTYPE == HS_LOGITS_F32) ? 4 : 2;
-  const char *base = reinterpret_cast<const char *>(logits) + row * (int64_t)V * elem;
-  const int per16 = 16 / (int)elem;
-  // 16-byte path over the aligned body, scalar head and tail
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(base);
-  int head = (int)(((16 - (addr & 15)) & 15) / elem);
-  if ((addr & (elem - 1)) != 0) head = V;  // misaligned element: all scalar
-  if (head > V) head = V;
-  const int nvec = (V - head) / per16;
-  auto load = [&](int32_t i) -> float {
-    if (DTYPE == HS_LOGITS_F32) return reinterpret_cast<const float *>(base)[i];
-    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[i]);
-  };
-  for (int i = threadIdx.x; i < head; i += blockDim.x) take(best, load(i), i);
-  const uint4 *body = reinterpret_cast<const uint4 *>(base + (int64_t)head * elem);
-  for (int k = threadIdx.x; k < nvec; k += blockDim.x) {
-    const uint4 w = __ldcs(body + k);
-    const int32_t i0 = head + k * per16;
-    if (DTYPE == HS_LOGITS_F32) {
-      take(best, __uint_as_float(w.x), i0);
-      take(best, __uint_as_float(w.y), i0 + 1);
-      take(best, __uint_as_float(w.z), i0 + 2);
-      take(best, __uint_as_float(w.w), i0 + 3);
-    } else {
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        take(best, __uint_as_float(ws[q] << 16), i0 + 2 * q);
-        take(best, __uint_as_float(ws[q] & 0xFFFF0000u), i0 + 2 * q + 1);
-      }
-    }
-  }
-  for (int i = head + nvec * per16 + threadIdx.x; i < V; i += blockDim.x) take(best, load(i), i);
-
-  best = warp_best(best);
-  __shared__ Best wb[16];
-  if ((threadIdx.x & 31) == 0) wb[threadIdx.x >> 5] = best;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    Best b = (threadIdx.x < (blockDim.x >> 5)) ? wb[threadIdx.x] : Best{-INFINITY, INT32_MAX};
-    b = warp_best(b);
-    if (threadIdx.x == 0) {
-      const int64_t req = row / rows_per_req, i = row % rows_per_req;
-      pred[req * n_step + i] = b.i;
-    }
+  const int32_t best = hs_row_argmax<DTYPE>(
+      reinterpret_cast<const char *>(logits) + row * (int64_t)V * elem, V);
+  if (threadIdx.x == 0) {
+    const int64_t req = row / rows_per_req, i = row % rows_per_req;
+    pred[req * n_step + i] = best;
   }
 }
 
@@ -200,10 +143,10 @@ extern "C" int hs_verify_finalize(hs_buffer *buf, const void *logits, int32_t lo
   buf->clock += 1;
   const int rows = B * (d + 1);
   if (logits_dtype == HS_LOGITS_F32)
-    k_verify_argmax<HS_LOGITS_F32><<<rows, 512, 0, stream>>>(logits, V, d + 1, buf->n_step,
+    k_verify_argmax<HS_LOGITS_F32><<<rows, HS_ARGMAX_THREADS, 0, stream>>>(logits, V, d + 1, buf->n_step,
                                                              buf->pred);
   else
-    k_verify_argmax<HS_LOGITS_BF16><<<rows, 512, 0, stream>>>(logits, V, d + 1, buf->n_step,
+    k_verify_argmax<HS_LOGITS_BF16><<<rows, HS_ARGMAX_THREADS, 0, stream>>>(logits, V, d + 1, buf->n_step,
                                                               buf->pred);
   HS_LAUNCH_CHECK("k_verify_argmax");
   k_verify_commit<<<B, 256, (size_t)buf->S * sizeof(int32_t), stream>>>(

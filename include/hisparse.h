@@ -149,6 +149,13 @@ int hs_buffer_dump(hs_buffer *buf, hs_stream_t stream, int32_t *token_slot,
 /* Number of swap-in and commit calls made so far (the LRU clock). */
 int64_t hs_buffer_clock(const hs_buffer *buf);
 
+/* Limits the copy kernels of hs_swap_in and hs_swap_apply_plan on this
+ * buffer to about n_sms SMs' worth of blocks (0, the default: every SM). The
+ * host link saturates well before every SM is busy, so a caller that overlaps
+ * a swap-in with attention on another stream can leave most SMs to the
+ * attention. Takes effect from the next call; n_sms >= 0. */
+int hs_buffer_set_copy_sms(hs_buffer *buf, int32_t n_sms);
+
 /* Text of the last error returned on this thread. */
 const char *hs_last_error_string(void);
 
