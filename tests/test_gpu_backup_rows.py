@@ -123,3 +123,43 @@ def test_apply_plan_other_row_formats():
         torch.cuda.synchronize()
         for i in range(len(fmts)):
             assert np.array_equal(f_hot[i].cpu().numpy(), e_hot[i]), fmts[i]
+
+
+def test_backup_rows_and_apply_plan_64_layers():
+    """The most layers one call takes (64), for both calls."""
+    hs = lib()
+    g = np.random.default_rng(64)
+    n_l, n_src, n = 64, 50, 30
+    src = [_rand_bytes(g, n_src, 144).to(DEV) for _ in range(n_l)]
+    dst = [torch.zeros((40, 144), dtype=torch.uint8, pin_memory=True) for _ in range(n_l)]
+    ss = g.integers(0, n_src, size=n).astype(np.int32)
+    ds = g.permutation(40)[:n].astype(np.int32)
+    hs.hs_backup_rows(src, dst, _t(ss), _t(ds))
+    e_dst = [np.zeros((40, 144), np.uint8) for _ in range(n_l)]
+    O.backup_rows([x.cpu().numpy() for x in src], e_dst, ss, ds)
+    torch.cuda.synchronize()
+    for l in range(n_l):
+        assert np.array_equal(dst[l].numpy(), e_dst[l])
+    # follower caches: 64 layers of 16-byte rows on one plan
+    B, S, n_step, bs, max_ctx = 2, 4, 1, 4, 16
+    nblk = max_ctx // bs
+    S_tot = S + n_step
+    hbt = g.permutation(B * nblk).reshape(B, nblk).astype(np.int32)
+    pool = W.host_pool_tensor(B * nblk * bs, 8, device=DEV)
+    hot = torch.zeros((B * S_tot, 576), dtype=torch.bfloat16, device=DEV)
+    buf = hs.HsBuffer(B, S, n_step, max_ctx, bs, hot, pool, _t(hbt))
+    ref = O.HotBuffer(B, S, n_step, max_ctx, bs, hbt, pool.clone())
+    f_pool = [_rand_bytes(g, B * nblk * bs, 16).pin_memory() for _ in range(n_l)]
+    f_hot = [torch.zeros((B * S_tot, 16), dtype=torch.uint8, device=DEV) for _ in range(n_l)]
+    req = np.array([0, 1], np.int32)
+    clen = np.array([12, 9], np.int32)
+    topk = np.array([[0, 5, 11], [1, 2, 8]], np.int32)
+    out = torch.empty((2, 3), dtype=torch.int32, device=DEV)
+    hs.hs_swap_in(buf, _t(req), _t(clen), _t(np.array([12, 9], np.int32)), _t(topk), out)
+    ref.swap_in(req, clen, [12, 9], topk)
+    hs.hs_swap_apply_plan(buf, f_hot, f_pool)
+    torch.cuda.synchronize()
+    for l in range(n_l):
+        e = np.zeros((B * S_tot, 16), np.uint8)
+        O.apply_plan(ref.last_plan, e, f_pool[l].numpy(), hbt, bs, S_tot)
+        assert np.array_equal(f_hot[l].cpu().numpy(), e)

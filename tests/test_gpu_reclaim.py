@@ -83,6 +83,25 @@ def test_mixed_attention_matches_oracle_and_single_cache():
         assert torch.equal(l1, lse[rows])
 
 
+def test_mixed_attention_flags_by_row():
+    """No row_req: the flags are indexed by row directly."""
+    hs = lib()
+    g = np.random.default_rng(13)
+    R, H, K, NA, NH = 4, 64, 100, 900, 300
+    q = _bf16(g.standard_normal((R, H, 576)) / 24).to(DEV)
+    kv_a = _bf16(g.standard_normal((NA, 576)) / 24).to(DEV)
+    kv_h = _bf16(g.standard_normal((NH, 576)) / 24).to(DEV)
+    idx = g.integers(0, NH, size=(R, K)).astype(np.int32)
+    flags = np.array([0, 1, 1, 0], np.int32)
+    out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((R, H), dtype=torch.float32, device=DEV)
+    hs.hs_sparse_attn_decode_mixed(q, kv_a, kv_h, None, _t(flags), _t(idx), 0.04, out, lse)
+    ref, ref_lse = O.sparse_attn_decode_mixed(q.cpu(), kv_a.cpu(), kv_h.cpu(), None, flags, idx,
+                                              0.04)
+    torch.cuda.synchronize()
+    check_attn(out, ref, lse, ref_lse)
+
+
 def test_mixed_attention_unknown_request_gives_empty_row():
     hs = lib()
     g = np.random.default_rng(12)

@@ -88,6 +88,25 @@ def test_attention_several_head_groups(H, K):
     check_attn(out, ref, lse, ref_lse)
 
 
+@pytest.mark.parametrize("K,sharp", [(4096, False), (8192, True)])
+def test_attention_long_rows(K, sharp):
+    """Rows of 128 and 256 tiles (the ring slots wrap many times; padding,
+    out-of-range and duplicate entries as in the small cases)."""
+    hs = lib()
+    R, H, N = 2, 128, 20000
+    q, kv, idx = _attn_case(K + 7, R, H, K, N, sharp)
+    scale = 1.0 / 24
+    ref, ref_lse = O.sparse_attn_decode(q, kv, idx, scale)
+    out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((R, H), dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hs.hs_sparse_attn_decode(q.to(DEV), kv.to(DEV), torch.as_tensor(idx, device=DEV), scale,
+                             out, lse, st)
+    torch.cuda.synchronize()
+    check_attn(out, ref, lse, ref_lse)
+    assert int(st.item()) == 0
+
+
 def test_attention_single_valid_key_is_exact():
     hs = lib()
     g = np.random.default_rng(3)
