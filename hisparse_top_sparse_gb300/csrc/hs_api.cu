@@ -65,7 +65,7 @@ int hs_check_buffer(const hs_buffer *buf) {
 static void free_buffer(hs_buffer *b) {
   if (!b) return;
   void *ptrs[] = {b->token_slot, b->slot_token, b->slot_ts, b->lru_order, b->pos_mark,
-                  b->copy_desc,  b->copy_cnt,   b->pred,    b->status};
+                  b->copy_desc,  b->copy_cnt,   b->pred,    b->row_count, b->status};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   free(b);
@@ -142,6 +142,7 @@ extern "C" int hs_buffer_create(const hs_buffer_desc *d, hs_buffer **out) {
       {(void **)&b->copy_desc, R * S * 8, 0},
       {(void **)&b->copy_cnt, R * 4, 0},
       {(void **)&b->pred, R * (size_t)d->step_slots * 4, 0},
+      {(void **)&b->row_count, R * 4, 0},
       {(void **)&b->status, 4, 0},
   };
   for (auto &e : plan) {

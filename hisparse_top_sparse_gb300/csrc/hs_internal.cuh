@@ -35,6 +35,7 @@ struct hs_buffer {
   uint64_t *copy_desc;   // [max_reqs][S]: (host pool row << 16) | hot slot, per miss
   int32_t *copy_cnt;     // [max_reqs]: misses to copy in the current call
   int32_t *pred;         // [max_reqs*n_step] argmax per verify row
+  int32_t *row_count;    // [max_reqs] verify rows done per request in a call (0 between calls)
   uint32_t *status;      // device status word
 
   int64_t clock;         // LRU clock: swap-in and commit calls made so far

@@ -19,6 +19,8 @@
 #define HS_NOALLOC_MAX_DEVICES 64
 
 static __device__ __align__(256) int32_t g_accept_scratch[HS_NOALLOC_MAX_ROWS];
+// per request: argmax rows done in the current call (back to 0 at its end)
+static __device__ __align__(256) int32_t g_accept_count[HS_NOALLOC_MAX_ROWS];
 
 namespace {
 
@@ -26,9 +28,10 @@ namespace {
 // code the array's name is only a host-side stand-in; kernels must receive the
 // address that cudaGetSymbolAddress returns for the current device.
 int32_t *g_scratch_dev[HS_NOALLOC_MAX_DEVICES] = {nullptr};
+int32_t *g_count_dev[HS_NOALLOC_MAX_DEVICES] = {nullptr};
 std::mutex g_scratch_mu;
 
-int scratch_for_current_device(int32_t **out) {
+int scratch_for_current_device(int32_t **out, int32_t **count) {
   int dev = -1;
   HS_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= HS_NOALLOC_MAX_DEVICES)
@@ -40,37 +43,45 @@ int scratch_for_current_device(int32_t **out) {
     if (e != cudaSuccess || !p)
       return hs_set_error(HS_ERR_CUDA, "cudaGetSymbolAddress(g_accept_scratch) failed: %s",
                           cudaGetErrorString(e));
+    void *pc = nullptr;
+    e = cudaGetSymbolAddress(&pc, g_accept_count);
+    if (e != cudaSuccess || !pc)
+      return hs_set_error(HS_ERR_CUDA, "cudaGetSymbolAddress(g_accept_count) failed: %s",
+                          cudaGetErrorString(e));
     g_scratch_dev[dev] = static_cast<int32_t *>(p);
+    g_count_dev[dev] = static_cast<int32_t *>(pc);
   }
   *out = g_scratch_dev[dev];
+  *count = g_count_dev[dev];
   return HS_OK;
 }
 
-// Block per logits row: argmax with ties to the lowest index, written to
-// pred[row] (every row of the call is written, so nothing needs clearing).
+// Block per logits row: argmax with ties to the lowest index into pred[row];
+// the request's last row to finish (a count per request) then takes the
+// longest agreeing prefix and the next token, and puts the count back to 0.
 template <int DTYPE>
-__global__ void __launch_bounds__(HS_ARGMAX_THREADS) k_accept_argmax(const void *__restrict__ logits,
-                                                                    int32_t V,
-                                                                    int32_t *__restrict__ pred) {
+__global__ void __launch_bounds__(HS_ARGMAX_THREADS) k_accept(const void *__restrict__ logits,
+                                                             int32_t V, int32_t d,
+                                                             const int32_t *__restrict__ drafts,
+                                                             int32_t *pred, int32_t *count,
+                                                             int32_t *__restrict__ accept_len,
+                                                             int32_t *__restrict__ next_token) {
   const int64_t row = blockIdx.x;
   const int64_t elem = (DTYPE == HS_LOGITS_F32) ? 4 : 2;
   const int32_t best = hs_row_argmax<DTYPE>(
       reinterpret_cast<const char *>(logits) + row * (int64_t)V * elem, V);
-  if (threadIdx.x == 0) pred[row] = best;
-}
-
-// Thread per request: longest agreeing prefix and the next token.
-__global__ void k_accept_prefix(const int32_t *__restrict__ pred,
-                                const int32_t *__restrict__ drafts, int32_t B, int32_t d,
-                                int32_t *__restrict__ accept_len,
-                                int32_t *__restrict__ next_token) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= B) return;
-  const int32_t *p = pred + (int64_t)b * (d + 1);
+  if (threadIdx.x != 0) return;
+  pred[row] = best;
+  __threadfence();
+  const int64_t b = row / (d + 1);
+  if (atomicAdd(&count[b], 1) != d) return;
+  __threadfence();   // every row of request b has its pred
+  count[b] = 0;
+  const int32_t *p = pred + b * (d + 1);
   int m = 0;
-  while (m < d && drafts[(int64_t)b * d + m] == p[m]) ++m;
+  while (m < d && drafts[b * d + m] == __ldcg(p + m)) ++m;
   accept_len[b] = m;
-  next_token[b] = p[m];
+  next_token[b] = __ldcg(p + m);
 }
 
 }  // namespace
@@ -89,17 +100,18 @@ extern "C" int hs_verify_accept_noalloc(const void *logits, int32_t logits_dtype
     return hs_set_error(HS_ERR_INVALID_ARG, "logits_dtype %d", logits_dtype);
   if (!logits || (d > 0 && !draft_tokens) || !accept_len || !next_token)
     return hs_set_error(HS_ERR_INVALID_ARG, "NULL argument");
-  int32_t *pred = nullptr;
-  int rc = scratch_for_current_device(&pred);
+  int32_t *pred = nullptr, *count = nullptr;
+  int rc = scratch_for_current_device(&pred, &count);
   if (rc) return rc;
   const int rows = B * (d + 1);
   if (logits_dtype == HS_LOGITS_F32)
-    k_accept_argmax<HS_LOGITS_F32><<<rows, HS_ARGMAX_THREADS, 0, stream>>>(logits, V, pred);
+    k_accept<HS_LOGITS_F32><<<rows, HS_ARGMAX_THREADS, 0, stream>>>(logits, V, d, draft_tokens,
+                                                                    pred, count, accept_len,
+                                                                    next_token);
   else
-    k_accept_argmax<HS_LOGITS_BF16><<<rows, HS_ARGMAX_THREADS, 0, stream>>>(logits, V, pred);
-  HS_LAUNCH_CHECK("k_accept_argmax");
-  k_accept_prefix<<<(B + 127) / 128, 128, 0, stream>>>(pred, draft_tokens, B, d, accept_len,
-                                                       next_token);
-  HS_LAUNCH_CHECK("k_accept_prefix");
+    k_accept<HS_LOGITS_BF16><<<rows, HS_ARGMAX_THREADS, 0, stream>>>(logits, V, d, draft_tokens,
+                                                                     pred, count, accept_len,
+                                                                     next_token);
+  HS_LAUNCH_CHECK("k_accept");
   return HS_OK;
 }

@@ -8,13 +8,12 @@
 // picked last has no KV until the next round, where it is the anchor at
 // position L (section ⑥ and the closing table).
 //
-// Two launches:
-//   k_verify_argmax  block per (request, input) row: streaming argmax over the
-//                    vocabulary with 16-byte loads, ties to the lowest index
-//   k_verify_commit  block per request: accepted length, next token, host-pool
-//                    write of the kept rows through the mapped pool, LRU slot
-//                    choice (the head of the request's (ts, slot) order, which
-//                    is then rotated), hot-slot write and the kv_len update
+// One launch, k_verify: a block per (request, input) row takes the streaming
+// argmax over the vocabulary (16-byte loads, ties to the lowest index); the
+// last of a request's rows to finish then, with the whole block, takes the
+// accepted length and next token and commits: host-pool write of the kept
+// rows through the mapped pool, LRU slot choice (the head of the request's
+// (ts, slot) order, which is then rotated), hot-slot write, kv_len update.
 
 #include <float.h>
 
@@ -22,39 +21,54 @@
 
 namespace {
 
-template <int DTYPE>
-__global__ void __launch_bounds__(HS_ARGMAX_THREADS) k_verify_argmax(const void *__restrict__ logits,
-                                                                    int32_t V, int32_t rows_per_req,
-                                                                    int32_t n_step,
-                                                                    int32_t *__restrict__ pred) {
-  const int64_t row = blockIdx.x;
-  const int64_t elem = (DTYPE == HS_LOGITS_F32) ? 4 : 2;
-  const int32_t best = hs_row_argmax<DTYPE>(
-      reinterpret_cast<const char *>(logits) + row * (int64_t)V * elem, V);
-  if (threadIdx.x == 0) {
-    const int64_t req = row / rows_per_req, i = row % rows_per_req;
-    pred[req * n_step + i] = best;
-  }
-}
+struct CommitArgs {
+  int32_t d;
+  const int32_t *drafts;
+  int32_t *pred;
+  const uint4 *step_kv;
+  const int32_t *req_ids;
+  int32_t *kv_len, *accept_len, *next_token;
+  int32_t max_reqs, S, S_tot, n_step, max_ctx, block_size, hbt_stride;
+  const int32_t *hbt;
+  int64_t pool_rows;
+  uint4 *pool, *hot;
+  int32_t *token_slot, *slot_token;
+  int64_t *slot_ts;
+  int32_t *lru_order;
+  uint32_t *status;
+  int64_t now;
+};
 
-__global__ void __launch_bounds__(256) k_verify_commit(
-    int32_t d, const int32_t *__restrict__ drafts, const int32_t *__restrict__ pred,
-    const uint4 *__restrict__ step_kv, const int32_t *__restrict__ req_ids,
-    int32_t *kv_len, int32_t *accept_len, int32_t *next_token, int32_t max_reqs, int32_t S,
-    int32_t S_tot, int32_t n_step, int32_t max_ctx, int32_t block_size, int32_t hbt_stride,
-    const int32_t *__restrict__ hbt, int64_t pool_rows, uint4 *pool, uint4 *hot,
-    int32_t *token_slot, int32_t *slot_token, int64_t *slot_ts, int32_t *lru_order,
-    uint32_t *status, int64_t now) {
-  const int b = blockIdx.x;
+// Acceptance and commit of batch request b, by a whole block (HS_ARGMAX_THREADS
+// threads): longest agreeing prefix m and next token; then the m + 1 kept step
+// rows go to the host pool and to the first m + 1 slots of the LRU order
+// (nothing protected), which take the current time and move to the order's
+// end; the maps and kv_len follow. `ord` is S int32 of dynamic shared memory.
+__device__ __forceinline__ void commit_request(const int b, const CommitArgs &ca, int32_t *ord) {
+  const int32_t d = ca.d;
+  const int32_t *drafts = ca.drafts;
+  const int32_t *pred = ca.pred;
+  const uint4 *step_kv = ca.step_kv;
+  const int32_t *req_ids = ca.req_ids;
+  int32_t *kv_len = ca.kv_len, *accept_len = ca.accept_len, *next_token = ca.next_token;
+  const int32_t max_reqs = ca.max_reqs, S = ca.S, S_tot = ca.S_tot, n_step = ca.n_step,
+                max_ctx = ca.max_ctx, block_size = ca.block_size, hbt_stride = ca.hbt_stride;
+  const int32_t *hbt = ca.hbt;
+  const int64_t pool_rows = ca.pool_rows;
+  uint4 *pool = ca.pool, *hot = ca.hot;
+  int32_t *token_slot = ca.token_slot, *slot_token = ca.slot_token, *lru_order = ca.lru_order;
+  int64_t *slot_ts = ca.slot_ts;
+  uint32_t *status = ca.status;
+  const int64_t now = ca.now;
   __shared__ int sm_m, sm_L, sm_ok;
   __shared__ int32_t chosen[HS_MAX_STEP];
   const int32_t req = req_ids ? req_ids[b] : b;
   if (threadIdx.x == 0) {
-    const int32_t *p = pred + (int64_t)b * n_step;
+    const int32_t *p = pred + (int64_t)b * n_step;   // rows written by other blocks
     int m = 0;
-    while (m < d && drafts[(int64_t)b * d + m] == p[m]) ++m;
+    while (m < d && drafts[(int64_t)b * d + m] == __ldcg(p + m)) ++m;
     accept_len[b] = m;
-    next_token[b] = p[m];
+    next_token[b] = __ldcg(p + m);
     int ok = 1;
     int L = 0;
     if (req < 0 || req >= max_reqs) {
@@ -77,7 +91,6 @@ __global__ void __launch_bounds__(256) k_verify_commit(
   // The victims are the first n slots of the LRU order (ascending (ts, slot),
   // nothing protected). They take the current time, so the new order is the
   // rest of the order followed by the victims in slot order.
-  extern __shared__ int32_t ord[];                 // [S]
   int32_t *lru = lru_order + sbase;
   for (int i = threadIdx.x; i < S; i += blockDim.x) ord[i] = lru[i];
   __syncthreads();
@@ -123,6 +136,35 @@ __global__ void __launch_bounds__(256) k_verify_commit(
   if (threadIdx.x == 0) kv_len[req] = L + n;
 }
 
+
+// Block per logits row: its argmax into pred; the request's last row to finish
+// (a count per request, put back to 0) then commits the request with the
+// whole block.
+template <int DTYPE>
+__global__ void __launch_bounds__(HS_ARGMAX_THREADS) k_verify(const void *__restrict__ logits,
+                                                             int32_t V, int32_t *row_count,
+                                                             const __grid_constant__ CommitArgs ca) {
+  extern __shared__ int32_t ord[];                 // [S], for the commit
+  __shared__ int s_last;
+  const int64_t row = blockIdx.x;
+  const int rows_per_req = ca.d + 1;
+  const int64_t elem = (DTYPE == HS_LOGITS_F32) ? 4 : 2;
+  const int32_t best = hs_row_argmax<DTYPE>(
+      reinterpret_cast<const char *>(logits) + row * (int64_t)V * elem, V);
+  const int b = (int)(row / rows_per_req);
+  if (threadIdx.x == 0) {
+    ca.pred[(int64_t)b * ca.n_step + row % rows_per_req] = best;
+    __threadfence();
+    s_last = atomicAdd(&row_count[b], 1) == ca.d;
+    if (s_last) {
+      __threadfence();   // every row of request b has its pred
+      row_count[b] = 0;
+    }
+  }
+  __syncthreads();
+  if (s_last) commit_request(b, ca, ord);
+}
+
 }  // namespace
 
 extern "C" int hs_verify_finalize(hs_buffer *buf, const void *logits, int32_t logits_dtype,
@@ -142,20 +184,22 @@ extern "C" int hs_verify_finalize(hs_buffer *buf, const void *logits, int32_t lo
     return hs_set_error(HS_ERR_INVALID_ARG, "step_kv must be 16-byte aligned");
   buf->clock += 1;
   const int rows = B * (d + 1);
+  CommitArgs ca;
+  ca.d = d; ca.drafts = draft_tokens; ca.pred = buf->pred;
+  ca.step_kv = reinterpret_cast<const uint4 *>(step_kv); ca.req_ids = req_ids;
+  ca.kv_len = kv_len; ca.accept_len = accept_len; ca.next_token = next_token;
+  ca.max_reqs = buf->max_reqs; ca.S = buf->S; ca.S_tot = buf->S_tot; ca.n_step = buf->n_step;
+  ca.max_ctx = buf->max_ctx; ca.block_size = buf->block_size; ca.hbt_stride = buf->hbt_stride;
+  ca.hbt = buf->hbt; ca.pool_rows = buf->host_pool_rows;
+  ca.pool = reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(buf->host_pool));
+  ca.hot = reinterpret_cast<uint4 *>(buf->hot_kv);
+  ca.token_slot = buf->token_slot; ca.slot_token = buf->slot_token; ca.slot_ts = buf->slot_ts;
+  ca.lru_order = buf->lru_order; ca.status = buf->status; ca.now = buf->clock;
+  const size_t smem = (size_t)buf->S * sizeof(int32_t);
   if (logits_dtype == HS_LOGITS_F32)
-    k_verify_argmax<HS_LOGITS_F32><<<rows, HS_ARGMAX_THREADS, 0, stream>>>(logits, V, d + 1, buf->n_step,
-                                                             buf->pred);
+    k_verify<HS_LOGITS_F32><<<rows, HS_ARGMAX_THREADS, smem, stream>>>(logits, V, buf->row_count, ca);
   else
-    k_verify_argmax<HS_LOGITS_BF16><<<rows, HS_ARGMAX_THREADS, 0, stream>>>(logits, V, d + 1, buf->n_step,
-                                                              buf->pred);
-  HS_LAUNCH_CHECK("k_verify_argmax");
-  k_verify_commit<<<B, 256, (size_t)buf->S * sizeof(int32_t), stream>>>(
-      d, draft_tokens, buf->pred, reinterpret_cast<const uint4 *>(step_kv), req_ids, kv_len,
-      accept_len, next_token, buf->max_reqs, buf->S, buf->S_tot, buf->n_step, buf->max_ctx,
-      buf->block_size, buf->hbt_stride, buf->hbt, buf->host_pool_rows,
-      reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(buf->host_pool)),
-      reinterpret_cast<uint4 *>(buf->hot_kv), buf->token_slot, buf->slot_token, buf->slot_ts,
-      buf->lru_order, buf->status, buf->clock);
-  HS_LAUNCH_CHECK("k_verify_commit");
+    k_verify<HS_LOGITS_BF16><<<rows, HS_ARGMAX_THREADS, smem, stream>>>(logits, V, buf->row_count, ca);
+  HS_LAUNCH_CHECK("k_verify");
   return HS_OK;
 }

@@ -458,14 +458,16 @@ int hs_verify_finalize(hs_buffer *buf, const void *logits, int32_t logits_dtype,
  * bring. It needs no hs_buffer and commits no KV (the caller does that).
  *   logits, logits_dtype, draft_tokens, accept_len, next_token: as for
  *   hs_verify_finalize ([B][d+1][V] logits, [B][d] drafts, [B] outputs).
- * Scratch: a static device array of 65536 int32 (256 KiB) inside the library,
- * held by every GPU that loads it until the process exits. Sizes with
- * B * (d + 1) > 65536 return HS_ERR_INVALID_ARG. No cudaMalloc, cudaFree or
- * allocating library routine is called. The first call on a device looks up
- * the array's device address (cudaGetSymbolAddress); make that first call
- * before any stream capture. Every call writes all the scratch rows it reads,
- * so nothing carries over between calls, but all calls share the one array:
- * calls that overlap on the GPU (different streams without ordering) race.
+ * Scratch: two static device arrays of 65536 int32 (512 KiB) inside the
+ * library (per-row argmax, per-request row counts), held by every GPU that
+ * loads it until the process exits. Sizes with B * (d + 1) > 65536 return
+ * HS_ERR_INVALID_ARG. No cudaMalloc, cudaFree or allocating library routine
+ * is called. The first call on a device looks up the arrays' device addresses
+ * (cudaGetSymbolAddress); make that first call before any stream capture. One
+ * launch: the last row of each request to finish takes its prefix and puts
+ * the request's count back to 0, so nothing carries over between calls, but
+ * all calls share the arrays: calls that overlap on the GPU (different
+ * streams without ordering) race.
  * Requirements: B >= 1, d >= 0, V >= 1.
  */
 int hs_verify_accept_noalloc(const void *logits, int32_t logits_dtype, int32_t B,
