@@ -346,7 +346,7 @@ def run_e2e(hs, cfg, rc, dev, args):
     return {"value": round(R / (ms * 1e-3), 1), "unit": "query-rows/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "chunks_per_step": n_ch, "cuda_graph": True,
-            "l2": "not flushed between steps: the KV cache read (302 MB) is larger than L2, "
+            "l2": "not flushed between steps: the KV cache (304 MB) is larger than L2, "
                   "and each step copies 36.7 MB through it"}
 
 
