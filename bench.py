@@ -350,6 +350,17 @@ def run_e2e(hs, cfg, rc, dev, args):
                   "and each step copies 36.7 MB through it"}
 
 
+def _lead(stream=None, cycles=1 << 18):
+    """A short GPU sleep on the timing stream right before a timed region, so
+    that the host has queued the timed calls before the first event fires
+    and the events bracket GPU work, not host-side launch time."""
+    if stream is None:
+        torch.cuda._sleep(cycles)
+    else:
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(cycles)
+
+
 def measure_link(hs, dev):
     """Host->device bandwidth: best of a 1 GiB pinned cudaMemcpyAsync and the
     zero-copy read probe over the same pinned buffer."""
@@ -360,6 +371,7 @@ def measure_link(hs, dev):
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     best_copy = 0.0
     for _ in range(3):
+        _lead()
         a.record()
         d.copy_(host, non_blocking=True)
         b.record()
@@ -370,6 +382,7 @@ def measure_link(hs, dev):
     for blocks in (sms * 4, sms * 8, sms * 16):
         sink = torch.empty(blocks, dtype=torch.int64, device=dev)
         for _ in range(2):
+            _lead()
             a.record()
             hs.hs_read_probe(host, sink, blocks)
             b.record()
@@ -393,7 +406,6 @@ def run_swap_bench(hs, dev, args):
              for s in range(cfg.steps)]
     t_req, t_clen = torch.as_tensor(req, device=dev), torch.as_tensor(clen, device=dev)
     out = torch.empty((cfg.R, cfg.K), dtype=torch.int32, device=dev)
-    stats = torch.zeros(2, dtype=torch.int64, device=dev)
     q = W.step_q(cfg, 0, device=dev)
     o = torch.empty((cfg.R, cfg.H, 512), dtype=torch.bfloat16, device=dev)
     # two follower layers (next row 1): their own hot buffers and host pools,
@@ -401,24 +413,29 @@ def run_swap_bench(hs, dev, args):
     n_follow = 2
     f_hot = [torch.empty_like(hb["hot"]) for _ in range(n_follow)]
     f_pool = [W.host_pool_tensor(hb["pool"].shape[0], 900 + i, device=dev) for i in range(n_follow)]
-    a, b, c, d = (torch.cuda.Event(enable_timing=True) for _ in range(4))
-
     def sequence(buf):
-        swap_ms, attn_ms, apply_ms, miss = [], [], [], []
+        # the steps are queued back to back, as a decode loop issues them (no
+        # host synchronisation between steps), so each step's events time the
+        # GPU work alone; a short GPU sleep first lets step 0 be queued before
+        # its first event
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(cfg.steps)]
+        st = torch.zeros((cfg.steps, 2), dtype=torch.int64, device=dev)
+        torch.cuda.synchronize()
+        _lead(cycles=1 << 20)
         for s in range(cfg.steps):
-            stats.zero_()
-            a.record()
-            hs.hs_swap_in(buf, t_req, t_clen, hb["kv_len"], topks[s], out, None, stats)
-            b.record()
+            e = evs[s]
+            e[0].record()
+            hs.hs_swap_in(buf, t_req, t_clen, hb["kv_len"], topks[s], out, None, st[s])
+            e[1].record()
             hs.hs_sparse_attn_decode(q, hb["hot"], out, cfg.scale, o)
-            c.record()
+            e[2].record()
             hs.hs_swap_apply_plan(buf, f_hot, f_pool)
-            d.record()
-            d.synchronize()
-            swap_ms.append(a.elapsed_time(b))
-            attn_ms.append(b.elapsed_time(c))
-            apply_ms.append(c.elapsed_time(d))
-            miss.append(int(stats[1].item()))
+            e[3].record()
+        torch.cuda.synchronize()
+        swap_ms = [e[0].elapsed_time(e[1]) for e in evs]
+        attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+        apply_ms = [e[2].elapsed_time(e[3]) for e in evs]
+        miss = [int(x) for x in st[:, 1].tolist()]
         return swap_ms, attn_ms, apply_ms, miss
 
     # the sequence runs twice, each time on an empty hot buffer; the first run
@@ -477,6 +494,7 @@ def run_verify_bench(hs, dev, peak_hbm):
     # all 264.8 MB again: more than L2); the per-call time is the mean
     ms = []
     for _ in range(5):
+        _lead()
         a.record()
         for _ in range(10):
             hs.hs_verify_accept_noalloc(logits, t_drafts, acc, nxt)
@@ -496,6 +514,7 @@ def run_verify_bench(hs, dev, peak_hbm):
     out_idx = torch.empty((cfg.R, cfg.K), dtype=torch.int32, device=dev)
     hs.hs_swap_in(buf, torch.as_tensor(req, device=dev), clen, hb["kv_len"], topk, out_idx)
     skv = W.step_kv(cfg, 0, device=dev)
+    _lead()
     a.record()
     hs.hs_verify_finalize(buf, logits, t_drafts, skv, hb["kv_len"], acc, nxt)
     b.record()
@@ -568,6 +587,7 @@ def run_overlap_bench(hs, dev, steps=8):
         hs.hs_buffer_set_copy_sms(buf, n_sms)
         ms = []
         for st in range(steps):
+            _lead(s1)
             a.record(s1)
             fn(buf, st)
             b.record(s1)
@@ -604,6 +624,7 @@ def run_backup_bench(hs, dev, layers=4, pages=512, block_rows=64):
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ms = []
     for _ in range(6):
+        _lead()
         a.record()
         hs.hs_backup_pages(src, dst, src_blocks, dst_blocks, offs, block_rows, 2)
         b.record()
@@ -616,6 +637,7 @@ def run_backup_bench(hs, dev, layers=4, pages=512, block_rows=64):
     dsrc = torch.empty(n, dtype=torch.uint8, device=dev)
     best_copy = 0.0
     for _ in range(3):
+        _lead()
         a.record()
         host.copy_(dsrc, non_blocking=True)
         b.record()
@@ -627,6 +649,7 @@ def run_backup_bench(hs, dev, layers=4, pages=512, block_rows=64):
     def timed(fn):
         ts = []
         for _ in range(6):
+            _lead()
             a.record()
             fn()
             b.record()

@@ -108,6 +108,30 @@ constexpr int ORD_REGS = HS_MAX_SLOTS / SW_THREADS;   // LRU order entries a thr
 
 __device__ __forceinline__ bool bit_of(const uint32_t *bm, int s) { return (bm[s >> 5] >> (s & 31)) & 1u; }
 
+// Exclusive scan over the block's 32 warps of one count per warp (every lane
+// passes its warp's count): the warp's offset, and the total in *total.
+// tmp holds 33 ints; every thread calls it.
+__device__ __forceinline__ int warp_exscan(int cnt, int *tmp, int *total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (lane == 0) tmp[w] = cnt;
+  __syncthreads();
+  if (w == 0) {
+    const int x = tmp[lane];
+    int xi = x;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, xi, off);
+      if (lane >= off) xi += y;
+    }
+    tmp[lane] = xi - x;
+    if (lane == 31) tmp[32] = xi;
+  }
+  __syncthreads();
+  const int r = tmp[w];
+  *total = tmp[32];
+  __syncthreads();
+  return r;
+}
+
 // Rows of request b among rows [from, R): fills rows[] with up to ROW_CHUNK of
 // them (in row order) and returns the count and the next scan position.
 __device__ int collect_rows(const SwapArgs &a, int b, int from, int *rows, int *next, int *s_cnt) {
@@ -205,11 +229,12 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
     if (out_valid)   // counted by the gather's table pass
       for (int i = threadIdx.x; i < n; i += SW_THREADS) out_valid[rows[i]] = 0;
     const int items = n * a.K;
-    // PB entries per thread per round: their loads, claims and lookups are all
-    // in flight together (each is a dependent global access)
+    // PB entries per thread per round. Every committed entry looks up its
+    // position's slot; a hit marks the slot (distinct hits = marked slots),
+    // and only a miss claims its position, so that a position missed by
+    // several rows gets one slot. The loads of a round are in flight together.
     for (int base = 0; base < items; base += SW_THREADS * PB) {
       int32_t t[PB], clen[PB], sl[PB];
-      bool first[PB];
 #pragma unroll
       for (int u = 0; u < PB; ++u) {
         const int i = base + u * SW_THREADS + (int)threadIdx.x;
@@ -221,36 +246,42 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
           clen[u] = a.clen[row];
         }
       }
+      bool bad = false;
 #pragma unroll
       for (int u = 0; u < PB; ++u) {
         const bool committed = t[u] >= 0 && t[u] < clen[u] && t[u] < L && t[u] < a.max_ctx;
-        if (use_bm) {
-          const uint32_t bit = 1u << (committed ? (t[u] & 31) : 0);
-          first[u] = committed && !(atomicOr(&pneed[committed ? (t[u] >> 5) : 0], bit) & bit);
-        } else {
-          first[u] = committed && atomicExch(&a.pos_mark[cbase + t[u]], a.epoch) != a.epoch;
-        }
+        bad |= t[u] >= 0 && (t[u] >= clen[u] || (t[u] < L && t[u] >= a.max_ctx));
+        sl[u] = committed ? a.token_slot[cbase + t[u]] : INT32_MIN;
       }
-#pragma unroll
-      for (int u = 0; u < PB; ++u) sl[u] = first[u] ? a.token_slot[cbase + t[u]] : -1;
+      unsigned mm[PB];
+      int my_total = 0;
 #pragma unroll
       for (int u = 0; u < PB; ++u) {
-        if (first[u] && sl[u] >= 0 && sl[u] < a.S) atomicOr(&hitmap[sl[u] >> 5], 1u << (sl[u] & 31));
-        const bool bad = t[u] >= 0 && (t[u] >= clen[u] || (t[u] < L && t[u] >= a.max_ctx));
-        const bool miss = first[u] && sl[u] < 0;
-        const unsigned bad_mask = __ballot_sync(0xffffffffu, bad);
-        const unsigned first_mask = __ballot_sync(0xffffffffu, first[u]);
-        const unsigned miss_mask = __ballot_sync(0xffffffffu, miss);
-        int mbase = 0;
-        if (lane == 0) {
-          if (bad_mask) s_bad = 1;
-          if (first_mask) atomicAdd(&s_need, __popc(first_mask));
-          if (miss_mask) mbase = atomicAdd(&s_miss, __popc(miss_mask));
+        if (sl[u] >= 0 && sl[u] < a.S) atomicOr(&hitmap[sl[u] >> 5], 1u << (sl[u] & 31));
+        bool first = false;
+        if (sl[u] < 0 && sl[u] != INT32_MIN) {      // a committed position not in the buffer
+          if (use_bm) {
+            const uint32_t bit = 1u << (t[u] & 31);
+            first = !(atomicOr(&pneed[t[u] >> 5], bit) & bit);
+          } else {
+            first = atomicExch(&a.pos_mark[cbase + t[u]], a.epoch) != a.epoch;
+          }
         }
+        mm[u] = __ballot_sync(0xffffffffu, first);
+        my_total += __popc(mm[u]);
+      }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) s_bad = 1;
+      if (my_total) {
+        int mbase = 0;
+        if (lane == 0) mbase = atomicAdd(&s_miss, my_total);
         mbase = __shfl_sync(0xffffffffu, mbase, 0);
-        if (miss) {
-          const int pos = mbase + __popc(miss_mask & ((1u << lane) - 1u));
-          if (pos < a.S) mkey[pos] = t[u];   // beyond S the request is refused below
+#pragma unroll
+        for (int u = 0; u < PB; ++u) {
+          if ((mm[u] >> lane) & 1u) {
+            const int pos = mbase + __popc(mm[u] & ((1u << lane) - 1u));
+            if (pos < a.S) mkey[pos] = t[u];   // beyond S the request is refused below
+          }
+          mbase += __popc(mm[u]);
         }
       }
     }
@@ -261,7 +292,12 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
   if (threadIdx.x == 0 && s_bad) atomicOr(a.status, HS_STATUS_INDEX);
 
   // ---- assign ---------------------------------------------------------------
-  const int need = s_need, nm = s_miss;
+  for (int w = threadIdx.x; w < (a.S + 31) / 32; w += SW_THREADS) {
+    const int c = __popc(hitmap[w]);
+    if (c) atomicAdd(&s_need, c);
+  }
+  __syncthreads();
+  const int nm = s_miss, need = s_need + nm;
   const bool failed = need > a.S;
   if (failed) {
     if (threadIdx.x == 0) {
@@ -274,32 +310,66 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
       atomicAdd((unsigned long long *)&a.stats[1], (unsigned long long)nm);
     }
     // victims: the first nm slots of the LRU order (ascending (ts, slot)) that
-    // hold no position needed in this call
+    // hold no position needed in this call. Order position i = w * CH + 32 j
+    // + lane belongs to warp w, round j; ranks come from warp ballots and one
+    // scan of the warp counts, so the writes of a warp are contiguous.
     int32_t *lru = a.lru_order + sbase;
 #pragma unroll
     for (int u = 0; u < ORD_REGS; ++u) {
       const int i = u * SW_THREADS + (int)threadIdx.x;
       if (i < a.S) ord[i] = ordv[u];
     }
+    const int w = threadIdx.x >> 5;
+    const int CH = ((a.S + 31) / 32 + 31) / 32 * 32;   // order positions per warp
+    const int NR = CH / 32;                             // rounds (at most ORD_REGS)
     __syncthreads();
-    {
-      const int E = (a.S + SW_THREADS - 1) / SW_THREADS;
-      const int lo = threadIdx.x * E, hi = min(a.S, lo + E);
-      int cnt = 0;
-      for (int i = lo; i < hi; ++i) cnt += !bit_of(hitmap, ord[i]);
-      int tot;
-      int k = hs_block_exscan(cnt, scan_tmp, &tot);
-      for (int i = lo; i < hi && k < nm; ++i)
-        if (!bit_of(hitmap, ord[i])) vict[k++] = ord[i];
+    unsigned fm[ORD_REGS];                              // free (not hit) slots, by round
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < ORD_REGS; ++j) {
+      const int i = w * CH + j * 32 + lane;
+      fm[j] = __ballot_sync(0xffffffffu, j < NR && i < a.S && !bit_of(hitmap, ord[i]));
+      cnt += __popc(fm[j]);
+    }
+    int n_free;
+    int k = warp_exscan(cnt, scan_tmp, &n_free);
+    // the first nm free slots become victims (touched from now on); the
+    // other free slots keep their order at the front of the new LRU order
+#pragma unroll
+    for (int j = 0; j < ORD_REGS; ++j) {
+      if ((fm[j] >> lane) & 1u) {
+        const int r = k + __popc(fm[j] & ((1u << lane) - 1u));
+        const int32_t sl = ord[w * CH + j * 32 + lane];
+        if (r < nm) {
+          vict[r] = sl;
+          atomicOr(&hitmap[sl >> 5], 1u << (sl & 31));
+        } else {
+          lru[r - nm] = sl;
+        }
+      }
+      k += __popc(fm[j]);
     }
     __syncthreads();
-    // hits and victims take the current time; the LRU order moves them last
-    for (int i = threadIdx.x; i < nm; i += SW_THREADS)
-      atomicOr(&hitmap[vict[i] >> 5], 1u << (vict[i] & 31));
-    __syncthreads();
-    hs_lru_reorder(ord, hitmap, a.S, lru, scan_tmp);
-    for (int sl = threadIdx.x; sl < a.S; sl += SW_THREADS)
-      if (bit_of(hitmap, sl)) a.slot_ts[sbase + sl] = a.now;
+    // hits and victims take the current time and follow in slot order
+    unsigned tm[ORD_REGS];
+    int ct = 0;
+#pragma unroll
+    for (int j = 0; j < ORD_REGS; ++j) {
+      const int sl = w * CH + j * 32 + lane;
+      tm[j] = __ballot_sync(0xffffffffu, j < NR && sl < a.S && bit_of(hitmap, sl));
+      ct += __popc(tm[j]);
+    }
+    int n_touched;
+    k = warp_exscan(ct, scan_tmp, &n_touched) + (n_free - nm);
+#pragma unroll
+    for (int j = 0; j < ORD_REGS; ++j) {
+      if ((tm[j] >> lane) & 1u) {
+        const int sl = w * CH + j * 32 + lane;
+        lru[k + __popc(tm[j] & ((1u << lane) - 1u))] = sl;
+        a.slot_ts[sbase + sl] = a.now;
+      }
+      k += __popc(tm[j]);
+    }
     if (nm > 0) {
       // misses in ascending position order take the victims in order: the
       // i-th smallest miss position gets vict[i]
