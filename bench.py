@@ -202,6 +202,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         for e in evs:
             flush.fill_(1)
+            _lead(stream)
             e[0].record(stream)
             hs.hs_resolve_topk(rc["req"], rc["clen"], rc["bt"], rc["topk"], cfg.block_size,
                                cfg.block_size, idx, valid)
