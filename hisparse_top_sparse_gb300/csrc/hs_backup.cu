@@ -219,6 +219,111 @@ __global__ void __launch_bounds__(BR_THREADS) k_backup_rows_narrow(
   if (bad && status) atomicOr(status, HS_STATUS_INDEX);
 }
 
+// Short rows that do not go 16 bytes at a time (token_stride not a multiple
+// of 16, or a host cache off 16-byte alignment): a warp takes RUN_EPL * 32
+// consecutive entries, compacts the ones with a row to copy (in entry order)
+// and works through them 32 at a time. Entries whose host rows are
+// consecutive form a run; the run's rows are staged in the warp's shared
+// memory as the run's byte image and written out as the 16-byte-aligned
+// chunks of host memory they cover, the run's partial first and last chunks
+// word by word. A backup of whole blocks (consecutive host rows) is thus
+// written in whole lines over the host link; scattered rows are runs of one.
+constexpr int RUN_EPL = 4;
+constexpr int RUN_WARPS = 8;
+
+__global__ void __launch_bounds__(RUN_WARPS * 32) k_backup_runs(
+    const __grid_constant__ RowLayers rl, int32_t n_layers, const int32_t *__restrict__ src_slots,
+    const int32_t *__restrict__ dst_slots, const int32_t *__restrict__ positions, int32_t n,
+    int32_t words, int32_t sbs, int32_t ratio, int64_t src_rows, int64_t dst_rows,
+    uint32_t *status) {
+  extern __shared__ uint32_t run_smem[];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  uint32_t *img = run_smem + (size_t)wib * (32 * words + 64);   // 32 rows' image
+  int32_t *s_sr = reinterpret_cast<int32_t *>(img + 32 * words);  // their device rows
+  int32_t *s_dr = s_sr + 32;                                       // their host rows
+  const int lbs = sbs * ratio;
+  const int64_t G = 32 * RUN_EPL;
+  const int64_t n_groups = ((int64_t)n + G - 1) / G;
+  const unsigned lt = (1u << lane) - 1u;
+  bool bad = false;
+  for (int64_t g = (int64_t)blockIdx.x * RUN_WARPS + wib; g < n_groups;
+       g += (int64_t)gridDim.x * RUN_WARPS) {
+    int32_t sr[RUN_EPL], dr[RUN_EPL];
+    unsigned vm[RUN_EPL];
+    int total = 0;
+#pragma unroll
+    for (int e = 0; e < RUN_EPL; ++e) {
+      const int64_t i = g * G + e * 32 + lane;
+      bool v = false;
+      sr[e] = -1;
+      dr[e] = -1;
+      if (i < n) {
+        sr[e] = __ldg(src_slots + i);
+        dr[e] = __ldg(dst_slots + i);
+        if (ratio > 0) {
+          const int p = __ldg(positions + i);
+          dr[e] = (dr[e] < 0 || p < 0) ? -1 : (dr[e] / lbs) * sbs + (p % lbs) / ratio;
+        }
+        if (sr[e] >= 0 && dr[e] >= 0) {
+          if (sr[e] < src_rows && dr[e] < dst_rows) v = true;
+          else bad = true;
+        }
+      }
+      vm[e] = __ballot_sync(0xffffffffu, v);
+      total += __popc(vm[e]);
+    }
+    for (int b0 = 0; b0 < total; b0 += 32) {
+      const int nb = min(32, total - b0);
+      int base = 0;
+#pragma unroll
+      for (int e = 0; e < RUN_EPL; ++e) {
+        if ((vm[e] >> lane) & 1u) {
+          const int k = base + __popc(vm[e] & lt) - b0;
+          if (k >= 0 && k < 32) { s_sr[k] = sr[e]; s_dr[k] = dr[e]; }
+        }
+        base += __popc(vm[e]);
+      }
+      __syncwarp();
+      const unsigned rs =
+          __ballot_sync(0xffffffffu, lane < nb && (lane == 0 || s_dr[lane] != s_dr[lane - 1] + 1));
+      for (int l = 0; l < n_layers; ++l) {
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(rl.src[l]);
+        for (int w = lane; w < nb * words; w += 32) {
+          const int k = w / words;
+          img[w] = src[(int64_t)s_sr[k] * words + (w - k * words)];
+        }
+        __syncwarp();
+        // word 0 of `dst` is the 16-byte aligned address at or below the
+        // cache's start; `mis` words lie between the two
+        const int mis = (int)((reinterpret_cast<uintptr_t>(rl.dst[l]) >> 2) & 3);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(reinterpret_cast<uintptr_t>(rl.dst[l]) & ~(uintptr_t)15);
+        unsigned m = rs;
+        while (m) {
+          const int k0 = __ffs(m) - 1;
+          m &= m - 1;
+          const int k1 = m ? __ffs(m) - 1 : nb;
+          const int64_t d0 = (int64_t)s_dr[k0] * words + mis;    // the run's first host word
+          const int64_t d1 = d0 + (int64_t)(k1 - k0) * words;
+          const int64_t i0 = (int64_t)k0 * words - d0;           // image index = host word + i0
+          for (int64_t c = (d0 >> 2) + lane; c < ((d1 + 3) >> 2); c += 32) {
+            const int64_t w0 = 4 * c;
+            if (w0 >= d0 && w0 + 4 <= d1) {
+              const uint32_t *ip = img + (w0 + i0);
+              *reinterpret_cast<uint4 *>(dst + w0) = make_uint4(ip[0], ip[1], ip[2], ip[3]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (w0 + e >= d0 && w0 + e < d1) dst[w0 + e] = img[w0 + e + i0];
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+  }
+  if (bad && status) atomicOr(status, HS_STATUS_INDEX);
+}
+
 int backup_rows_impl(int32_t n_layers, const void *const *src_caches, void *const *dst_caches,
                      const int32_t *src_slots, const int32_t *dst_slots,
                      const int32_t *positions, int32_t n, int32_t sbs, int32_t ratio,
@@ -251,6 +356,26 @@ int backup_rows_impl(int32_t n_layers, const void *const *src_caches, void *cons
   // (1152-byte rows at a 4-byte offset: 151 against 129 GB/s over the link);
   // shorter ones a word per thread (132-byte rows: 87 against 65 GB/s)
   const bool chunked = !wide && vec >= 64;
+  if (!wide && !chunked) {
+    const size_t smem = (size_t)RUN_WARPS * (32 * vec + 64) * sizeof(uint32_t);
+    static bool attr_done[64] = {false};
+    int dev = 0, nsm = 0;
+    HS_CUDA_TRY(cudaGetDevice(&dev));
+    HS_CUDA_TRY(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+    if (dev >= 64 || !attr_done[dev]) {
+      HS_CUDA_TRY(cudaFuncSetAttribute(k_backup_runs, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)((size_t)RUN_WARPS * (32 * 63 + 64) * sizeof(uint32_t))));
+      if (dev < 64) attr_done[dev] = true;
+    }
+    const int64_t groups = ((int64_t)n + 32 * RUN_EPL - 1) / (32 * RUN_EPL);
+    const int64_t want = (groups + RUN_WARPS - 1) / RUN_WARPS;
+    const int grid = (int)(want < (int64_t)nsm * 4 ? want : (int64_t)nsm * 4);
+    k_backup_runs<<<grid, RUN_WARPS * 32, smem, stream>>>(rl, n_layers, src_slots, dst_slots,
+                                                          positions, n, vec, sbs, ratio, src_rows,
+                                                          dst_rows, status);
+    HS_LAUNCH_CHECK("k_backup_runs");
+    return HS_OK;
+  }
   const int units = chunked ? vec / 4 + 2 : vec;
   const int tpr = units < BR_THREADS ? units : BR_THREADS;
   const int rows_per_block = BR_THREADS / tpr;

@@ -163,3 +163,34 @@ def test_backup_rows_and_apply_plan_64_layers():
         e = np.zeros((B * S_tot, 16), np.uint8)
         O.apply_plan(ref.last_plan, e, f_pool[l].numpy(), hbt, bs, S_tot)
         assert np.array_equal(f_hot[l].cpu().numpy(), e)
+
+
+@pytest.mark.parametrize("width,offset", [(4, 0), (20, 0), (132, 4), (128, 8), (252, 0)])
+@pytest.mark.parametrize("pattern", ["blocks", "scattered"])
+def test_backup_rows_short_rows_runs(width, offset, pattern):
+    """Rows that do not go 16 bytes at a time and are shorter than 256 bytes:
+    host rows in runs of consecutive slots (whole and partial blocks, holes,
+    entries without a row) or scattered, 2 layers, bit-exact."""
+    hs = lib()
+    g = np.random.default_rng(width * 7 + offset + (pattern == "blocks"))
+    n_src, n_dst, n, layers = 600, 1400, 1000, 2
+    src = [_rand_bytes(g, n_src, width).to(DEV) for _ in range(layers)]
+    dst = [_offset_view(n_dst, width, offset, pin=True) for _ in range(layers)]
+    src_slots = g.integers(0, n_src, size=n).astype(np.int32)
+    if pattern == "blocks":
+        # blocks of 16 host rows in shuffled order, some cut short
+        order = g.permutation(n_dst // 16)
+        dst_slots = np.concatenate([b * 16 + np.arange(16) for b in order])[:n].astype(np.int32)
+        dst_slots[g.integers(0, n, size=40)] = -1
+        src_slots[g.integers(0, n, size=40)] = -1
+    else:
+        dst_slots = g.permutation(n_dst)[:n].astype(np.int32)
+        dst_slots[::13] = -1
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hs.hs_backup_rows(src, dst, _t(src_slots), _t(dst_slots), st)
+    e_dst = [np.zeros((n_dst, width), np.uint8) for _ in range(layers)]
+    e_st = O.backup_rows([s.cpu().numpy() for s in src], e_dst, src_slots, dst_slots)
+    torch.cuda.synchronize()
+    assert int(st.item()) == e_st == 0
+    for l in range(layers):
+        assert np.array_equal(dst[l].numpy(), e_dst[l])
