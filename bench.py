@@ -265,26 +265,47 @@ def run_ours(args):
 def run_e2e(hs, cfg, rc, dev, args):
     """The same step through the C ABI from page-locked host buffers.
 
-    A step's rows go in `args.e2e_chunks` contiguous chunks over three
-    streams: while chunk k is resolved and attended, chunk k + 1's inputs come
-    in and chunk k - 1's output goes out (copies both ways overlap compute and
-    each other). Steps stay dependent: a step's first copy waits for the
+    A step's rows go in `args.e2e_chunks` contiguous chunks: inputs in on one
+    stream, output out on another, and chunk k resolved and attended on
+    compute stream k mod `args.e2e_streams`, so that while chunk k is
+    attended, chunk k + 1's inputs come in, chunk k - 1's output goes out, and
+    (with several compute streams) the attention launches of small chunks
+    share the SMs. Steps stay dependent: a step's first copy waits for the
     previous step's last result to reach host memory."""
     R, H, K = cfg.R, cfg.H, cfg.K
-    h_q = rc["q"].cpu().pin_memory()
-    h_topk = rc["topk"].cpu().pin_memory()
-    h_req = rc["req"].cpu().pin_memory()
-    h_clen = rc["clen"].cpu().pin_memory()
-    h_out = torch.empty((R, H, 512), dtype=torch.bfloat16).pin_memory()
-    d_q, d_topk = torch.empty_like(rc["q"]), torch.empty_like(rc["topk"])
-    d_req, d_clen = torch.empty_like(rc["req"]), torch.empty_like(rc["clen"])
-    idx = torch.empty_like(rc["topk"])
-    out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_topk, h_req, h_clen))
-    d2h = h_out.numel() * h_out.element_size()
     n_ch = max(1, min(args.e2e_chunks, R))
     bounds = [(R * k // n_ch, R * (k + 1) // n_ch) for k in range(n_ch)]
-    s_cap, s_in, s_cmp, s_out = (torch.cuda.Stream() for _ in range(4))
+    # each chunk's inputs (q, top-k, request ids, causal lengths of its rows)
+    # sit in one page-locked block, so a chunk comes in with one copy
+    names = ("q", "topk", "req", "clen")
+    layout, off = [], 0
+    for r0, r1 in bounds:
+        ent = {}
+        for nm in names:
+            sl = rc[nm][r0:r1]
+            off = (off + 15) // 16 * 16
+            ent[nm] = (off, sl.numel() * sl.element_size(), tuple(sl.shape), sl.dtype)
+            off += sl.numel() * sl.element_size()
+        layout.append(ent)
+    h_in = torch.empty(off, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(off, dtype=torch.uint8, device=dev)
+
+    def view(buf, e):
+        o, nb, shape, dt = e
+        return buf[o:o + nb].view(dt).view(shape)
+
+    for k, (r0, r1) in enumerate(bounds):
+        for nm in names:
+            view(h_in, layout[k][nm]).copy_(rc[nm][r0:r1].cpu())
+    spans = [(layout[k]["q"][0], layout[k]["clen"][0] + layout[k]["clen"][1]) for k in range(n_ch)]
+    h_out = torch.empty((R, H, 512), dtype=torch.bfloat16).pin_memory()
+    idx = torch.empty_like(rc["topk"])
+    out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=dev)
+    h2d = sum(hi - lo for lo, hi in spans)
+    d2h = h_out.numel() * h_out.element_size()
+    s_cap, s_in, s_out = (torch.cuda.Stream() for _ in range(3))
+    n_cmp = max(1, min(args.e2e_streams, n_ch))
+    s_cmps = [torch.cuda.Stream() for _ in range(n_cmp)]
     ev_start = torch.cuda.Event()
     ev_in = [torch.cuda.Event() for _ in bounds]
     ev_cmp = [torch.cuda.Event() for _ in bounds]
@@ -295,16 +316,16 @@ def run_e2e(hs, cfg, rc, dev, args):
         ev_start.record(s_cap)
         s_in.wait_event(ev_start)
         for k, (r0, r1) in enumerate(bounds):
+            lo, hi = spans[k]
             with torch.cuda.stream(s_in):
-                d_q[r0:r1].copy_(h_q[r0:r1], non_blocking=True)
-                d_topk[r0:r1].copy_(h_topk[r0:r1], non_blocking=True)
-                d_req[r0:r1].copy_(h_req[r0:r1], non_blocking=True)
-                d_clen[r0:r1].copy_(h_clen[r0:r1], non_blocking=True)
+                d_in[lo:hi].copy_(h_in[lo:hi], non_blocking=True)
                 ev_in[k].record(s_in)
+            s_cmp = s_cmps[k % n_cmp]
             s_cmp.wait_event(ev_in[k])
-            hs.hs_resolve_topk(d_req[r0:r1], d_clen[r0:r1], rc["bt"], d_topk[r0:r1],
-                               cfg.block_size, cfg.block_size, idx[r0:r1], stream=s_cmp)
-            hs.hs_sparse_attn_decode(d_q[r0:r1], rc["kv"], idx[r0:r1], cfg.scale, out[r0:r1],
+            d_q, d_topk, d_req, d_clen = (view(d_in, layout[k][nm]) for nm in names)
+            hs.hs_resolve_topk(d_req, d_clen, rc["bt"], d_topk, cfg.block_size, cfg.block_size,
+                               idx[r0:r1], stream=s_cmp)
+            hs.hs_sparse_attn_decode(d_q, rc["kv"], idx[r0:r1], cfg.scale, out[r0:r1],
                                      stream=s_cmp)
             ev_cmp[k].record(s_cmp)
             s_out.wait_event(ev_cmp[k])
@@ -346,7 +367,7 @@ def run_e2e(hs, cfg, rc, dev, args):
     ms = a.elapsed_time(b) / args.steps
     return {"value": round(R / (ms * 1e-3), 1), "unit": "query-rows/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "chunks_per_step": n_ch, "cuda_graph": True,
+            "chunks_per_step": n_ch, "compute_streams": n_cmp, "cuda_graph": True,
             "l2": "not flushed between steps: the KV cache (304 MB) is larger than L2, "
                   "and each step copies 36.7 MB through it"}
 
@@ -783,7 +804,9 @@ def main():
     ap.add_argument("--skip-swap", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.0)
-    ap.add_argument("--e2e-chunks", type=int, default=2,
+    ap.add_argument("--e2e-streams", type=int, default=2,
+                    help="compute streams the end-to-end step's chunks take in turn")
+    ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="row chunks per end-to-end step (copies overlap compute)")
     ap.add_argument("--swap-only", action="store_true",
                     help="run only the host-backed swap-in section and print its JSON")
