@@ -67,6 +67,16 @@ def _attn_bytes(valid_counts: np.ndarray, H: int, K: int) -> int:
     return int(valid_counts.sum()) * ROW_BYTES + R * H * (576 * 2 + 512 * 2) + R * K * 4
 
 
+def _union_rows(req: np.ndarray, clen: np.ndarray, topk: np.ndarray) -> int:
+    """Distinct valid positions per request, summed over requests."""
+    n = 0
+    for b in np.unique(req):
+        rows = req == b
+        t = topk[rows]
+        n += len(np.unique(t[(t >= 0) & (t < clen[rows][:, None])]))
+    return n
+
+
 class Clocks:
     """nvidia-smi samples (written to a file every 100 ms) while active."""
 
@@ -234,6 +244,13 @@ def run_ours(args):
                 "attn_ms": round(t_attn * 1e3, 4),
                 "tensor_floor_ms": round(R * H * K * 2 * (576 + 512) / (peaks["bf16_tflops"] * 1e12)
                                          * 1e3, 4)}
+    # secondary figure: the distinct rows each request's rows select (the
+    # least the gather can move when a request's rows share their reads)
+    uni = _union_rows(rc["req"].cpu().numpy(), rc["clen"].cpu().numpy(), rc["topk"].cpu().numpy())
+    u_bytes = uni * ROW_BYTES + R * H * (576 * 2 + 512 * 2) + R * K * 4
+    roofline["union"] = {"rows_per_request": round(uni / cfg.B, 1), "bytes": u_bytes,
+                         "achieved": round(u_bytes / t_attn / 1e9, 1),
+                         "frac": round(u_bytes / t_attn / 1e9 / peaks["hbm_gbs"], 4)}
 
     e2e = run_e2e(hs, cfg, rc, dev, args)
     swap = run_swap_bench(hs, dev, args) if (rank == 0 and not args.skip_swap) else None
@@ -372,6 +389,16 @@ def run_e2e(hs, cfg, rc, dev, args):
                   "and each step copies 36.7 MB through it"}
 
 
+def _attn_roofline(valid_per_step, ms_per_step, R, H, K):
+    """The attention's algorithmic bytes per step (every selected entry valid
+    here) over its CUDA-event time, against the measured HBM peak."""
+    byt = [v * ROW_BYTES + R * H * (576 * 2 + 512 * 2) + R * K * 4 for v in valid_per_step]
+    gbs = sum(byt) / (sum(ms_per_step) * 1e-3) / 1e9
+    peak = _peaks()[0]["hbm_gbs"]
+    return {"bytes_per_step": int(statistics.mean(byt)), "achieved": round(gbs, 1),
+            "peak": peak, "frac": round(gbs / peak, 4)}
+
+
 def _lead(stream=None, cycles=1 << 18):
     """A short GPU sleep on the timing stream right before a timed region, so
     that the host has queued the timed calls before the first event fires
@@ -474,6 +501,7 @@ def run_swap_bench(hs, dev, args):
     del hb, f_hot, f_pool
     backup = run_backup_bench(hs, dev)
     verify = run_verify_bench(hs, dev, _peaks()[0]["hbm_gbs"])
+    tiny = run_tiny_bench(hs, dev)
     overlap = run_overlap_bench(hs, dev)
     link = measure_link(hs, dev)
     steady = range(1, cfg.steps)
@@ -488,6 +516,9 @@ def run_swap_bench(hs, dev, args):
             "misses_per_step": miss, "swap_ms_per_step": [round(x, 4) for x in swap_ms],
             "cold_step_gbs": round(miss[0] * ROW_BYTES / (swap_ms[0] * 1e-3) / 1e9, 2),
             "attn_ms_per_step_mean": round(statistics.mean(attn_ms[1:]), 4),
+            "attn_roofline": _attn_roofline(
+                [int((topks[s] >= 0).sum().item()) for s in steady], [attn_ms[s] for s in steady],
+                cfg.R, cfg.H, cfg.K),
             "query_rows_per_s_attention": round(cfg.R / (statistics.mean(attn_ms[1:]) * 1e-3), 1),
             "follower_apply": {
                 "layers": n_follow,
@@ -495,8 +526,66 @@ def run_swap_bench(hs, dev, args):
                 "frac_of_link": round(n_follow * bytes_ss / (sum(apply_ms[s] for s in steady) * 1e-3)
                                       / 1e9 / link["peak_gbs"], 4),
                 "ms_per_step": [round(x, 4) for x in apply_ms]},
-            "backup": backup, "verify": verify, "overlap_workload4": overlap,
+            "backup": backup, "verify": verify, "overlap_workload4": overlap, "tiny_workload1": tiny,
             "status": st, "gpu_launches_per_step": 2}
+
+
+def run_tiny_bench(hs, dev, reps=4):
+    """Workload 1 (2 requests, 16 heads, top-k 64, 128 hot slots): a decode
+    step = four waves of hs_swap_in + hs_sparse_attn_decode (one row of every
+    request per wave) and hs_verify_finalize, timed per step with CUDA events.
+    Latency bound at this size: reported, not graded against a roofline."""
+    cfg = W.get_config(1)
+    req, ri = W.rows_of(cfg)
+    logits, drafts, _ = W.planted_logits(cfg)
+    d_logits, d_drafts = logits.to(dev), torch.as_tensor(drafts, device=dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ms, st = [], 0
+    for _ in range(reps):
+        hb = W.host_backed_case(cfg, device=dev, extra_positions=cfg.steps * (cfg.d + 1))
+        buf = hs.HsBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hb["hot"],
+                          hb["pool"], hb["hbt"])
+        L = list(cfg.L)
+        for step in range(cfg.steps):
+            skv = W.step_kv(cfg, step, device=dev)
+            for r in range(cfg.B):     # the step's own KV, written by the model
+                lo = r * hb["S_tot"] + cfg.S
+                hb["hot"][lo:lo + cfg.d + 1] = skv[r]
+            topk = W.topk_independent(cfg, step, L, req, ri)
+            clen = W.causal_lengths(L, req, ri)
+            q = W.step_q(cfg, step, device=dev)
+            waves = []
+            for w in range(cfg.d + 1):
+                rows = np.where(ri == w)[0]
+                waves.append((torch.as_tensor(req[rows], device=dev),
+                              torch.as_tensor(clen[rows], device=dev),
+                              torch.as_tensor(topk[rows], device=dev),
+                              q[torch.as_tensor(rows, device=dev)].contiguous(),
+                              torch.empty((len(rows), cfg.K), dtype=torch.int32, device=dev),
+                              torch.empty((len(rows), cfg.H, 512), dtype=torch.bfloat16,
+                                          device=dev)))
+            acc = torch.empty(cfg.B, dtype=torch.int32, device=dev)
+            nxt = torch.empty_like(acc)
+            torch.cuda.synchronize()
+            _lead()
+            a.record()
+            for t_req, t_clen, t_topk, qq, idx, out in waves:
+                hs.hs_swap_in(buf, t_req, t_clen, hb["kv_len"], t_topk, idx)
+                hs.hs_sparse_attn_decode(qq, hb["hot"], idx, cfg.scale, out)
+            hs.hs_verify_finalize(buf, d_logits, d_drafts, skv, hb["kv_len"], acc, nxt)
+            b.record()
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+            L = [int(x) for x in hb["kv_len"].cpu().tolist()]
+        st |= hs.hs_get_status(buf)
+        buf.close()
+        del hb
+    steady = ms[1:]
+    return {"workload": cfg.name, "ms_per_step": [round(x, 4) for x in ms],
+            "steady_ms": round(statistics.mean(steady), 4),
+            "query_rows_per_s": round(cfg.R / (statistics.mean(steady) * 1e-3), 1),
+            "launches_per_step": 2 * (cfg.d + 1) + 1, "status": st,
+            "note": "latency bound (16 heads, top-k 64): reported, not graded"}
 
 
 def run_verify_bench(hs, dev, peak_hbm):
@@ -585,8 +674,11 @@ def run_overlap_bench(hs, dev, steps=8):
     e_done = torch.cuda.Event()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
+    e_mid = torch.cuda.Event(enable_timing=True)
+
     def serial(buf, st):
         hs.hs_swap_in(buf, t_req, t_clen, hb["kv_len"], topks[st], idx_s, stream=s1)
+        e_mid.record(s1)
         hs.hs_sparse_attn_decode(q, hb["hot"], idx_s, cfg.scale, out_s, stream=s1)
 
     def overlapped(buf, st):
@@ -600,7 +692,7 @@ def run_overlap_bench(hs, dev, steps=8):
         e_done.record(s2)
         s1.wait_event(e_done)
 
-    res = {}
+    res, attn_serial = {}, []
     variants = [("serial", serial, hb["hot"], 0)] + \
         [(f"overlapped_copy_sms_{n}" if n else "overlapped", overlapped, hot2, n) for n in (0, 24)]
     for name, fn, hot, n_sms in variants:
@@ -615,6 +707,8 @@ def run_overlap_bench(hs, dev, steps=8):
             b.record(s1)
             b.synchronize()
             ms.append(a.elapsed_time(b))
+            if fn is serial:
+                attn_serial.append(e_mid.elapsed_time(b))
         res[name] = {"ms_per_step": [round(x, 4) for x in ms],
                      "steady_ms": round(statistics.mean(ms[1:]), 4),
                      "status": hs.hs_get_status(buf)}
@@ -622,6 +716,9 @@ def run_overlap_bench(hs, dev, steps=8):
         torch.cuda.synchronize()
         if fn is overlapped and not torch.equal(out_s.view(torch.int16), out_o.view(torch.int16)):
             raise RuntimeError("overlapped decode step differs from the serial one")
+    res["serial"]["attn_roofline"] = _attn_roofline(
+        [int((topks[st] >= 0).sum().item()) for st in range(1, steps)], attn_serial[1:], cfg.R, cfg.H,
+        cfg.K)
     del hb, hot2
     ser = res["serial"]["steady_ms"]
     best = min((k for k in res if k != "serial"), key=lambda k: res[k]["steady_ms"])
