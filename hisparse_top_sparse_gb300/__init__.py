@@ -36,7 +36,7 @@ VALUE_DIM = 512
 EXPORTS = (
     "hs_buffer_create", "hs_buffer_destroy", "hs_request_reset", "hs_get_status",
     "hs_buffer_dump", "hs_buffer_clock", "hs_last_error_string", "hs_resolve_topk",
-    "hs_swap_in", "hs_sparse_attn_decode", "hs_verify_finalize", "hs_read_probe",
+    "hs_swap_in", "hs_sparse_attn_decode", "hs_verify_finalize", "hs_read_probe", "hs_wait_probe",
     "hs_verify_accept_noalloc", "hs_swap_apply_plan", "hs_backup_pages", "hs_reclaim_resident",
     "hs_sparse_attn_decode_mixed", "hs_backup_rows", "hs_backup_indexer",
     "hs_buffer_set_copy_sms",
@@ -92,6 +92,7 @@ def lib() -> ctypes.CDLL:
             "hs_reclaim_resident": (_I, [_P, _I, _I, _P, _I, _P, _P, _P, _P]),
             "hs_verify_finalize": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
             "hs_read_probe": (_I, [_P, ctypes.c_size_t, _P, _I, _P]),
+            "hs_wait_probe": (_I, [_P, _I64, _P]),
             "hs_verify_accept_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
             "hs_swap_apply_plan": (_I, [_P, _I, _P, _P, _I64, _I, _P]),
             "hs_backup_rows": (_I, [_I, _P, _P, _P, _P, _I, _I, _I64, _I64, _P, _P]),
@@ -346,6 +347,12 @@ def hs_read_probe(src: torch.Tensor, sink: torch.Tensor, blocks: int, stream=Non
     _check(lib().hs_read_probe(src.data_ptr(), nbytes,
                                _ptr(sink, "sink", torch.int64, (blocks,)), blocks,
                                _stream(stream)), "hs_read_probe")
+
+def hs_wait_probe(status: torch.Tensor, max_cycles: int, stream=None) -> None:
+    """One bounded device wait that runs out; sets HS_STATUS_TIMEOUT in status."""
+    _check(lib().hs_wait_probe(_ptr(status, "status", torch.int32, (1,)), int(max_cycles),
+                               _stream(stream)), "hs_wait_probe")
+
 
 def _ptr_array(tensors, name, dtype, device):
     """A ctypes array of the tensors' data pointers (checked like _ptr)."""

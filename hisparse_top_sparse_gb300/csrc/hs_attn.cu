@@ -188,8 +188,8 @@ __device__ __forceinline__ void bar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
 // Bounded wait for the phase of the given parity: gives up (false) after
-// about 2^31 SM cycles (~1 s) or WAIT_LIMIT polls, whichever comes first.
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+// max_cycles SM cycles or WAIT_LIMIT polls, whichever comes first.
+__device__ __forceinline__ bool bar_wait_n(uint32_t bar, uint32_t parity, long long max_cycles) {
   const long long t0 = clock64();
   for (int i = 0; i < WAIT_LIMIT; ++i) {
     uint32_t ok;
@@ -200,9 +200,13 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
         : "r"(bar), "r"(parity)
         : "memory");
     if (ok) return true;
-    if (clock64() - t0 > (1ll << 31)) break;
+    if (clock64() - t0 > max_cycles) break;
   }
   return false;
+}
+// the kernel's waits: about 2^31 SM cycles (~1 s)
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  return bar_wait_n(bar, parity, 1ll << 31);
 }
 
 // The same wait taken by a whole warp, with one verdict for every lane (the
@@ -759,6 +763,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 }  // namespace
+
+// A wait that runs out: one warp takes the kernel's bounded wait, cut to
+// max_cycles, on an mbarrier phase that nothing completes, and reports
+// HS_STATUS_TIMEOUT the way k_attn_pair does.
+__global__ void k_wait_probe(uint32_t *status, long long max_cycles) {
+  __shared__ uint64_t probe_bar;
+  const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&probe_bar);
+  if (threadIdx.x == 0) bar_init(bar, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  __syncwarp();
+  const bool ok = __all_sync(0xffffffffu, bar_wait_n(bar, 0, max_cycles));
+  if (!ok && threadIdx.x == 0) atomicOr(status, HS_STATUS_TIMEOUT);
+}
+
+extern "C" int hs_wait_probe(uint32_t *status, int64_t max_cycles, hs_stream_t stream) {
+  if (!status) return hs_set_error(HS_ERR_INVALID_ARG, "NULL status");
+  if (max_cycles < 1 || max_cycles > (1ll << 31))
+    return hs_set_error(HS_ERR_INVALID_ARG, "max_cycles %lld not in 1..2^31", (long long)max_cycles);
+  k_wait_probe<<<1, 32, 0, stream>>>(status, (long long)max_cycles);
+  HS_LAUNCH_CHECK("k_wait_probe");
+  return HS_OK;
+}
 
 extern "C" int hs_sparse_attn_decode_mixed(const void *q, const void *kv_resident,
                                            int64_t n_resident, const void *kv_hot, int64_t n_hot,

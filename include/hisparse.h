@@ -486,6 +486,15 @@ int hs_verify_accept_noalloc(const void *logits, int32_t logits_dtype, int32_t B
 int hs_read_probe(const void *src, size_t bytes, uint64_t *sink, int32_t blocks,
                   hs_stream_t stream);
 
+/* Failure-detection check: one warp runs the attention kernel's bounded
+ * mbarrier wait, cut to max_cycles SM cycles (1..2^31), on a phase that
+ * nothing completes; when it gives up, HS_STATUS_TIMEOUT is OR-ed into the
+ * device uint32 *status, exactly as a wait of hs_sparse_attn_decode that ran
+ * out would. Shows that a wait which gives up ends the kernel and leaves the
+ * context usable. Returns HS_ERR_INVALID_ARG for a NULL status or a limit
+ * out of range. */
+int hs_wait_probe(uint32_t *status, int64_t max_cycles, hs_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

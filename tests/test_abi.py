@@ -59,3 +59,8 @@ def test_argument_errors_return_without_a_gpu():
     assert b"token_stride" in L.hs_last_error_string()
     assert L.hs_backup_indexer(1, None, None, None, None, None, 4, 0, 4, 16, 10, 10, None,
                                None) == hs.HS_ERR_INVALID_ARG
+    # the bounded-wait check: a NULL status word or a limit out of range
+    assert L.hs_wait_probe(None, 1000, None) == hs.HS_ERR_INVALID_ARG
+    assert L.hs_wait_probe(ctypes.c_void_p(16), 0, None) == hs.HS_ERR_INVALID_ARG
+    assert L.hs_wait_probe(ctypes.c_void_p(16), (1 << 31) + 1, None) == hs.HS_ERR_INVALID_ARG
+    assert b"max_cycles" in L.hs_last_error_string()
