@@ -242,6 +242,9 @@ __global__ void __launch_bounds__(256) k_resolve_topk(
     const int32_t *__restrict__ bt, int32_t bt_stride, const int32_t *__restrict__ topk,
     int32_t K, int32_t bs, int32_t stride, int32_t *__restrict__ out,
     int32_t *__restrict__ out_valid, uint32_t *status) {
+  // the attention launched after this kernel may begin its prologue now; it
+  // reads this kernel's output only after this kernel has finished
+  asm volatile("griddepcontrol.launch_dependents;\n");
   const int r = blockIdx.x;
   const int32_t b = req_id[r];
   const int32_t n = clen[r];

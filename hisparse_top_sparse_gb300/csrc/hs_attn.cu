@@ -354,15 +354,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int T = (K + NK - 1) / NK;
   const int n_own = T > c ? (T - c + 1) / 2 : 0;
   const int32_t *idx_row = idx + (int64_t)r * K;
-  // the row's cache: the paged resident cache while its request is fully
-  // resident, else the hot buffer its swap-in indices address
-  // (a request id outside [0, n_reqs) leaves the row without a valid entry)
-  const int32_t req = fully_resident ? (row_req ? __ldg(row_req + r) : r) : 0;
-  const bool req_ok = !fully_resident || (req >= 0 && req < n_reqs);
-  const bool hot = req_ok && fully_resident && __ldg(fully_resident + req) == 0;
-  const char *kv = hot ? kv_hot : kv_res;
-  const int64_t n_kv = !req_ok ? 0 : hot ? n_hot : n_res;
-  if (!req_ok && status && tid == 0 && c == 0) atomicOr(status, HS_STATUS_INDEX);
 
   if (tid == 0) {
     for (int s = 0; s < RA_SLOTS; ++s) {
@@ -444,6 +435,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   fence_before();
   __syncthreads();         // Q is in place; the staging area is free for KV tiles
   fence_after();
+
+  // Up to here the kernel has read only q. It is launched as a programmatic
+  // dependent of the kernel before it (hs_resolve_topk lets it start at once),
+  // so that its prologue overlaps that kernel: the indices and the request
+  // flags are read only after that kernel has finished.
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  // the row's cache: the paged resident cache while its request is fully
+  // resident, else the hot buffer its swap-in indices address
+  // (a request id outside [0, n_reqs) leaves the row without a valid entry)
+  const int32_t req = fully_resident ? (row_req ? __ldg(row_req + r) : r) : 0;
+  const bool req_ok = !fully_resident || (req >= 0 && req < n_reqs);
+  const bool hot = req_ok && fully_resident && __ldg(fully_resident + req) == 0;
+  const char *kv = hot ? kv_hot : kv_res;
+  const int64_t n_kv = !req_ok ? 0 : hot ? n_hot : n_res;
+  if (!req_ok && status && tid == 0 && c == 0) atomicOr(status, HS_STATUS_INDEX);
 
 
   if (warp >= 4 && warp < 8) {
@@ -836,11 +842,23 @@ extern "C" int hs_sparse_attn_decode_mixed(const void *q, const void *kv_residen
                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (er != CUDA_SUCCESS) return hs_set_error(HS_ERR_CUDA, "tensor map of q failed (%d)", (int)er);
-  k_attn_pair<<<(unsigned)blocks, THREADS, SMEM_ALLOC, stream>>>(
-      tmap, reinterpret_cast<const char *>(q), reinterpret_cast<const char *>(kv_resident),
-      n_resident, reinterpret_cast<const char *>(kv_hot), n_hot, row_req, fully_resident, n_reqs, idx,
-      H, K,
-      scale * 1.4426950408889634f, reinterpret_cast<__nv_bfloat16 *>(out), lse, status);
+  // a programmatic dependent launch: the prologue (barriers, TMEM, Q) may
+  // run while the previous kernel in the stream finishes
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  HS_CUDA_TRY(cudaLaunchKernelEx(
+      &cfg, k_attn_pair, tmap, reinterpret_cast<const char *>(q),
+      reinterpret_cast<const char *>(kv_resident), n_resident,
+      reinterpret_cast<const char *>(kv_hot), n_hot, row_req, fully_resident, n_reqs, idx, H, K,
+      scale * 1.4426950408889634f, reinterpret_cast<__nv_bfloat16 *>(out), lse, status));
   HS_LAUNCH_CHECK("k_attn_pair");
   return HS_OK;
 }

@@ -245,6 +245,13 @@ int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
  *   status device uint32 or NULL: HS_STATUS_TIMEOUT is OR-ed in if one of
  *          the kernel's bounded internal waits gives up (never expected)
  * Requirements: R >= 0, 1 <= H <= 1024, K >= 0.
+ * Launch: a programmatic dependent launch on `stream`. Its prologue (which
+ * reads only q) may start before the previous kernel in the stream has
+ * finished, if that kernel lets its dependents start early, as
+ * hs_resolve_topk does; idx, kv and the request flags are read only after
+ * the previous kernel has finished. So q must not be written by such an
+ * early-releasing kernel immediately before this call (no call of this
+ * library writes q).
  */
 int hs_sparse_attn_decode(const void *q, const void *kv, int64_t n_kv_rows,
                           const int32_t *idx, int32_t R, int32_t H, int32_t K,
