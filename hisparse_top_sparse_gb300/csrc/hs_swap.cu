@@ -180,6 +180,9 @@ __device__ int collect_rows(const SwapArgs &a, int b, int from, int *rows, int *
 __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
                                                                  int32_t *__restrict__ out,
                                                                  int32_t *__restrict__ out_valid) {
+  // the gather launched after this kernel may take its SMs now; it reads this
+  // kernel's copy lists only after this kernel has finished
+  asm volatile("griddepcontrol.launch_dependents;\n");
   extern __shared__ __align__(16) unsigned char smem[];
   const int b = blockIdx.x;
   const int nS = pow2_ceil(a.S);
@@ -470,6 +473,9 @@ __global__ void __launch_bounds__(256) k_swap_gather(const int32_t *__restrict__
   extern __shared__ int pre[];                     // [max_reqs + 1] chunk offsets
   __shared__ int part[256];
   const int tid = threadIdx.x;
+  // a programmatic dependent launch of k_swap_request: resident early, it
+  // waits here until that kernel has finished and its writes are visible
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int seg = (max_reqs + 255) / 256;
   auto cnt_of = [&](int i) -> int { const int c = copy_cnt[i]; return c > 0 ? c : 0; };
   int sum = 0;
@@ -684,8 +690,19 @@ extern "C" int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
   ta.out = out_slot_idx; ta.out_valid = out_valid; ta.status = buf->status;
   const size_t gsmem = (size_t)(buf->max_reqs + 1) * sizeof(int);
   if (buf->copy_sms > 0 && buf->copy_sms < nsm) nsm = buf->copy_sms;
-  k_swap_gather<<<nsm * 8, 256, gsmem, stream>>>(buf->copy_cnt, buf->copy_desc, buf->max_reqs,
-                                                 buf->S, buf->S_tot, a.pool, a.hot, ta);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(nsm * 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = gsmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_swap_gather, (const int32_t *)buf->copy_cnt,
+                                 (const uint64_t *)buf->copy_desc, (int32_t)buf->max_reqs,
+                                 (int32_t)buf->S, (int32_t)buf->S_tot, a.pool, a.hot, ta));
   HS_LAUNCH_CHECK("k_swap_gather");
   return HS_OK;
 }
