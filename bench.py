@@ -137,8 +137,15 @@ class Clocks:
 
 
 def _source_sha() -> str:
+    """sha256 prefix of the attention source without its // comments and
+    blank lines (a comment edit does not invalidate the counters)."""
     p = os.path.join(ROOT, "hisparse_top_sparse_gb300", "csrc", "hs_attn.cu")
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    code = []
+    for line in open(p, encoding="utf-8"):
+        line = line.split("//", 1)[0].rstrip()
+        if line:
+            code.append(line)
+    return hashlib.sha256("\n".join(code).encode()).hexdigest()[:16]
 
 
 def _traffic():

@@ -40,6 +40,9 @@
 // Warp roles (352 threads): warps 0-3 softmax, P exchange and epilogue (thread
 // = head = TMEM lane), warps 4-7 gather producers, warps 8-9 issue Q K^T for
 // own tiles into S buffers 0 / 1, warp 10 issues P V for every tile in order.
+// The kernel is a programmatic dependent launch: its prologue (barriers, TMEM,
+// Q) overlaps the previous kernel (hs_resolve_topk releases it at entry), and
+// it reads the indices and request flags after griddepcontrol.wait.
 // Every mbarrier wait is bounded; a wait that gives up sets HS_STATUS_TIMEOUT
 // in the caller's status word and the CTA winds down.
 

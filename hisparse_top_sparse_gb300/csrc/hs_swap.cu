@@ -9,19 +9,25 @@
 //
 // Two launches. k_swap_request: one 1024-thread block per request that has
 // rows in the call works through that request alone:
-//   probe   every entry of the request's rows: classify it, claim each needed
-//           committed position once per call (a shared-memory bitmap of the
-//           request's positions, or epoch-stamped marks when it does not fit),
-//           record hit slots in a shared-memory bitmap, compact misses with
-//           __ballot_sync / __popc into a shared-memory list
+//   probe   every entry of the request's rows: classify it and look up its
+//           position's slot; a hit marks the slot in a shared-memory bitmap
+//           (distinct hits = marked slots), a miss claims its position once
+//           per call (a shared-memory bitmap of the request's positions, or
+//           epoch-stamped marks when it does not fit) and the first claims
+//           are compacted with __ballot_sync / __popc into a shared-memory
+//           list (one shared atomic per warp and round)
 //   assign  capacity check; the victims are the first slots of the request's
 //           LRU order (a persistent array kept in ascending (ts, slot) order)
-//           that hold no needed position (one block prefix scan); the misses,
-//           in ascending position order (their ranks in a bitmap of miss
-//           positions), take them in order; hits and victims take the current
-//           time and move to the end of the order in slot order (two prefix
-//           scans) -- no sort over all S slots
+//           that hold no needed position; the misses, in ascending position
+//           order (their ranks in a bitmap of miss positions), take them in
+//           order; hits and victims take the current time and move to the end
+//           of the order in slot order. Victims and the new order come from
+//           warp ballots over the order with one scan of the 32 warp counts
+//           -- no sort over all S slots
 //   publish (host pool row, hot slot) of every miss
+// k_swap_gather is a programmatic dependent launch of k_swap_request: its
+// blocks take the SMs the metadata kernel leaves free and wait
+// (griddepcontrol.wait) until its copy lists are complete.
 // k_swap_gather: every SM copies a share of every request's missed 1152-byte
 // rows from the device-mapped page-locked host pool with 16-byte loads (four
 // in flight per thread): reads over the host link need requests in flight
