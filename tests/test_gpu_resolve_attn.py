@@ -190,3 +190,41 @@ def test_workload2_full_size():
         e_idx, cfg.scale, rows)
     check_attn(out, np.stack([outs[r] for r in rows]), lse, np.stack([lses[r] for r in rows]),
                rows=rows)
+
+
+def test_resolve_then_attention_back_to_back_sees_fresh_indices():
+    """The attention is a programmatic dependent launch of the resolve before
+    it: over several steps, each with new top-k positions written on the
+    device and no host synchronisation between resolve and attention, every
+    attention must use its own step's indices (a stale read would match an
+    earlier step, not this one)."""
+    hs = lib()
+    g = np.random.default_rng(11)
+    B, L, bs, H, K = 4, 900, 64, 128, 300
+    R = B
+    nblk = (L + bs) // bs + 1
+    bt = g.permutation(B * nblk).reshape(B, nblk).astype(np.int32)
+    kv = (torch.randn((B * nblk * bs, 576), generator=torch.Generator().manual_seed(3)) / 4).to(
+        torch.bfloat16).to(DEV)
+    q = (torch.randn((R, H, 576), generator=torch.Generator().manual_seed(4)) / 4).to(
+        torch.bfloat16).to(DEV)
+    req = np.arange(B, dtype=np.int32)
+    clen = np.full(B, L, np.int32)
+    d_req, d_clen, d_bt = (torch.as_tensor(x, device=DEV) for x in (req, clen, bt))
+    steps = 6
+    topks = [np.stack([g.permutation(L)[:K] for _ in range(R)]).astype(np.int32)
+             for _ in range(steps)]
+    d_topk = torch.empty((R, K), dtype=torch.int32, device=DEV)
+    idx = torch.empty_like(d_topk)
+    outs = [torch.empty((R, H, 512), dtype=torch.bfloat16, device=DEV) for _ in range(steps)]
+    host_topk = [torch.as_tensor(t).pin_memory() for t in topks]
+    for s in range(steps):
+        d_topk.copy_(host_topk[s], non_blocking=True)
+        hs.hs_resolve_topk(d_req, d_clen, d_bt, d_topk, bs, bs, idx)
+        hs.hs_sparse_attn_decode(q, kv, idx, 0.05, outs[s])
+    torch.cuda.synchronize()
+    kv_np = kv.cpu()
+    for s in range(steps):
+        e_idx, _, _ = O.resolve_topk(req, clen, bt, topks[s], bs, bs)
+        ref, _ = O.sparse_attn_decode(q.cpu(), kv_np, e_idx, 0.05)
+        check_attn(outs[s], ref)
