@@ -28,7 +28,7 @@ section of the page):
   ``HiSparseCacheHandle.resolve_topk`` (fully-resident index conversion versus
   swap-in) and "数据 back up" (paged host row = block * block_size + offset).
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 R1  Row ``i`` of request ``b`` is the query at position ``L_b + i``; its causal
     length is ``L_b + i + 1``. ``L_b`` is the committed KV length.
