@@ -7,15 +7,16 @@
 // allocation can cause. Such a caller can still hand over its own logits,
 // drafts and output arrays, but cannot create an hs_buffer (that allocates).
 //
-// The per-row argmax needs scratch (one int32 per verified row). Here it lives
-// in a file-scope __device__ array of fixed size, which every GPU that loads
-// this library holds until the process exits. No call below allocates.
+// The one launch needs scratch: one int32 per verified row (its argmax) and
+// one per request (its rows done so far). Both live in file-scope __device__
+// arrays of fixed size, which every GPU that loads this library holds until
+// the process exits. No call below allocates.
 
 #include <mutex>
 
 #include "hs_internal.cuh"
 
-#define HS_NOALLOC_MAX_ROWS 65536   // B * (d + 1) limit: 256 KiB of int32 scratch
+#define HS_NOALLOC_MAX_ROWS 65536   // B * (d + 1) limit: two int32 arrays, 512 KiB
 #define HS_NOALLOC_MAX_DEVICES 64
 
 static __device__ __align__(256) int32_t g_accept_scratch[HS_NOALLOC_MAX_ROWS];
