@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(BR_THREADS) k_backup_rows_narrow(
 // word by word. A backup of whole blocks (consecutive host rows) is thus
 // written in whole lines over the host link; scattered rows are runs of one.
 constexpr int RUN_EPL = 4;
-constexpr int RUN_WARPS = 8;
+constexpr int RUN_WARPS = 4;
 
 __global__ void __launch_bounds__(RUN_WARPS * 32) k_backup_runs(
     const __grid_constant__ RowLayers rl, int32_t n_layers, const int32_t *__restrict__ src_slots,
