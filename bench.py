@@ -67,6 +67,55 @@ def _attn_bytes(valid_counts: np.ndarray, H: int, K: int) -> int:
     return int(valid_counts.sum()) * ROW_BYTES + R * H * (576 * 2 + 512 * 2) + R * K * 4
 
 
+def run_mixed_and_reclaim(hs, cfg, rc, idx, flush, stream, reps=10):
+    """Next row 3 on workload 2: the attention over a batch that mixes both
+    kinds of request (every other request reads a second copy of the cache,
+    as a host-backed request reads its hot buffer), against the same rows in
+    a plain call; then hs_reclaim_resident releasing pages from the
+    workload's block table (not a step operation: it runs when allocation
+    fails). L2 flushed before each timed call."""
+    R, H = cfg.R, cfg.H
+    out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=rc["q"].device)
+    kv_hot = rc["kv"].clone()
+    flags = torch.as_tensor((np.arange(cfg.B) % 2).astype(np.int32), device=rc["q"].device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        ts = []
+        for _ in range(reps + 2):
+            flush.fill_(1)
+            _lead(stream)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts[2:])
+
+    plain = timed(lambda: hs.hs_sparse_attn_decode(rc["q"], rc["kv"], idx, cfg.scale, out))
+    mixed = timed(lambda: hs.hs_sparse_attn_decode_mixed(rc["q"], rc["kv"], kv_hot, rc["req"],
+                                                         flags, idx, cfg.scale, out))
+    del kv_hot
+    bt = rc["bt"].clone()
+    nblk = torch.full((cfg.B,), bt.shape[1], dtype=torch.int32, device=bt.device)
+    need = 512
+    freed = torch.empty(need, dtype=torch.int32, device=bt.device)
+    n_freed = torch.empty(1, dtype=torch.int32, device=bt.device)
+    ts = []
+    for _ in range(reps):
+        bt.copy_(rc["bt"])
+        _lead(stream)
+        a.record(stream)
+        hs.hs_reclaim_resident(bt, nblk, need, freed, None, n_freed)
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return {"attention_plain_ms": round(plain, 4), "attention_mixed_ms": round(mixed, 4),
+            "mixed": "every other request reads a second copy of the cache through its flag",
+            "reclaim_ms": round(statistics.median(ts), 4), "reclaim_need": need,
+            "reclaim_table": f"{cfg.B} x {bt.shape[1]}", "reclaim_freed": int(n_freed.item())}
+
+
 def _union_rows(req: np.ndarray, clen: np.ndarray, topk: np.ndarray) -> int:
     """Distinct valid positions per request, summed over requests."""
     n = 0
@@ -269,6 +318,7 @@ def run_ours(args):
                          "achieved": round(u_bytes / t_attn / 1e9, 1),
                          "frac": round(u_bytes / t_attn / 1e9 / peaks["hbm_gbs"], 4)}
 
+    next3 = run_mixed_and_reclaim(hs, cfg, rc, idx, flush, stream) if rank == 0 else None
     e2e = run_e2e(hs, cfg, rc, dev, args)
     swap = run_swap_bench(hs, dev, args) if (rank == 0 and not args.skip_swap) else None
     cpu = cpu_baseline(cfg, rc) if (rank == 0 and ws == 1 and not args.skip_cpu) else None
@@ -290,6 +340,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{ws}, requests sharded, no collective"},
             "gpu_launches": 2 * args.steps,
             "roofline": roofline, "e2e": e2e, "clocks": clk.summary(),
+            "mixed_batch_and_reclaim": next3,
             "swap_in": swap, "cpu_baseline": cpu,
         }
         print(json.dumps(line))
