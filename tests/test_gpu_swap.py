@@ -181,3 +181,23 @@ def test_workload3_sampled_requests():
 
 def test_workload4_sampled_requests():
     _run_locality(4, sample=[5, 127], steps=3)
+
+
+def test_largest_slot_count_and_long_context():
+    """S = 8192 (the largest slot count) and a 300,000-position context, past
+    the bitmap limit of 262,144 positions, so claims go through epoch marks
+    and the misses through the bitonic sort. Five calls of 3000 positions
+    shared by both rows, half of them reused, fill the buffer and evict;
+    every piece of state matches the oracle after each call."""
+    g = np.random.default_rng(21)
+    S, max_ctx, L = 8192, 300_000, 290_000
+    p = Pair(1, S, 2, max_ctx, 64, 21)
+    req = np.zeros(2, np.int32)
+    clen = np.array([L + 1, L + 2], np.int32)
+    cur = g.choice(L, 3000, replace=False)
+    for call in range(5):
+        topk = np.stack([g.permutation(cur), g.permutation(cur)]).astype(np.int32)
+        p.call(req, clen, [L], topk)
+        p.compare_state()
+        fresh = np.setdiff1d(g.choice(L, 3000, replace=False), cur)[:1500]
+        cur = np.concatenate([g.permutation(cur)[:3000 - len(fresh)], fresh])
