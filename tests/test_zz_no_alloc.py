@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import workloads as W
+from oracle import hs_oracle as O
 from gpu_util import lib, np_
 
 pytestmark = pytest.mark.gpu
@@ -59,3 +60,28 @@ def test_noalloc_rejects_sizes_beyond_the_static_scratch():
     acc = torch.empty(20000, dtype=torch.int32, device=DEV)
     with pytest.raises(hs.HisparseError, match="static scratch"):
         hs.hs_verify_accept_noalloc(logits, drafts, acc, acc.clone())
+
+
+def test_noalloc_at_the_static_scratch_limit():
+    """B * (d + 1) = 65536 rows, the most the static scratch takes, twice (the
+    per-request row counts must be back at 0 after the first call); ties
+    are frequent (integer logits) and half the drafts are planted as the
+    argmax; every request against the oracle's argmax and acceptance."""
+    hs = lib()
+    B, d, V = 16384, 3, 64
+    g = np.random.default_rng(77)
+    for call in range(2):
+        lg = g.integers(-4, 5, size=(B, d + 1, V)).astype(np.float32)
+        drafts = g.integers(0, V, size=(B, d)).astype(np.int32)
+        plant = g.random((B, d)) < 0.5
+        for b, i in zip(*np.nonzero(plant)):
+            drafts[b, i] = int(np.argmax(lg[b, i]))
+        acc = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+        nxt = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+        hs.hs_verify_accept_noalloc(torch.as_tensor(lg, device=DEV),
+                                    torch.as_tensor(drafts, device=DEV), acc, nxt)
+        torch.cuda.synchronize()
+        want = [O.greedy_accept([O.argmax_lowest(lg[b, i]) for i in range(d + 1)], drafts[b])
+                for b in range(B)]
+        assert np_(acc).tolist() == [m for m, _ in want]
+        assert np_(nxt).tolist() == [t for _, t in want]
