@@ -174,3 +174,54 @@ def test_workload5_verify_finalize():
         assert stok[b].tolist() == ref.slot_token[b]
         assert sts[b].tolist() == ref.slot_ts[b]
     assert np.array_equal(_u16(hb["pool"]), ref.host_pool)
+
+
+def test_longest_draft_chain_commits_and_evicts():
+    """d = 15 drafts (16 step slots, the most a buffer takes), drafts planted
+    as the argmax with probability 0.9 so that some requests accept all 15
+    and commit 16 rows, 40 LRU slots so that commits evict: two verify steps
+    after a warm swap-in, every piece of state against the oracle."""
+    hs = lib()
+    g = np.random.default_rng(15)
+    B, d, V, S, bs, max_ctx = 6, 15, 300, 40, 16, 512
+    nblk = max_ctx // bs
+    hbt = g.permutation(B * nblk).reshape(B, nblk).astype(np.int32)
+    pool = W.host_pool_tensor(B * nblk * bs, 15, device=DEV)
+    hot = torch.zeros((B * (S + d + 1), 576), dtype=torch.bfloat16, device=DEV)
+    buf = hs.HsBuffer(B, S, d + 1, max_ctx, bs, hot, pool, _t(hbt))
+    ref = O.HotBuffer(B, S, d + 1, max_ctx, bs, hbt, pool.clone())
+    L = [int(x) for x in g.integers(100, 300, size=B)]
+    kv_len = _t(np.asarray(L, np.int32))
+    # warm state: one row per request selecting 30 committed positions
+    req = np.arange(B, dtype=np.int32)
+    clen = np.array([x + 1 for x in L], np.int32)
+    topk = np.stack([g.choice(x, 30, replace=False) for x in L]).astype(np.int32)
+    out = torch.empty((B, 30), dtype=torch.int32, device=DEV)
+    hs.hs_swap_in(buf, _t(req), _t(clen), kv_len, _t(topk), out)
+    e_out, _, _, _ = ref.swap_in(req, clen, L, topk)
+    assert np.array_equal(np_(out), e_out)
+    for step in range(2):
+        lg = g.standard_normal((B, d + 1, V)).astype(np.float32)
+        drafts = g.integers(0, V, size=(B, d)).astype(np.int32)
+        for b in range(B):
+            for i in range(d):
+                if b == 0 or g.random() < 0.9:      # request 0 accepts all 15
+                    drafts[b, i] = int(np.argmax(lg[b, i]))
+        skv = W.bf16_normal((B, d + 1, 576), 1.0, 15 + step, "skv15")
+        acc = torch.empty(B, dtype=torch.int32, device=DEV)
+        nxt = torch.empty_like(acc)
+        hs.hs_verify_finalize(buf, torch.as_tensor(lg, device=DEV), _t(drafts), skv.to(DEV),
+                              kv_len, acc, nxt)
+        e_acc, e_nxt, e_L, e_st = O.verify_finalize(ref, torch.as_tensor(lg), drafts, skv, L)
+        torch.cuda.synchronize()
+        assert np.array_equal(np_(acc), e_acc) and np.array_equal(np_(nxt), e_nxt)
+        assert np.array_equal(np_(kv_len), e_L) and hs.hs_get_status(buf) == e_st == 0
+        assert int(e_acc[0]) == d                   # 16 rows committed, slots evicted
+        L = [int(x) for x in e_L]
+        ts, stok, sts = buf.dump()
+        for b in range(B):
+            assert stok[b].tolist() == ref.slot_token[b]
+            assert sts[b].tolist() == ref.slot_ts[b]
+            assert np.array_equal(ts[b].numpy(), ref.token_slot_array(b))
+        assert np.array_equal(_u16(pool), ref.host_pool)
+    buf.close()
