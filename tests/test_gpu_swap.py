@@ -201,3 +201,20 @@ def test_largest_slot_count_and_long_context():
         p.compare_state()
         fresh = np.setdiff1d(g.choice(L, 3000, replace=False), cur)[:1500]
         cur = np.concatenate([g.permutation(cur)[:3000 - len(fresh)], fresh])
+
+
+def test_most_requests_per_buffer():
+    """max_reqs = 16384, the limit (the gather's prefix over every request
+    sits in shared memory, and the metadata launch has a block per request),
+    with rows of three requests at the start, middle and end of the range."""
+    g = np.random.default_rng(31)
+    B, S, n_step, max_ctx, bs = 16384, 8, 2, 16, 4
+    p = Pair(B, S, n_step, max_ctx, bs, 31)
+    L = [10] * B
+    active = [0, 8191, 16383]
+    for call in range(3):
+        req = np.array([0, 0, 8191, 16383, 16383], np.int32)
+        clen = np.array([L[b] + 1 + (i % 2) for i, b in enumerate(req)], np.int32)
+        topk = np.stack([g.choice(c, 6, replace=False) for c in clen]).astype(np.int32)
+        p.call(req, clen, L, topk)
+        p.compare_state(reqs=active)
