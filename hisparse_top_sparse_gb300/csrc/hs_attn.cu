@@ -21,14 +21,16 @@
 //     operand, dims 384..575 in shared memory (3 x 16 KB, 128-byte swizzle);
 //     S has two 32-column TMEM buffers [448, 512), and the softmax writes P
 //     (bf16 pairs) over the first 16 columns of its buffer;
-//   * P of an own tile goes to the CTA's own P V (read from TMEM) and, by
-//     st.async into the peer's shared memory, to the peer's P V (read from
-//     shared memory); the peer's P V commit arrives back on this CTA's
-//     mbarrier (tcgen05.commit multicast), freeing the slot;
+//   * P of an own tile goes to the CTA's own P V (read from TMEM) and to the
+//     peer's P V (read from shared memory): each softmax warp stages its 32
+//     rows in this CTA's shared memory and sends them with one 2 KB bulk
+//     copy into the peer's; the peer's P V commit arrives back on this CTA's
+//     mbarrier (tcgen05.commit multicast), freeing both slots;
 //   * the KV rows of an own tile are gathered whole (16-byte cp.async, each
 //     producer thread's copies arriving on the tile's mbarrier as they land):
-//     the four 64-dim swizzle blocks of this CTA's value half into ring VO,
-//     the other five into ring A (freed once Q K^T is done); of a peer tile
+//     the four 64-dim swizzle blocks of this CTA's value half into ring VO
+//     (3 slots), the other five into ring A (2 slots, each freed once its
+//     Q K^T is done); of a peer tile
 //     only this CTA's value half is gathered, into ring VP;
 //   * both CTAs use one softmax reference per head: the larger of their first
 //     tiles' maxima, agreed through distributed shared memory before any P is
@@ -64,7 +66,7 @@ constexpr int QT_DIMS = 384;              // Q dims held in TMEM
 constexpr int QS_BLOCKS = (D - QT_DIMS) / 64;   // 3 swizzle blocks of Q in SMEM
 constexpr int NSB = 2;                    // S / P buffers (own tiles)
 constexpr int VB_BLOCKS = 4;              // swizzle blocks of one value half
-constexpr int RA_SLOTS = 3, VO_SLOTS = 3, VP_SLOTS = 3, XP_SLOTS = 2;
+constexpr int RA_SLOTS = 2, VO_SLOTS = 3, VP_SLOTS = 3, XP_SLOTS = 2;
 constexpr int THREADS = 352;
 constexpr int NPROD = 128;
 constexpr float REF_SLACK = 30.0f;        // P <= 2^30 on the shared reference
@@ -73,20 +75,22 @@ constexpr float REF_SLACK = 30.0f;        // P <= 2^30 on the shared reference
 constexpr int KV_BLOCK_BYTES = NK * 128;                    // 4096
 constexpr int QS_OFF = 0;
 constexpr int QS_BYTES = QS_BLOCKS * HG * 128;              // 49152
-constexpr int XP_OFF = QS_OFF + QS_BYTES;                   // peer's P: 128 rows x 128 B,
-constexpr int XP_BYTES = HG * 128;                          // slot s = bytes [64s, 64s + 64)
 constexpr int RA_SLOT_BYTES = (D / 64 - VB_BLOCKS) * KV_BLOCK_BYTES;   // 20480
 constexpr int V_SLOT_BYTES = VB_BLOCKS * KV_BLOCK_BYTES;              // 16384
-constexpr int RA_OFF = XP_OFF + XP_BYTES;
+constexpr int P_SLOT_BYTES = HG * NK * 2;                   // 8192: 128 rows x 64 B, 64-byte swizzle
+constexpr int RA_OFF = QS_OFF + QS_BYTES;
 constexpr int VO_OFF = RA_OFF + RA_SLOTS * RA_SLOT_BYTES;
-constexpr int VP_OFF = VO_OFF + VO_SLOTS * V_SLOT_BYTES;
+constexpr int XS_OFF = VO_OFF + VO_SLOTS * V_SLOT_BYTES;    // own P staged for the bulk copy
+constexpr int XP_OFF = XS_OFF + XP_SLOTS * P_SLOT_BYTES;    // the peer's P
+constexpr int VP_OFF = XP_OFF + XP_SLOTS * P_SLOT_BYTES;
 constexpr int XMAX_OFF = VP_OFF + VP_SLOTS * V_SLOT_BYTES;  // peer's first-tile maxima
 constexpr int XEND_OFF = XMAX_OFF + HG * 4;                 // peer's (l, max, flag) per pass
 constexpr int BAR_OFF = XEND_OFF + 2 * HG * 16;
 constexpr int SMEM_USED = BAR_OFF + 512;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;                // slack for the 1 KB alignment
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-static_assert(RA_OFF % 1024 == 0 && VO_OFF % 1024 == 0 && VP_OFF % 1024 == 0, "slot alignment");
+static_assert(RA_OFF % 1024 == 0 && VO_OFF % 1024 == 0 && VP_OFF % 1024 == 0 &&
+                  XS_OFF % 1024 == 0 && XP_OFF % 1024 == 0, "slot alignment");
 
 // TMEM columns
 constexpr uint32_t COL_O = 0, COL_Q = 256, COL_S = 448;
@@ -133,6 +137,17 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
   // shared-memory matrix descriptor, 128-byte swizzle, descriptor version 1
   return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ uint64_t sdesc64(uint32_t addr) {
+  // the same for K-major rows of 64 bytes, 64-byte swizzle: 8-row groups of
+  // 512 bytes
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(512 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)4 << 61);
+}
+// byte offset of 16-byte chunk j (keys 8j..8j+7) of row `row` in a P slot
+__device__ __forceinline__ uint32_t sw64(uint32_t row, uint32_t j) {
+  return row * 64 + ((j ^ ((row >> 1) & 3)) << 4);
 }
 
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
@@ -306,6 +321,16 @@ __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t
                "r"(v), "r"(rbar)
                : "memory");
 }
+// `bytes` of this CTA's shared memory into the peer's, counted by the peer's
+// mbarrier `rbar` when they land (both addresses 16-byte aligned)
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                             uint32_t rbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          dst),
+      "r"(src), "r"(bytes), "r"(rbar)
+      : "memory");
+}
 // this thread's arrival plus the bytes still to come in the current phase
 __device__ __forceinline__ void arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
@@ -397,9 +422,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // Q by nine tensor copies of 128 heads x 64 dims (16 KB, 128-byte swizzle,
   // rows past H filled with zeros), each issued by one CTA of the pair and
   // multicast to both: dims 384..575 land in SMEM as the MMA's A operand,
-  // dims 0..383 in a staging area in the (still empty) KV rings, from where
+  // dims 0..383 in a staging area over the (still empty) rings A and VO and
+  // the P staging slots, from where
   // each head's thread moves them into TMEM
-  static_assert(6 * HG * 128 <= VP_OFF - RA_OFF, "Q staging fits rings A and VO");
+  static_assert(6 * HG * 128 <= XP_OFF - RA_OFF, "Q staging fits rings A, VO and the P staging");
   fence_before();
   cluster_sync();          // both CTAs' barriers exist before any remote operation
   fence_after();
@@ -593,11 +619,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             }
             if (!ok) break;
             fence_after();
-            fence_proxy_async();   // V by cp.async, P by st.async
+            fence_proxy_async();   // V by cp.async, P by a bulk copy
             const uint32_t vb = sbase + VP_OFF + sp * V_SLOT_BYTES;
 #pragma unroll
             for (int ks = 0; ks < NK / 16; ++ks)
-              mma_ss(tmem + COL_O, sdesc(sbase + XP_OFF + xs * 64 + ks * 32, 16, 1024),
+              mma_ss(tmem + COL_O, sdesc64(sbase + XP_OFF + xs * P_SLOT_BYTES + ks * 32),
                      sdesc(vb + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (t > 0 || ks > 0));
             mma_commit(bar(B_EMPTYVP + sp));
             mma_commit_multicast(bar(B_XPFREE + xs), (uint16_t)(1u << peer));   // the peer may refill
@@ -612,7 +638,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // -------------------------------- softmax + P exchange (warps 0-3) ----
     const int hrow = tid;                          // head row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t peer_xp = peer_addr(sbase + XP_OFF, peer) + (uint32_t)hrow * 128;
+    const uint32_t peer_xp = peer_addr(sbase + XP_OFF, peer) + (uint32_t)warp * 32 * 64;
     float ref = 0.f, l = 0.f, l_peer = 0.f, m_ex = -INFINITY;
     bool flag = false, ref_unset = false, decided = false;
     int ig = 0, last_pass = 0;
@@ -680,18 +706,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) bar_arrive(bar(B_PFULL + sb));
 
-        // the same P to the peer: slot ig % 2 of its P buffer, 128-byte
-        // swizzled K-major rows (the A operand layout of its P V)
+        // the same P to the peer, into slot ig % 2 of its P buffer (64-byte
+        // swizzled K-major rows, the A operand layout of its P V): staged in
+        // this CTA's slot of the same number, then one 2 KB bulk copy per
+        // warp. The peer's P V commit on a slot (XPFREE) means that the copy
+        // out of the staging slot has landed as well.
         const int xs = ig % XP_SLOTS;
         if (ig >= XP_SLOTS && !warp_wait_cluster(bar(B_XPFREE + xs), ((ig / XP_SLOTS) - 1) & 1)) {
           timed_out = true;
           break;
         }
-        const uint32_t rbar = peer_addr(bar(B_XPFULL + xs), peer);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          st_async_v4(peer_xp + ((uint32_t)((xs * 4 + q4) ^ (hrow & 7)) << 4), sr[4 * q4],
-                      sr[4 * q4 + 1], sr[4 * q4 + 2], sr[4 * q4 + 3], rbar);
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4 *>(sm + XS_OFF + xs * P_SLOT_BYTES + sw64(hrow, j)) =
+              make_uint4(sr[4 * j], sr[4 * j + 1], sr[4 * j + 2], sr[4 * j + 3]);
+        fence_proxy_async();     // the bulk copy reads through the async proxy
+        __syncwarp();
+        if (lane == 0)
+          bulk_to_peer(peer_xp + xs * P_SLOT_BYTES,
+                       sbase + XS_OFF + xs * P_SLOT_BYTES + warp * 32 * 64, 32 * 64,
+                       peer_addr(bar(B_XPFULL + xs), peer));
       }
       if (timed_out) break;
       if (pass == 0 && n_own == 0 && !agree_ref(-INFINITY)) { timed_out = true; break; }
