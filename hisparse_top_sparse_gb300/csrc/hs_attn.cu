@@ -25,11 +25,13 @@
 //     peer's P V (read from shared memory): each softmax warp stages its 32
 //     rows in this CTA's shared memory and sends them with one 2 KB bulk
 //     copy into the peer's; the peer's P V commit arrives back on this CTA's
-//     mbarrier (tcgen05.commit multicast), freeing both slots;
+//     mbarrier (tcgen05.commit multicast), freeing both buffers (one
+//     staging and one receiving buffer per CTA: the next own tile's P waits
+//     for the peer's P V of the previous one);
 //   * the KV rows of an own tile are gathered whole (16-byte cp.async, each
 //     producer thread's copies arriving on the tile's mbarrier as they land):
 //     the four 64-dim swizzle blocks of this CTA's value half into ring VO
-//     (3 slots), the other five into ring A (2 slots, each freed once its
+//     (3 slots), the other five into ring A (3 slots, each freed once its
 //     Q K^T is done); of a peer tile
 //     only this CTA's value half is gathered, into ring VP;
 //   * both CTAs use one softmax reference per head: the larger of their first
@@ -66,7 +68,7 @@ constexpr int QT_DIMS = 384;              // Q dims held in TMEM
 constexpr int QS_BLOCKS = (D - QT_DIMS) / 64;   // 3 swizzle blocks of Q in SMEM
 constexpr int NSB = 2;                    // S / P buffers (own tiles)
 constexpr int VB_BLOCKS = 4;              // swizzle blocks of one value half
-constexpr int RA_SLOTS = 2, VO_SLOTS = 3, VP_SLOTS = 3, XP_SLOTS = 2;
+constexpr int RA_SLOTS = 3, VO_SLOTS = 3, VP_SLOTS = 3, XP_SLOTS = 1;
 constexpr int THREADS = 352;
 constexpr int NPROD = 128;
 constexpr float REF_SLACK = 30.0f;        // P <= 2^30 on the shared reference
@@ -706,11 +708,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) bar_arrive(bar(B_PFULL + sb));
 
-        // the same P to the peer, into slot ig % 2 of its P buffer (64-byte
-        // swizzled K-major rows, the A operand layout of its P V): staged in
-        // this CTA's slot of the same number, then one 2 KB bulk copy per
-        // warp. The peer's P V commit on a slot (XPFREE) means that the copy
-        // out of the staging slot has landed as well.
+        // the same P to the peer, into slot ig % XP_SLOTS of its P buffer
+        // (64-byte swizzled K-major rows, the A operand layout of its P V):
+        // staged in this CTA's slot of the same number, then one 2 KB bulk
+        // copy per warp. The peer's P V commit on a slot (XPFREE) means that
+        // the copy out of the staging slot has landed as well.
         const int xs = ig % XP_SLOTS;
         if (ig >= XP_SLOTS && !warp_wait_cluster(bar(B_XPFREE + xs), ((ig / XP_SLOTS) - 1) & 1)) {
           timed_out = true;
