@@ -349,10 +349,30 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def _chunk_bounds(R, n_chunks, weights=None):
+    """Contiguous row ranges of a step's chunks: `n_chunks` equal ones, or
+    sizes in proportion to `weights` (comma-separated), every chunk at least
+    one row."""
+    if weights:
+        w = [float(x) for x in str(weights).split(",") if x.strip()]
+        if not w or min(w) <= 0:
+            raise ValueError(f"bad chunk weights {weights!r}")
+        w = w[:R]
+        tot, acc, cuts = sum(w), 0.0, [0]
+        for x in w[:-1]:
+            acc += x
+            cuts.append(min(R - (len(w) - len(cuts)), max(cuts[-1] + 1, round(R * acc / tot))))
+        cuts.append(R)
+        return list(zip(cuts[:-1], cuts[1:]))
+    n = max(1, min(n_chunks, R))
+    return [(R * k // n, R * (k + 1) // n) for k in range(n)]
+
+
 def run_e2e(hs, cfg, rc, dev, args):
     """The same step through the C ABI from page-locked host buffers.
 
-    A step's rows go in `args.e2e_chunks` contiguous chunks: inputs in on one
+    A step's rows go in contiguous chunks (sizes in proportion to
+    `args.e2e_weights`, else `args.e2e_chunks` equal ones): inputs in on one
     stream, output out on another, and chunk k resolved and attended on
     compute stream k mod `args.e2e_streams`, so that while chunk k is
     attended, chunk k + 1's inputs come in, chunk k - 1's output goes out, and
@@ -360,8 +380,8 @@ def run_e2e(hs, cfg, rc, dev, args):
     share the SMs. Steps stay dependent: a step's first copy waits for the
     previous step's last result to reach host memory."""
     R, H, K = cfg.R, cfg.H, cfg.K
-    n_ch = max(1, min(args.e2e_chunks, R))
-    bounds = [(R * k // n_ch, R * (k + 1) // n_ch) for k in range(n_ch)]
+    bounds = _chunk_bounds(R, args.e2e_chunks, getattr(args, "e2e_weights", None))
+    n_ch = len(bounds)
     # each chunk's inputs (q, top-k, request ids, causal lengths of its rows)
     # sit in one page-locked block, so a chunk comes in with one copy
     names = ("q", "topk", "req", "clen")
@@ -454,7 +474,8 @@ def run_e2e(hs, cfg, rc, dev, args):
     ms = a.elapsed_time(b) / args.steps
     return {"value": round(R / (ms * 1e-3), 1), "unit": "query-rows/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "chunks_per_step": n_ch, "compute_streams": n_cmp, "cuda_graph": True,
+            "chunks_per_step": n_ch, "chunk_rows": [r1 - r0 for r0, r1 in bounds],
+            "compute_streams": n_cmp, "cuda_graph": True,
             "l2": "not flushed between steps: the KV cache (304 MB) is larger than L2, "
                   "and each step copies 36.7 MB through it"}
 
@@ -981,6 +1002,10 @@ def main():
     ap.add_argument("--soak-s", type=float, default=1.0)
     ap.add_argument("--e2e-streams", type=int, default=2,
                     help="compute streams the end-to-end step's chunks take in turn")
+    ap.add_argument("--e2e-weights", default="3,3,2,1",
+                    help="end-to-end leg: chunk sizes in proportion to these comma-separated "
+                         "weights (the last chunks smaller, so that less work follows the last "
+                         "copy in); an empty string gives --e2e-chunks equal chunks")
     ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="row chunks per end-to-end step (copies overlap compute)")
     ap.add_argument("--swap-only", action="store_true",
