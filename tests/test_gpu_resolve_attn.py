@@ -228,3 +228,47 @@ def test_resolve_then_attention_back_to_back_sees_fresh_indices():
         e_idx, _, _ = O.resolve_topk(req, clen, bt, topks[s], bs, bs)
         ref, _ = O.sparse_attn_decode(q.cpu(), kv_np, e_idx, 0.05)
         check_attn(outs[s], ref)
+
+
+def test_chunked_rows_on_two_streams_match_one_call():
+    """The rows of workload 2 in unequal chunks (43 / 42 / 29 / 14), each
+    resolved and attended on one of two streams with no host synchronisation,
+    give the one-call output bit for bit (rows are independent and the kernel
+    is deterministic); sampled rows are checked against the oracle."""
+    hs = lib()
+    cfg = W.get_config(2)
+    rc = W.resident_case(cfg, 0, device=DEV)
+    idx_all = torch.empty_like(rc["topk"])
+    out_all = torch.empty((cfg.R, cfg.H, 512), dtype=torch.bfloat16, device=DEV)
+    lse_all = torch.empty((cfg.R, cfg.H), dtype=torch.float32, device=DEV)
+    hs.hs_resolve_topk(rc["req"], rc["clen"], rc["bt"], rc["topk"], cfg.block_size,
+                       cfg.block_size, idx_all)
+    hs.hs_sparse_attn_decode(rc["q"], rc["kv"], idx_all, cfg.scale, out_all, lse_all)
+    idx = torch.empty_like(rc["topk"])
+    out = torch.full_like(out_all, 7.0)
+    lse = torch.zeros_like(lse_all)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    start = torch.cuda.Event()
+    start.record()
+    cuts = [0, 43, 85, 114, cfg.R]
+    for k in range(len(cuts) - 1):
+        r0, r1 = cuts[k], cuts[k + 1]
+        s = streams[k % 2]
+        s.wait_event(start)
+        hs.hs_resolve_topk(rc["req"][r0:r1], rc["clen"][r0:r1], rc["bt"], rc["topk"][r0:r1],
+                           cfg.block_size, cfg.block_size, idx[r0:r1], stream=s)
+        hs.hs_sparse_attn_decode(rc["q"][r0:r1], rc["kv"], idx[r0:r1], cfg.scale, out[r0:r1],
+                                 lse[r0:r1], stream=s)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx_all)
+    assert torch.equal(out.view(torch.int16), out_all.view(torch.int16))
+    assert torch.equal(lse, lse_all)
+    e_idx, _, _ = O.resolve_topk(rc["req_np"], rc["clen_np"], rc["bt_np"], rc["topk_np"],
+                                 cfg.block_size, cfg.block_size)
+    rows = [42, 43, 84, 85, 113, 114, 127]
+    kvc = rc["kv"]
+    outs, lses = O.sparse_attn_decode_rows(
+        rc["q"].cpu(), lambda r: kvc[torch.as_tensor(r, device=DEV)].cpu().double().numpy(),
+        e_idx, cfg.scale, rows)
+    check_attn(out, np.stack([outs[r] for r in rows]), lse, np.stack([lses[r] for r in rows]),
+               rows=rows)
