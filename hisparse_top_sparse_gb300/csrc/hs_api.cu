@@ -246,30 +246,30 @@ __global__ void __launch_bounds__(256) k_resolve_topk(
   // reads this kernel's output only after this kernel has finished
   asm volatile("griddepcontrol.launch_dependents;\n");
   const int r = blockIdx.x;
+  // No branch on the request id before the top-k loads: the id, the causal
+  // length and the row's entries are read together, and only the block-table
+  // lookups wait for them. A row with no request (id < 0) gives -1
+  // everywhere, no valid entry and the index status bit.
   const int32_t b = req_id[r];
   const int32_t n = clen[r];
-  const int32_t *bt_row = bt + (int64_t)b * bt_stride;
+  const bool none = b < 0;
+  const int32_t *bt_row = bt + (int64_t)(none ? 0 : b) * bt_stride;
   const int32_t *tk = topk + (int64_t)r * K;
   int32_t *o = out + (int64_t)r * K;
   int cnt = 0;
-  bool bad = false;
+  bool bad = none && K > 0;
   auto conv = [&](int32_t t) -> int32_t {
-    if (t < 0) return -1;
+    if (t < 0 || none) return -1;
     if (t >= n) { bad = true; return -1; }
     int32_t blk = bt_row[t / bs];
     if (blk < 0) { bad = true; return -1; }
     ++cnt;
     return blk * stride + t % bs;
   };
-  if (b < 0) {  // a row with no request: nothing valid, flag it
-    for (int j = threadIdx.x; j < K; j += blockDim.x) o[j] = -1;
-    if (threadIdx.x == 0 && status && K > 0) atomicOr(status, HS_STATUS_INDEX);
-    if (threadIdx.x == 0 && out_valid) out_valid[r] = 0;
-    return;
-  }
   if (VEC) {
     const int4 *tk4 = reinterpret_cast<const int4 *>(tk);
     int4 *o4 = reinterpret_cast<int4 *>(o);
+#pragma unroll 2
     for (int j = threadIdx.x; j < K / 4; j += blockDim.x) {
       int4 t = tk4[j];
       int4 v;

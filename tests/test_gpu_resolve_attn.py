@@ -166,6 +166,30 @@ def test_attention_leading_padding(lead):
     check_attn(out, ref, lse, ref_lse)
 
 
+def test_resolve_rows_without_a_request():
+    """A row whose request id is negative gets -1 everywhere, no valid entry
+    and the index status bit; the other rows of the call are unaffected."""
+    hs = lib()
+    g = np.random.default_rng(21)
+    B, bs, nblk, R, K = 3, 16, 8, 6, 64
+    bt = g.permutation(B * nblk).reshape(B, nblk).astype(np.int32)
+    req = np.array([0, -1, 2, 1, -5, 0], np.int32)
+    clen = np.full(R, nblk * bs, np.int32)
+    topk = g.integers(-1, nblk * bs, size=(R, K)).astype(np.int32)
+    t = lambda a: torch.as_tensor(a, device=DEV)
+    out = torch.full((R, K), 7, dtype=torch.int32, device=DEV)
+    valid = torch.full((R,), 7, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hs.hs_resolve_topk(t(req), t(clen), t(bt), t(topk), bs, bs, out, valid, st)
+    torch.cuda.synchronize()
+    ok = req >= 0
+    e_idx, e_valid, e_st = O.resolve_topk(req[ok], clen[ok], bt, topk[ok], bs, bs)
+    assert e_st == 0
+    assert np.array_equal(np_(out)[ok], e_idx) and np.array_equal(np_(valid)[ok], e_valid)
+    assert (np_(out)[~ok] == -1).all() and (np_(valid)[~ok] == 0).all()
+    assert int(st.item()) == O.STATUS_INDEX
+
+
 def test_workload2_full_size():
     hs = lib()
     cfg = W.get_config(2)
