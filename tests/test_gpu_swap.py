@@ -18,9 +18,10 @@ def _t(a):
 
 
 class Pair:
-    """The GPU buffer and the oracle buffer over the same inputs."""
+    """The GPU buffer and the oracle buffer over the same inputs (copy_sms >
+    0: the swap-in's copy kernel held to about that many SMs)."""
 
-    def __init__(self, B, S, n_step, max_ctx, bs, seed):
+    def __init__(self, B, S, n_step, max_ctx, bs, seed, copy_sms=0):
         hs = lib()
         g = np.random.default_rng(seed)
         nblk = (max_ctx + bs - 1) // bs
@@ -28,6 +29,8 @@ class Pair:
         self.pool = W.host_pool_tensor(B * nblk * bs, seed, device=DEV)
         self.hot = torch.zeros((B * (S + n_step), 576), dtype=torch.bfloat16, device=DEV)
         self.buf = hs.HsBuffer(B, S, n_step, max_ctx, bs, self.hot, self.pool, _t(self.hbt))
+        if copy_sms:
+            hs.hs_buffer_set_copy_sms(self.buf, copy_sms)
         self.ref = O.HotBuffer(B, S, n_step, max_ctx, bs, self.hbt, self.pool.clone())
         self.B, self.S, self.n_step = B, S, n_step
         self.hs = hs
@@ -60,11 +63,12 @@ class Pair:
         assert self.buf.clock == self.ref.now
 
 
+@pytest.mark.parametrize("copy_sms", [0, 3])
 @pytest.mark.parametrize("seed", range(6))
-def test_random_sequences_tiny(seed):
+def test_random_sequences_tiny(seed, copy_sms):
     g = np.random.default_rng(1000 + seed)
     B, S, n_step, bs, max_ctx = 3, int(g.integers(2, 12)), 3, 4, 48
-    p = Pair(B, S, n_step, max_ctx, bs, seed)
+    p = Pair(B, S, n_step, max_ctx, bs, seed, copy_sms)
     L = [int(x) for x in g.integers(1, 44, size=B)]
     for call in range(12):
         R = int(g.integers(1, 6))
@@ -139,7 +143,7 @@ def test_resolve_and_swap_paths_give_identical_attention():
     assert hs.hs_get_status(buf) == 0
 
 
-def _run_locality(cfg_no, sample, steps=None):
+def _run_locality(cfg_no, sample, steps=None, copy_sms=0):
     hs = lib()
     cfg = W.get_config(cfg_no)
     steps = steps or cfg.steps
@@ -148,6 +152,8 @@ def _run_locality(cfg_no, sample, steps=None):
     hb = W.host_backed_case(cfg, device=DEV)
     buf = hs.HsBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hb["hot"],
                       hb["pool"], hb["hbt"])
+    if copy_sms:
+        hs.hs_buffer_set_copy_sms(buf, copy_sms)
     ref = O.HotBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hb["hbt_np"],
                       hb["pool"])
     sets = [W.locality_sets(cfg, cfg.L[b], b, steps) for b in range(cfg.B)]
@@ -176,6 +182,11 @@ def _run_locality(cfg_no, sample, steps=None):
 
 def test_workload3_sampled_requests():
     stats = _run_locality(3, sample=[0, 17, 63], steps=6)
+    assert stats[1] > 0
+
+
+def test_workload3_sampled_requests_separate_copy_kernel():
+    stats = _run_locality(3, sample=[1, 40], steps=3, copy_sms=16)
     assert stats[1] > 0
 
 
