@@ -128,7 +128,7 @@ int hs_check_buffer(const hs_buffer *buf);
 
 // The index of the largest of logits[0 .. V-1] (fp32 or bf16 as dtype says),
 // the lowest index among equals, for the block's thread 0 (others: unspecified).
-// 16-byte streaming loads over the aligned body, four in flight per thread;
+// 16-byte streaming loads over the aligned body, eight in flight per thread;
 // scalar loads for the unaligned head and the tail. Every thread of the block
 // (HS_ARGMAX_THREADS of them) calls it.
 template <int DTYPE>
@@ -168,12 +168,12 @@ __device__ __forceinline__ int32_t hs_row_argmax(const char *base, int32_t V) {
   for (int i = threadIdx.x; i < head; i += NT) take(best, load(i), i);
   const uint4 *body = reinterpret_cast<const uint4 *>(base + (int64_t)head * elem);
   int k = threadIdx.x;
-  for (; k + 3 * NT < nvec; k += 4 * NT) {
-    uint4 w[4];
+  for (; k + 7 * NT < nvec; k += 8 * NT) {
+    uint4 w[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) w[u] = __ldcs(body + k + u * NT);
+    for (int u = 0; u < 8; ++u) w[u] = __ldcs(body + k + u * NT);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) take16(best, w[u], head + (k + u * NT) * per16);
+    for (int u = 0; u < 8; ++u) take16(best, w[u], head + (k + u * NT) * per16);
   }
   for (; k < nvec; k += NT) take16(best, __ldcs(body + k), head + k * per16);
   for (int i = head + nvec * per16 + threadIdx.x; i < V; i += NT) take(best, load(i), i);
