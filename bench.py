@@ -45,11 +45,50 @@ L2_FLUSH_BYTES = 256 << 20
 ROW_BYTES = 576 * 2
 
 
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal (context for the measured peak)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def init_dist(ws: int) -> None:
+    """One process per GPU under torchrun: NCCL when CUDA is there, gloo
+    otherwise (the CPU tests of this launch path). Only the barrier and the
+    step-time reduction use it; the data path has no collective."""
+    if ws > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+
+def barrier(ws: int) -> None:
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own batch of the same shape (weak scaling)."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(t_ms: float, ws: int, device=None) -> float:
+    """The job's step time: the slowest rank's."""
+    if ws <= 1:
+        return t_ms
+    import torch.distributed as dist
+    t = torch.tensor([t_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(ws: int, rows_per_rank: int, t_ms: float) -> float:
+    """Whole-job throughput: the query rows of every rank over the job's step time."""
+    return ws * rows_per_rank / (t_ms * 1e-3)
 
 
 def _peaks():
@@ -218,12 +257,10 @@ def run_ours(args):
     ws, rank, local = _dist()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    init_dist(ws)
 
     cfg = W.get_config(2)
-    cfg.seed = cfg.seed + 1000 * rank          # each rank its own batch, same shape
+    cfg.seed = rank_seed(cfg.seed, rank)       # each rank its own batch, same shape
     rc = W.resident_case(cfg, 0, device=dev)
     R, H, K = cfg.R, cfg.H, cfg.K
     idx = torch.empty_like(rc["topk"])
@@ -247,11 +284,6 @@ def run_ours(args):
     torch.cuda.synchronize()
     valid_np = valid.cpu().numpy()
 
-    def barrier():
-        if ws > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
     step_ms, attn_ms = [], []
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -264,7 +296,7 @@ def run_ours(args):
             flush.fill_(1)
             step()
             torch.cuda.synchronize()
-        barrier()
+        barrier(ws)
         torch.cuda.synchronize()
         # the step: no event between the two launches, so that the attention
         # (a programmatic dependent launch) starts its prologue under resolve
@@ -277,7 +309,7 @@ def run_ours(args):
             hs.hs_sparse_attn_decode(rc["q"], rc["kv"], idx, cfg.scale, out, lse)
             e[2].record(stream)
         torch.cuda.synchronize()
-        barrier()
+        barrier(ws)
         # the attention launch alone, for its roofline: same flush, its own events
         for e in evs:
             flush.fill_(1)
@@ -286,17 +318,12 @@ def run_ours(args):
             hs.hs_sparse_attn_decode(rc["q"], rc["kv"], idx, cfg.scale, out, lse)
             e[3].record(stream)
         torch.cuda.synchronize()
-        barrier()
+        barrier(ws)
     for e in evs:
         step_ms.append(e[0].elapsed_time(e[2]))
         attn_ms.append(e[1].elapsed_time(e[3]))
-    t_step = sum(step_ms) / len(step_ms)
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([t_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step = float(t.item())
-    rows_per_s = ws * R / (t_step * 1e-3)
+    t_step = max_over_ranks(sum(step_ms) / len(step_ms), ws, dev)
+    rows_per_s = job_rows_per_s(ws, R, t_step)
 
     # roofline of the attention kernel
     peaks, peak_kind = _peaks()
@@ -305,6 +332,8 @@ def run_ours(args):
     achieved = alg_bytes / t_attn / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                "nominal_peak": NOMINAL_HBM_GBS,
                 "traffic": _traffic(), "peak_kind": peak_kind,
                 "kernel": "k_attn_pair", "algorithmic_bytes_per_launch": alg_bytes,
                 "attn_ms": round(t_attn * 1e3, 4),
@@ -487,7 +516,8 @@ def _attn_roofline(valid_per_step, ms_per_step, R, H, K):
     gbs = sum(byt) / (sum(ms_per_step) * 1e-3) / 1e9
     peak = _peaks()[0]["hbm_gbs"]
     return {"bytes_per_step": int(statistics.mean(byt)), "achieved": round(gbs, 1),
-            "peak": peak, "frac": round(gbs / peak, 4)}
+            "peak": peak, "frac": round(gbs / peak, 4),
+            "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4)}
 
 
 def _lead(stream=None, cycles=1 << 18):

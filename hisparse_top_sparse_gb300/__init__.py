@@ -332,6 +332,12 @@ def hs_verify_accept_noalloc(logits, draft_tokens, accept_len, next_token,
         dt = HS_LOGITS_BF16
     else:
         raise TypeError("logits must be float32 or bfloat16")
+    # the static scratch and the stream used are those of the current device
+    cur = torch.cuda.current_device()
+    for name, t in (("logits", logits), ("draft_tokens", draft_tokens),
+                    ("accept_len", accept_len), ("next_token", next_token)):
+        if isinstance(t, torch.Tensor) and t.is_cuda and t.device.index != cur:
+            raise ValueError(f"{name} is on {t.device}, not on the current device cuda:{cur}")
     _check(lib().hs_verify_accept_noalloc(
         _ptr(logits, "logits"), dt, B, d, V,
         _ptr(draft_tokens, "draft_tokens", torch.int32, (B, d), allow_none=(d == 0)),

@@ -65,7 +65,8 @@ int hs_check_buffer(const hs_buffer *buf) {
 static void free_buffer(hs_buffer *b) {
   if (!b) return;
   void *ptrs[] = {b->token_slot, b->slot_token, b->slot_ts, b->lru_order, b->pos_mark,
-                  b->copy_desc,  b->copy_cnt,   b->pred,    b->row_count, b->status};
+                  b->copy_desc,  b->copy_cnt,   b->pred,    b->row_count, b->verify_claim,
+                  b->status};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   free(b);
@@ -143,6 +144,7 @@ extern "C" int hs_buffer_create(const hs_buffer_desc *d, hs_buffer **out) {
       {(void **)&b->copy_cnt, R * 4, 0},
       {(void **)&b->pred, R * (size_t)d->step_slots * 4, 0},
       {(void **)&b->row_count, R * 4, 0},
+      {(void **)&b->verify_claim, R * 4, 0},
       {(void **)&b->status, 4, 0},
   };
   for (auto &e : plan) {

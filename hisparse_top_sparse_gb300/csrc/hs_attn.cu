@@ -422,33 +422,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 
   // Q by nine tensor copies of 128 heads x 64 dims (16 KB, 128-byte swizzle,
-  // rows past H filled with zeros), each issued by one CTA of the pair and
-  // multicast to both: dims 384..575 land in SMEM as the MMA's A operand,
-  // dims 0..383 in a staging area over the (still empty) rings A and VO and
-  // the P staging slots, from where
-  // each head's thread moves them into TMEM
+  // rows past H filled with zeros), all issued by this CTA into its own
+  // shared memory: dims 384..575 land in SMEM as the MMA's A operand, dims
+  // 0..383 in a staging area over the (still empty) rings A and VO and the P
+  // staging slots, from where each head's thread moves them into TMEM
   static_assert(6 * HG * 128 <= XP_OFF - RA_OFF, "Q staging fits rings A, VO and the P staging");
+  if (tid == 0) {
+    // the barrier was initialised by this thread; the copies need no peer
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    arrive_expect_tx(bar(B_QLOAD), 9 * HG * 128);
+    for (int a = 0; a < D / 64; ++a) {
+      const uint32_t dst = a < 6 ? sbase + RA_OFF + a * (HG * 128) : sbase + QS_OFF + (a - 6) * (HG * 128);
+      asm volatile(
+          "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+          " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+          "l"(reinterpret_cast<uint64_t>(&tmap_q)), "r"(64 * a), "r"(h0), "r"(r), "r"(bar(B_QLOAD))
+          : "memory");
+    }
+  }
   fence_before();
   cluster_sync();          // both CTAs' barriers exist before any remote operation
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (tid == 0) {
-    arrive_expect_tx(bar(B_QLOAD), 9 * HG * 128);
-    for (int a = c; a < D / 64; a += 2) {
-      const uint32_t dst = a < 6 ? sbase + RA_OFF + a * (HG * 128) : sbase + QS_OFF + (a - 6) * (HG * 128);
-      asm volatile(
-          "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-          ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;\n" ::"r"(dst),
-          "l"(reinterpret_cast<uint64_t>(&tmap_q)), "r"(64 * a), "r"(h0), "r"(r), "r"(bar(B_QLOAD)),
-          "h"((uint16_t)3)
-          : "memory");
-    }
-  }
   bool timed_out = false;
   if (warp < 4) {
     // staged Q dims 0..383 -> TMEM columns [256, 448): lane = head, column j
     // holds dims 2j, 2j+1
-    if (!warp_wait_cluster(bar(B_QLOAD), 0)) timed_out = true;
+    if (!warp_wait(bar(B_QLOAD), 0)) timed_out = true;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
     for (int part = 0; part < QT_DIMS / 64; ++part) {
@@ -798,7 +798,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   }
 
-  if (timed_out && status) atomicOr(status, 4u);
+  if (timed_out && status) atomicOr(status, HS_STATUS_TIMEOUT);
   fence_before();
   cluster_sync();          // the peer writes into this CTA's shared memory until here
   if (warp == 0) {

@@ -36,6 +36,7 @@ struct hs_buffer {
   int32_t *copy_cnt;     // [max_reqs]: misses to copy in the current call
   int32_t *pred;         // [max_reqs*n_step] argmax per verify row
   int32_t *row_count;    // [max_reqs] verify rows done per request in a call (0 between calls)
+  uint32_t *verify_claim; // [max_reqs]: low 32 bits of the clock of the last commit of a request
   uint32_t *status;      // device status word
 
   int64_t clock;         // LRU clock: swap-in and commit calls made so far

@@ -12,6 +12,8 @@
 // arrays of fixed size, which every GPU that loads this library holds until
 // the process exits. No call below allocates.
 
+#include <cuda.h>
+
 #include <mutex>
 
 #include "hs_internal.cuh"
@@ -25,12 +27,64 @@ static __device__ __align__(256) int32_t g_accept_count[HS_NOALLOC_MAX_ROWS];
 
 namespace {
 
-// Device address of g_accept_scratch on each device, looked up once. In host
-// code the array's name is only a host-side stand-in; kernels must receive the
-// address that cudaGetSymbolAddress returns for the current device.
-int32_t *g_scratch_dev[HS_NOALLOC_MAX_DEVICES] = {nullptr};
-int32_t *g_count_dev[HS_NOALLOC_MAX_DEVICES] = {nullptr};
+// Device addresses of the two arrays in each device's current context. In
+// host code an array's name is only a host-side stand-in; kernels must
+// receive the address that cudaGetSymbolAddress returns with the device
+// current. The addresses belong to a context: after cudaDeviceReset the
+// device gets a new primary context and the arrays new addresses, so each
+// cache entry remembers the unique id of the context it was taken in
+// (cuCtxGetId) and is looked up again when the current context's id differs.
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  int32_t *pred;
+  int32_t *count;
+};
+ScratchEntry g_entry[HS_NOALLOC_MAX_DEVICES] = {};
 std::mutex g_scratch_mu;
+
+using PFN_ctxGetCurrent = CUresult (*)(CUcontext *);
+using PFN_ctxGetId = CUresult (*)(CUcontext, unsigned long long *);
+
+// the unique id of the calling thread's current context (0 when unknown)
+int current_ctx_id(unsigned long long *id) {
+  static PFN_ctxGetCurrent get_current = nullptr;
+  static PFN_ctxGetId get_id = nullptr;
+  if (!get_current || !get_id) {
+    void *f1 = nullptr, *f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) !=
+            cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || !f1 ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) !=
+            cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess || !f2)
+      return hs_set_error(HS_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId not available");
+    get_current = reinterpret_cast<PFN_ctxGetCurrent>(f1);
+    get_id = reinterpret_cast<PFN_ctxGetId>(f2);
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx)
+    return hs_set_error(HS_ERR_CUDA, "no current CUDA context");
+  if (get_id(ctx, id) != CUDA_SUCCESS)
+    return hs_set_error(HS_ERR_CUDA, "cuCtxGetId failed");
+  return HS_OK;
+}
+
+int lookup_symbols(ScratchEntry *e) {
+  void *p = nullptr;
+  cudaError_t err = cudaGetSymbolAddress(&p, g_accept_scratch);
+  if (err != cudaSuccess || !p)
+    return hs_set_error(HS_ERR_CUDA, "cudaGetSymbolAddress(g_accept_scratch) failed: %s",
+                        cudaGetErrorString(err));
+  void *pc = nullptr;
+  err = cudaGetSymbolAddress(&pc, g_accept_count);
+  if (err != cudaSuccess || !pc)
+    return hs_set_error(HS_ERR_CUDA, "cudaGetSymbolAddress(g_accept_count) failed: %s",
+                        cudaGetErrorString(err));
+  e->pred = static_cast<int32_t *>(p);
+  e->count = static_cast<int32_t *>(pc);
+  return HS_OK;
+}
 
 int scratch_for_current_device(int32_t **out, int32_t **count) {
   int dev = -1;
@@ -38,22 +92,23 @@ int scratch_for_current_device(int32_t **out, int32_t **count) {
   if (dev < 0 || dev >= HS_NOALLOC_MAX_DEVICES)
     return hs_set_error(HS_ERR_UNSUPPORTED, "device %d beyond %d", dev, HS_NOALLOC_MAX_DEVICES);
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_dev[dev]) {
-    void *p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_accept_scratch);
-    if (e != cudaSuccess || !p)
-      return hs_set_error(HS_ERR_CUDA, "cudaGetSymbolAddress(g_accept_scratch) failed: %s",
-                          cudaGetErrorString(e));
-    void *pc = nullptr;
-    e = cudaGetSymbolAddress(&pc, g_accept_count);
-    if (e != cudaSuccess || !pc)
-      return hs_set_error(HS_ERR_CUDA, "cudaGetSymbolAddress(g_accept_count) failed: %s",
-                          cudaGetErrorString(e));
-    g_scratch_dev[dev] = static_cast<int32_t *>(p);
-    g_count_dev[dev] = static_cast<int32_t *>(pc);
+  ScratchEntry &e = g_entry[dev];
+  unsigned long long id = 0;
+  if (current_ctx_id(&id) != HS_OK) {
+    // no current context yet: the symbol lookup makes the device's primary
+    // context current, then its id can be read
+    int rc = lookup_symbols(&e);
+    if (rc) return rc;
+    rc = current_ctx_id(&id);
+    if (rc) return rc;
+    e.ctx_id = id;
+  } else if (!e.pred || e.ctx_id != id) {
+    int rc = lookup_symbols(&e);
+    if (rc) return rc;
+    e.ctx_id = id;
   }
-  *out = g_scratch_dev[dev];
-  *count = g_count_dev[dev];
+  *out = e.pred;
+  *count = e.count;
   return HS_OK;
 }
 

@@ -35,6 +35,7 @@ struct CommitArgs {
   int32_t *token_slot, *slot_token;
   int64_t *slot_ts;
   int32_t *lru_order;
+  uint32_t *verify_claim;
   uint32_t *status;
   int64_t now;
 };
@@ -72,6 +73,10 @@ __device__ __forceinline__ void commit_request(const int b, const CommitArgs &ca
     int ok = 1;
     int L = 0;
     if (req < 0 || req >= max_reqs) {
+      ok = 0;
+      atomicOr(status, HS_STATUS_INDEX);
+    } else if (atomicExch(ca.verify_claim + req, (uint32_t)now) == (uint32_t)now) {
+      // the request appears twice in req_ids: only its first claimant commits
       ok = 0;
       atomicOr(status, HS_STATUS_INDEX);
     } else {
@@ -194,7 +199,8 @@ extern "C" int hs_verify_finalize(hs_buffer *buf, const void *logits, int32_t lo
   ca.pool = reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(buf->host_pool));
   ca.hot = reinterpret_cast<uint4 *>(buf->hot_kv);
   ca.token_slot = buf->token_slot; ca.slot_token = buf->slot_token; ca.slot_ts = buf->slot_ts;
-  ca.lru_order = buf->lru_order; ca.status = buf->status; ca.now = buf->clock;
+  ca.lru_order = buf->lru_order; ca.verify_claim = buf->verify_claim; ca.status = buf->status;
+  ca.now = buf->clock;
   const size_t smem = (size_t)buf->S * sizeof(int32_t);
   if (logits_dtype == HS_LOGITS_F32)
     k_verify<HS_LOGITS_F32><<<rows, HS_ARGMAX_THREADS, smem, stream>>>(logits, V, buf->row_count, ca);

@@ -260,8 +260,9 @@ int hs_sparse_attn_decode(const void *q, const void *kv, int64_t n_kv_rows,
 
 /* ------------------------------------------------------------------------ */
 /* next-3: a batch mixing fully-resident and host-backed requests            */
-/*         ("hiSparse-MTP" page: reclaim_resident_blocks, the fully_resident */
-/*          flag and HiSparseCacheHandle.resolve_topk)                       */
+/*         ("vllm 分析(十二) HiSparse 下篇": the HiSparseResidentSpec and      */
+/*          reclaim_resident_blocks sections, the fully_resident flag, and   */
+/*          HiSparseCacheHandle.resolve_topk)                                */
 /* ------------------------------------------------------------------------ */
 
 /*
@@ -443,7 +444,12 @@ int hs_backup_indexer(int32_t n_layers, const void *const *src_caches, void *con
  *   step_kv       device bf16 [B][d+1][576]
  *   kv_len        device int32 [max_reqs], updated in place
  *   accept_len, next_token  device int32 [B]
- *   req_ids       device int32 [B] or NULL (identity)
+ *   req_ids       device int32 [B] or NULL (identity); distinct request ids.
+ *                 A request id out of [0, max_reqs) or repeated within the
+ *                 call sets HS_STATUS_INDEX; of a repeated id's entries only
+ *                 the first to finish its acceptance commits (which one is
+ *                 not specified), the others commit nothing. Every entry
+ *                 still gets its accept_len and next_token.
  * Requirements: 1 <= B <= max_reqs, 0 <= d, d + 1 <= step_slots, V >= 1.
  */
 int hs_verify_finalize(hs_buffer *buf, const void *logits, int32_t logits_dtype,
@@ -470,7 +476,11 @@ int hs_verify_finalize(hs_buffer *buf, const void *logits, int32_t logits_dtype,
  * loads it until the process exits. Sizes with B * (d + 1) > 65536 return
  * HS_ERR_INVALID_ARG. No cudaMalloc, cudaFree or allocating library routine
  * is called. The first call on a device looks up the arrays' device addresses
- * (cudaGetSymbolAddress); make that first call before any stream capture. One
+ * (cudaGetSymbolAddress) in the device's current context; make that first
+ * call before any stream capture. The addresses are kept per device together
+ * with the id of that context, and looked up again when a call finds another
+ * context current (after cudaDeviceReset, say). Every pointer argument must
+ * be memory of the current device. One
  * launch: the last row of each request to finish takes its prefix and puts
  * the request's count back to 0, so nothing carries over between calls, but
  * all calls share the arrays: calls that overlap on the GPU (different

@@ -207,7 +207,8 @@ def test_workload2_full_size():
                                           rc["topk_np"], cfg.block_size, cfg.block_size)
     assert np.array_equal(np_(idx), e_idx) and np.array_equal(np_(valid), e_valid)
     assert int(st.item()) == e_st == 0
-    rows = [0, 1, 2, 3, 45, 64, 101, 127]
+    # every row of the workload against the oracle (about a second of float64)
+    rows = list(range(cfg.R))
     kvc = rc["kv"]
     outs, lses = O.sparse_attn_decode_rows(
         rc["q"].cpu(), lambda r: kvc[torch.as_tensor(r, device=DEV)].cpu().double().numpy(),

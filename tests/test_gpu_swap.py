@@ -143,7 +143,14 @@ def test_resolve_and_swap_paths_give_identical_attention():
     assert hs.hs_get_status(buf) == 0
 
 
-def _run_locality(cfg_no, sample, steps=None, copy_sms=0):
+def _run_locality(cfg_no, sample, steps=None, copy_sms=0, attn=True):
+    """Workload 3 or 4 over its decode steps: every swap-in call on all the
+    workload's rows; the oracle follows the sampled requests (their rows of
+    the same calls). After every call the sampled rows' slot tables and valid
+    counts must match bit for bit, and (attn) the attention over the GPU's
+    hot buffer with the GPU's slot tables must match the oracle's attention
+    over its own hot buffer with its own tables (R13); at the end the sampled
+    requests' maps, timestamps and hot rows must match bit for bit."""
     hs = lib()
     cfg = W.get_config(cfg_no)
     steps = steps or cfg.steps
@@ -158,6 +165,7 @@ def _run_locality(cfg_no, sample, steps=None, copy_sms=0):
                       hb["pool"])
     sets = [W.locality_sets(cfg, cfg.L[b], b, steps) for b in range(cfg.B)]
     rows_s = np.where(np.isin(req, sample))[0]
+    t_rows = torch.as_tensor(rows_s, device=DEV)
     stats = torch.zeros(2, dtype=torch.int64, device=DEV)
     for step in range(steps):
         topk = W.topk_shared_sets(cfg, sets, step)
@@ -169,6 +177,17 @@ def _run_locality(cfg_no, sample, steps=None, copy_sms=0):
         assert np.array_equal(np_(out)[rows_s], e_out)
         assert np.array_equal(np_(valid)[rows_s], e_valid)
         assert hs.hs_get_status(buf) == e_st == 0
+        if attn:
+            q = W.step_q(cfg, step, device=DEV)[t_rows].contiguous()
+            o = torch.empty((len(rows_s), cfg.H, 512), dtype=torch.bfloat16, device=DEV)
+            lse = torch.empty((len(rows_s), cfg.H), dtype=torch.float32, device=DEV)
+            hs.hs_sparse_attn_decode(q, hb["hot"], out[t_rows].contiguous(), cfg.scale, o, lse)
+            qc = q.cpu()
+            outs, lses = O.sparse_attn_decode_rows(
+                qc, lambda sel: O.bf16_bits_to_f64(ref.hot[np.asarray(sel)]), e_out, cfg.scale,
+                range(len(rows_s)))
+            check_attn(o, np.stack([outs[k] for k in range(len(rows_s))]), lse,
+                       np.stack([lses[k] for k in range(len(rows_s))]))
     ts, stok, sts = buf.dump()
     hot = hb["hot"].view(torch.int16).cpu().numpy().view(np.uint16)
     for b in sample:
@@ -180,18 +199,23 @@ def _run_locality(cfg_no, sample, steps=None, copy_sms=0):
     return np_(stats)
 
 
-def test_workload3_sampled_requests():
-    stats = _run_locality(3, sample=[0, 17, 63], steps=6)
+def test_workload3_all_steps_every_eighth_request():
+    """All 16 steps of workload 3; requests 0, 8, ..., 56 followed by the
+    oracle, with the attention on their swap-in indices every step."""
+    stats = _run_locality(3, sample=list(range(0, 64, 8)))
     assert stats[1] > 0
 
 
 def test_workload3_sampled_requests_separate_copy_kernel():
-    stats = _run_locality(3, sample=[1, 40], steps=3, copy_sms=16)
+    stats = _run_locality(3, sample=[1, 40], steps=3, copy_sms=16, attn=False)
     assert stats[1] > 0
 
 
-def test_workload4_sampled_requests():
-    _run_locality(4, sample=[5, 127], steps=3)
+def test_workload4_all_steps_every_eighth_request():
+    """All 8 steps of workload 4 (contexts 16K-128K); requests 0, 8, ..., 120
+    followed by the oracle, with the attention on their swap-in indices
+    every step."""
+    _run_locality(4, sample=list(range(0, 128, 8)))
 
 
 def test_largest_slot_count_and_long_context():

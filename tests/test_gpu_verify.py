@@ -169,11 +169,17 @@ def test_workload5_verify_finalize():
     for b in range(cfg.B):
         m = int(e_acc[b])
         assert planted[b, :m].all() and (m == cfg.d or not planted[b, m])
+    # every request's maps, timestamps and LRU hot rows, and the whole host pool
     ts, stok, sts = buf.dump()
-    for b in range(0, cfg.B, 17):
+    for b in range(cfg.B):
         assert stok[b].tolist() == ref.slot_token[b]
         assert sts[b].tolist() == ref.slot_ts[b]
+        assert np.array_equal(ts[b].numpy(), ref.token_slot_array(b))
     assert np.array_equal(_u16(hb["pool"]), ref.host_pool)
+    hot = _u16(hb["hot"])
+    lru = np.concatenate([np.arange(b * hb["S_tot"], b * hb["S_tot"] + cfg.S)
+                          for b in range(cfg.B)])
+    assert np.array_equal(hot[lru], ref.hot[lru])
 
 
 def test_longest_draft_chain_commits_and_evicts():
@@ -224,4 +230,116 @@ def test_longest_draft_chain_commits_and_evicts():
             assert sts[b].tolist() == ref.slot_ts[b]
             assert np.array_equal(ts[b].numpy(), ref.token_slot_array(b))
         assert np.array_equal(_u16(pool), ref.host_pool)
+    buf.close()
+
+
+def _small_verify_setup(seed, B=6, d=3, V=500, S=24, bs=8, max_ctx=256):
+    hs = lib()
+    g = np.random.default_rng(seed)
+    nblk = max_ctx // bs
+    hbt = g.permutation(B * nblk).reshape(B, nblk).astype(np.int32)
+    pool = W.host_pool_tensor(B * nblk * bs, seed, device=DEV)
+    hot = torch.zeros((B * (S + d + 1), 576), dtype=torch.bfloat16, device=DEV)
+    buf = hs.HsBuffer(B, S, d + 1, max_ctx, bs, hot, pool, _t(hbt))
+    ref = O.HotBuffer(B, S, d + 1, max_ctx, bs, hbt, pool.clone())
+    L = [int(x) for x in g.integers(40, 120, size=B)]
+    kv_len = _t(np.asarray(L, np.int32))
+    req = np.arange(B, dtype=np.int32)
+    clen = np.array([x + 1 for x in L], np.int32)
+    topk = np.stack([g.choice(x, 12, replace=False) for x in L]).astype(np.int32)
+    out = torch.empty((B, 12), dtype=torch.int32, device=DEV)
+    hs.hs_swap_in(buf, _t(req), _t(clen), kv_len, _t(topk), out)
+    e_out, _, _, _ = ref.swap_in(req, clen, L, topk)
+    assert np.array_equal(np_(out), e_out)
+    return hs, g, buf, ref, hot, pool, kv_len, L
+
+
+def _compare_request(buf, ref, hot, b, S, S_tot):
+    ts, stok, sts = buf.dump()
+    assert stok[b].tolist() == ref.slot_token[b]
+    assert sts[b].tolist() == ref.slot_ts[b]
+    assert np.array_equal(ts[b].numpy(), ref.token_slot_array(b))
+    lo = b * S_tot
+    assert np.array_equal(_u16(hot)[lo:lo + S], ref.hot[lo:lo + S])
+
+
+def test_verify_with_permuted_request_ids():
+    """req_ids maps batch entry b to request perm[b]: the same computation as
+    the identity batch with its entries reordered, so the oracle runs on the
+    reordered batch and every entry's result and every request's state must
+    match bit for bit."""
+    B, d, V, S = 6, 3, 500, 24
+    hs, g, buf, ref, hot, pool, kv_len, L = _small_verify_setup(41, B, d, V, S)
+    perm = g.permutation(B).astype(np.int32)
+    lg = g.standard_normal((B, d + 1, V)).astype(np.float32)
+    drafts = g.integers(0, V, size=(B, d)).astype(np.int32)
+    for b in range(B):
+        for i in range(d):
+            if g.random() < 0.6:
+                drafts[b, i] = int(np.argmax(lg[b, i]))
+    skv = W.bf16_normal((B, d + 1, 576), 1.0, 41, "skv_perm")
+    acc = torch.empty(B, dtype=torch.int32, device=DEV)
+    nxt = torch.empty_like(acc)
+    hs.hs_verify_finalize(buf, _t(lg), _t(drafts), skv.to(DEV), kv_len, acc, nxt,
+                          req_ids=_t(perm))
+    inv = np.argsort(perm)               # request r is batch entry inv[r]
+    e_acc, e_nxt, e_L, e_st = O.verify_finalize(ref, torch.as_tensor(lg[inv]), drafts[inv],
+                                                skv[torch.as_tensor(inv)], L)
+    torch.cuda.synchronize()
+    assert hs.hs_get_status(buf) == e_st == 0
+    assert np.array_equal(np_(acc), e_acc[perm]) and np.array_equal(np_(nxt), e_nxt[perm])
+    assert np.array_equal(np_(kv_len), e_L)
+    for b in range(B):
+        _compare_request(buf, ref, hot, b, S, S + d + 1)
+    assert np.array_equal(_u16(pool), ref.host_pool)
+    buf.close()
+
+
+def test_verify_with_a_repeated_request_id():
+    """A request id twice in one call: HS_STATUS_INDEX is set, every entry
+    still gets its acceptance, exactly one of the two entries commits (the
+    request's state equals the oracle's after committing either one), the
+    other request of the call commits normally and the rest are untouched."""
+    import copy
+    B, d, V, S = 6, 3, 500, 24
+    hs, g, buf, ref, hot, pool, kv_len, L = _small_verify_setup(43, B, d, V, S)
+    ids = np.array([2, 4, 2], np.int32)
+    n = len(ids)
+    lg = g.standard_normal((n, d + 1, V)).astype(np.float32)
+    drafts = g.integers(0, V, size=(n, d)).astype(np.int32)
+    drafts[0, :2] = np.argmax(lg[0, :2], axis=1)          # entry 0 accepts 2, entry 2 fewer
+    skv = W.bf16_normal((n, d + 1, 576), 1.0, 43, "skv_dup")
+    before = buf.dump()
+    acc = torch.empty(n, dtype=torch.int32, device=DEV)
+    nxt = torch.empty_like(acc)
+    hs.hs_verify_finalize(buf, _t(lg), _t(drafts), skv.to(DEV), kv_len, acc, nxt,
+                          req_ids=_t(ids))
+    torch.cuda.synchronize()
+    assert hs.hs_get_status(buf) == O.STATUS_INDEX
+    for k in range(n):
+        preds = [O.argmax_lowest(lg[k, i]) for i in range(d + 1)]
+        assert (int(acc[k]), int(nxt[k])) == O.greedy_accept(preds, drafts[k])
+    # the oracle with request 2 taking entry 0, and with it taking entry 2
+    matches = 0
+    for pick in (0, 2):
+        r = copy.deepcopy(ref)
+        full_lg = np.zeros((B, d + 1, V), np.float32)
+        full_dr = np.zeros((B, d), np.int32)
+        full_kv = torch.zeros((B, d + 1, 576), dtype=torch.bfloat16)
+        for req_id, k in ((2, pick), (4, 1)):
+            full_lg[req_id], full_dr[req_id], full_kv[req_id] = lg[k], drafts[k], skv[k]
+        _, _, e_L, _ = O.verify_finalize(r, torch.as_tensor(full_lg), full_dr, full_kv, L)
+        try:
+            assert int(kv_len[2]) == e_L[2] and int(kv_len[4]) == e_L[4]
+            for b in (2, 4):
+                _compare_request(buf, r, hot, b, S, S + d + 1)
+            matches += 1
+        except AssertionError:
+            pass
+    assert matches >= 1
+    after = buf.dump()
+    for b in (0, 1, 3, 5):
+        assert int(kv_len[b]) == L[b]
+        for x, y in zip(before, after):
+            assert torch.equal(x[b], y[b])
     buf.close()
