@@ -762,12 +762,16 @@ def run_verify_bench(hs, dev, peak_hbm):
             "finalize_ms": round(fin_ms, 4), "rows_committed": committed, "status": st}
 
 
-def run_overlap_bench(hs, dev, steps=8):
+def run_overlap_bench(hs, dev, steps=8, reps=3):
     """Workload 4 (128 requests, contexts 16K-128K, 90 % reuse): decode steps
-    of swap-in + attention, serial (one swap-in, then the attention) against
-    overlapped (requests in two halves: the second half's swap-in runs while
-    the first half's rows are attended on another stream). Both run on their
-    own empty hot buffer and must give the same output bit for bit."""
+    of swap-in + attention, serial (hs_swap_in, then hs_sparse_attn_decode,
+    on one stream) against hs_swap_in_attn_decode (the library's row groups:
+    the copies of each next group run beside the attention of the groups
+    before it, one copy block per SM next to an attention block). Each
+    variant runs its steps on its own empty hot buffer, the two alternating,
+    `reps` times; steady = mean of steps 1.. (step 0 fills the empty buffer);
+    spread = range of a variant's steady times over the repetitions. The
+    outputs must agree bit for bit at every step."""
     cfg = W.get_config(4)
     req, ri = W.rows_of(cfg)
     clen = W.causal_lengths(cfg.L, req, ri)
@@ -776,25 +780,14 @@ def run_overlap_bench(hs, dev, steps=8):
     sets = [W.locality_sets(cfg, cfg.L[r], r, steps) for r in range(cfg.B)]
     topks = [torch.as_tensor(W.topk_shared_sets(cfg, sets, st), device=dev) for st in range(steps)]
     t_req, t_clen = torch.as_tensor(req, device=dev), torch.as_tensor(clen, device=dev)
-    # the first part: whole requests filling whole attention waves (one wave =
-    # one row per two-SM cluster slot), so that splitting adds no wave
-    slots = torch.cuda.get_device_properties(dev).multi_processor_count // 2
-    rows_per_req = cfg.d + 1
-    waves = (cfg.R + slots - 1) // slots
-    half = max(1, (waves + 1) // 2) * slots
-    half -= half % rows_per_req
-    half = min(half, cfg.R - rows_per_req)
-    assert (req[:half] < req[half]).all() and (req[half:] >= req[half]).all()
+    groups = hs.hs_step_groups(cfg.R, cfg.H)
     q = W.step_q(cfg, 0, device=dev)
     out_s = torch.empty((cfg.R, cfg.H, 512), dtype=torch.bfloat16, device=dev)
-    out_o = torch.empty_like(out_s)
+    out_f = torch.empty_like(out_s)
     idx_s = torch.empty((cfg.R, cfg.K), dtype=torch.int32, device=dev)
-    idx_o = torch.empty_like(idx_s)
-    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
-    e_swap = [torch.cuda.Event() for _ in range(2)]
-    e_done = torch.cuda.Event()
+    idx_f = torch.empty_like(idx_s)
+    s1 = torch.cuda.Stream()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-
     e_mid = torch.cuda.Event(enable_timing=True)
 
     def serial(buf, st):
@@ -802,16 +795,9 @@ def run_overlap_bench(hs, dev, steps=8):
         e_mid.record(s1)
         hs.hs_sparse_attn_decode(q, hb["hot"], idx_s, cfg.scale, out_s, stream=s1)
 
-    def overlapped(buf, st):
-        for k, (r0, r1) in enumerate(((0, half), (half, cfg.R))):
-            hs.hs_swap_in(buf, t_req[r0:r1], t_clen[r0:r1], hb["kv_len"], topks[st][r0:r1],
-                          idx_o[r0:r1], stream=s1)
-            e_swap[k].record(s1)
-            s2.wait_event(e_swap[k])
-            hs.hs_sparse_attn_decode(q[r0:r1], hot2, idx_o[r0:r1], cfg.scale, out_o[r0:r1],
-                                     stream=s2)
-        e_done.record(s2)
-        s1.wait_event(e_done)
+    def fused(buf, st):
+        hs.hs_swap_in_attn_decode(buf, t_req, t_clen, hb["kv_len"], topks[st], q, cfg.scale,
+                                  idx_f, out_f, stream=s1)
 
     # one untimed pass first: the first touch of the freshly pinned 10.9 GB
     # host pool made the first variant's steps slow and erratic on some boxes
@@ -821,41 +807,51 @@ def run_overlap_bench(hs, dev, steps=8):
         serial(buf, st)
     torch.cuda.synchronize()
     buf.close()
-    res, attn_serial = {}, []
-    variants = [("serial", serial, hb["hot"], 0)] + \
-        [(f"overlapped_copy_sms_{n}" if n else "overlapped", overlapped, hot2, n) for n in (0, 24)]
-    for name, fn, hot, n_sms in variants:
-        buf = hs.HsBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hot,
-                          hb["pool"], hb["hbt"])
-        hs.hs_buffer_set_copy_sms(buf, n_sms)
-        ms = []
-        for st in range(steps):
-            _lead(s1)
-            a.record(s1)
-            fn(buf, st)
-            b.record(s1)
-            b.synchronize()
-            ms.append(a.elapsed_time(b))
-            if fn is serial:
-                attn_serial.append(e_mid.elapsed_time(b))
-        res[name] = {"ms_per_step": [round(x, 4) for x in ms],
-                     "steady_ms": round(statistics.mean(ms[1:]), 4),
-                     "status": hs.hs_get_status(buf)}
-        buf.close()
-        torch.cuda.synchronize()
-        if fn is overlapped and not torch.equal(out_s.view(torch.int16), out_o.view(torch.int16)):
-            raise RuntimeError("overlapped decode step differs from the serial one")
-    res["serial"]["attn_roofline"] = _attn_roofline(
-        [int((topks[st] >= 0).sum().item()) for st in range(1, steps)], attn_serial[1:], cfg.R, cfg.H,
-        cfg.K)
+    runs = {"serial": [], "fused": []}
+    attn_serial, status = [], 0
+    for rep in range(reps):
+        ref = []   # the serial step's slot table and output, per step
+        for name, fn, hot in (("serial", serial, hb["hot"]), ("fused", fused, hot2)):
+            buf = hs.HsBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hot,
+                              hb["pool"], hb["hbt"])
+            ms = []
+            for st in range(steps):
+                _lead(s1)
+                a.record(s1)
+                fn(buf, st)
+                b.record(s1)
+                b.synchronize()
+                ms.append(a.elapsed_time(b))
+                if fn is serial:
+                    ref.append((idx_s.clone(), out_s.clone()))
+                    if rep == 0:
+                        attn_serial.append(e_mid.elapsed_time(b))
+                elif not (torch.equal(idx_f, ref[st][0]) and
+                          torch.equal(out_f.view(torch.int16), ref[st][1].view(torch.int16))):
+                    raise RuntimeError(f"hs_swap_in_attn_decode differs from the serial step {st}")
+            runs[name].append(ms)
+            status |= hs.hs_get_status(buf)
+            buf.close()
+        del ref
     del hb, hot2
-    ser = res["serial"]["steady_ms"]
-    best = min((k for k in res if k != "serial"), key=lambda k: res[k]["steady_ms"])
-    return {"workload": cfg.name, "rows": cfg.R, "first_part_rows": half, "variants": res,
-            "best_overlapped": best,
+    res = {}
+    for name, rr in runs.items():
+        steady = [statistics.mean(ms[1:]) for ms in rr]
+        res[name] = {"ms_per_step": [[round(x, 4) for x in ms] for ms in rr],
+                     "steady_ms": round(statistics.mean(steady), 4),
+                     "steady_ms_per_rep": [round(x, 4) for x in steady],
+                     "spread_ms": round(max(steady) - min(steady), 4)}
+    res["serial"]["attn_roofline"] = _attn_roofline(
+        [int((topks[st] >= 0).sum().item()) for st in range(1, steps)], attn_serial[1:], cfg.R,
+        cfg.H, cfg.K)
+    ser, fus = res["serial"]["steady_ms"], res["fused"]["steady_ms"]
+    return {"workload": cfg.name, "rows": cfg.R, "group_row_end": groups, "variants": res,
             "query_rows_per_s_serial": round(cfg.R / (ser * 1e-3), 1),
-            "query_rows_per_s_best": round(cfg.R / (min(ser, res[best]["steady_ms"]) * 1e-3), 1),
-            "speedup": round(ser / res[best]["steady_ms"], 3)}
+            "query_rows_per_s_fused": round(cfg.R / (fus * 1e-3), 1),
+            "speedup": round(ser / fus, 3),
+            "margin_ms": round(ser - fus, 4),
+            "spread_ms": max(res["serial"]["spread_ms"], res["fused"]["spread_ms"]),
+            "bit_identical": True, "status": status}
 
 
 def run_backup_bench(hs, dev, layers=4, pages=512, block_rows=64):

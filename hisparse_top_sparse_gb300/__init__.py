@@ -39,7 +39,7 @@ EXPORTS = (
     "hs_swap_in", "hs_sparse_attn_decode", "hs_verify_finalize", "hs_read_probe", "hs_wait_probe",
     "hs_verify_accept_noalloc", "hs_swap_apply_plan", "hs_backup_pages", "hs_reclaim_resident",
     "hs_sparse_attn_decode_mixed", "hs_backup_rows", "hs_backup_indexer",
-    "hs_buffer_set_copy_sms",
+    "hs_buffer_set_copy_sms", "hs_swap_in_attn_decode", "hs_step_groups",
 )
 
 
@@ -89,6 +89,9 @@ def lib() -> ctypes.CDLL:
                                            _P, _P, _P, _P]),
             "hs_sparse_attn_decode_mixed": (_I, [_P, _P, _I64, _P, _I64, _P, _P, _I, _P, _I, _I,
                                                  _I, ctypes.c_float, _P, _P, _P, _P]),
+            "hs_swap_in_attn_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _I, ctypes.c_float,
+                                            _I, _P, _P, _P, _P, _P, _P, _P]),
+            "hs_step_groups": (_I, [_I, _I, _P, _P]),
             "hs_reclaim_resident": (_I, [_P, _I, _I, _P, _I, _P, _P, _P, _P]),
             "hs_verify_finalize": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
             "hs_read_probe": (_I, [_P, ctypes.c_size_t, _P, _I, _P]),
@@ -261,6 +264,45 @@ def hs_sparse_attn_decode(q, kv, idx, scale: float, out, lse=None, status=None,
         _ptr(lse, "lse", torch.float32, (R, H), allow_none=True),
         _ptr(status, "status", torch.int32, (1,), allow_none=True),
         _stream(stream)), "hs_sparse_attn_decode")
+
+
+def hs_swap_in_attn_decode(buf: HsBuffer, req_id_per_row, row_causal_len, kv_len, topk, q,
+                           scale: float, out_slot_idx, out, groups=None, out_valid=None,
+                           lse=None, stats=None, stream=None) -> None:
+    """hs_swap_in followed by hs_sparse_attn_decode over buf's hot cache, the
+    copies of later row groups overlapped with the attention of earlier ones.
+    groups: None (the library's split) or the end row of each group."""
+    R, K = topk.shape
+    Rq, H, D = q.shape
+    if D != LATENT_DIM or Rq != R:
+        raise ValueError("q must be [R][H][576]")
+    ends = None
+    if groups is not None:
+        groups = [int(x) for x in groups]
+        ends = (ctypes.c_int32 * max(1, len(groups)))(*groups)
+    _check(lib().hs_swap_in_attn_decode(
+        buf.handle,
+        _ptr(req_id_per_row, "req_id_per_row", torch.int32, (R,)),
+        _ptr(row_causal_len, "row_causal_len", torch.int32, (R,)),
+        _ptr(kv_len, "kv_len", torch.int32, (buf.max_reqs,)),
+        _ptr(topk, "topk", torch.int32), R, K,
+        _ptr(q, "q", torch.bfloat16), H, float(scale),
+        len(groups) if groups is not None else 0,
+        ctypes.cast(ends, ctypes.c_void_p) if ends is not None else None,
+        _ptr(out_slot_idx, "out_slot_idx", torch.int32, (R, K)),
+        _ptr(out_valid, "out_valid", torch.int32, (R,), allow_none=True),
+        _ptr(out, "out", torch.bfloat16, (R, H, VALUE_DIM)),
+        _ptr(lse, "lse", torch.float32, (R, H), allow_none=True),
+        _ptr(stats, "stats", torch.int64, (2,), allow_none=True),
+        _stream(stream)), "hs_swap_in_attn_decode")
+
+
+def hs_step_groups(R: int, H: int) -> list:
+    """End rows of the groups hs_swap_in_attn_decode picks on the current device."""
+    n = ctypes.c_int32(0)
+    ends = (ctypes.c_int32 * 8)()
+    _check(lib().hs_step_groups(int(R), int(H), ctypes.byref(n), ends), "hs_step_groups")
+    return [int(ends[i]) for i in range(n.value)]
 
 
 def hs_sparse_attn_decode_mixed(q, kv_resident, kv_hot, row_req, fully_resident, idx,

@@ -66,9 +66,16 @@ static void free_buffer(hs_buffer *b) {
   if (!b) return;
   void *ptrs[] = {b->token_slot, b->slot_token, b->slot_ts, b->lru_order, b->pos_mark,
                   b->copy_desc,  b->copy_cnt,   b->pred,    b->row_count, b->verify_claim,
-                  b->status};
+                  b->req_group,  b->status};
   for (void *p : ptrs)
     if (p) cudaFree(p);
+  for (cudaStream_t &st : b->side)
+    if (st) cudaStreamDestroy(st);
+  if (b->ev_fork) cudaEventDestroy(b->ev_fork);
+  for (cudaEvent_t &e : b->ev_gather)
+    if (e) cudaEventDestroy(e);
+  for (cudaEvent_t &e : b->ev_join)
+    if (e) cudaEventDestroy(e);
   free(b);
 }
 
@@ -145,6 +152,7 @@ extern "C" int hs_buffer_create(const hs_buffer_desc *d, hs_buffer **out) {
       {(void **)&b->pred, R * (size_t)d->step_slots * 4, 0},
       {(void **)&b->row_count, R * 4, 0},
       {(void **)&b->verify_claim, R * 4, 0},
+      {(void **)&b->req_group, R * 4, 0xFF},
       {(void **)&b->status, 4, 0},
   };
   for (auto &e : plan) {
@@ -154,6 +162,22 @@ extern "C" int hs_buffer_create(const hs_buffer_desc *d, hs_buffer **out) {
       free_buffer(b);
       return hs_set_error(HS_ERR_CUDA, "allocating %zu bytes of buffer metadata: %s",
                           e.bytes, cudaGetErrorString(err));
+    }
+  }
+  // the side streams and events of hs_swap_in_attn_decode
+  {
+    cudaError_t err = cudaSuccess;
+    for (cudaStream_t &st : b->side)
+      if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&b->ev_fork, cudaEventDisableTiming);
+    for (cudaEvent_t &e : b->ev_gather)
+      if (err == cudaSuccess) err = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+    for (cudaEvent_t &e : b->ev_join)
+      if (err == cudaSuccess) err = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+    if (err != cudaSuccess) {
+      free_buffer(b);
+      return hs_set_error(HS_ERR_CUDA, "creating the buffer's streams and events: %s",
+                          cudaGetErrorString(err));
     }
   }
   k_order_init<<<(int)std::min<size_t>(R * S / 256 + 1, 65535), 256>>>(b->lru_order, b->S,

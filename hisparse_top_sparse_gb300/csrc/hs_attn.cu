@@ -86,10 +86,14 @@ constexpr int XS_OFF = VO_OFF + VO_SLOTS * V_SLOT_BYTES;    // own P staged for 
 constexpr int XP_OFF = XS_OFF + XP_SLOTS * P_SLOT_BYTES;    // the peer's P
 constexpr int VP_OFF = XP_OFF + XP_SLOTS * P_SLOT_BYTES;
 constexpr int XMAX_OFF = VP_OFF + VP_SLOTS * V_SLOT_BYTES;  // peer's first-tile maxima
-constexpr int XEND_OFF = XMAX_OFF + HG * 4;                 // peer's (l, max, flag) per pass
-constexpr int BAR_OFF = XEND_OFF + 2 * HG * 16;
+constexpr int XEND_OFF = XMAX_OFF + HG * 4;                 // peer's (l or mark, max) per pass
+constexpr int BAR_OFF = XEND_OFF + 2 * HG * 8;
 constexpr int SMEM_USED = BAR_OFF + 512;
-constexpr int SMEM_ALLOC = SMEM_USED + 1024;                // slack for the 1 KB alignment
+// 1 KB of slack to align the base to 1024 bytes (the 128-byte swizzled tiles
+// need it) at run time; declaring the alignment instead gave slower code. The
+// SM keeps 3 KB of shared memory beside one CTA for a small kernel (the
+// swap-in gather).
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 static_assert(RA_OFF % 1024 == 0 && VO_OFF % 1024 == 0 && VP_OFF % 1024 == 0 &&
                   XS_OFF % 1024 == 0 && XP_OFF % 1024 == 0, "slot alignment");
@@ -308,14 +312,12 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
                    : "memory");
 }
-// 16 / 4 bytes into the peer's shared memory; the peer's mbarrier `rbar`
+// 8 / 4 bytes into the peer's shared memory; the peer's mbarrier `rbar`
 // counts the bytes when they land
-__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                            uint32_t d, uint32_t rbar) {
+__device__ __forceinline__ void st_async_v2(uint32_t addr, uint32_t a, uint32_t b, uint32_t rbar) {
   asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(
-          addr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar)
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];\n" ::"r"(addr),
+      "r"(a), "r"(b), "r"(rbar)
       : "memory");
 }
 __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t rbar) {
@@ -662,7 +664,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     };
     if (tid == 0) arrive_expect_tx(bar(B_XMAX), HG * 4);
     for (int pass = 0; pass < 2 && !timed_out; ++pass) {
-      if (tid == 0) arrive_expect_tx(bar(B_XEND + pass), HG * 16);
+      if (tid == 0) arrive_expect_tx(bar(B_XEND + pass), HG * 8);
       int32_t my_id = load_id(c);
       for (int il = 0; il < n_own; ++il, ++ig) {
         const int t = 2 * il + c;
@@ -733,14 +735,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (pass == 0 && n_own == 0 && !agree_ref(-INFINITY)) { timed_out = true; break; }
 
       // end of pass: (l, running max, flag) to the peer, the peer's back
-      st_async_v4(peer_addr(sbase + XEND_OFF + pass * HG * 16, peer) + hrow * 16, __float_as_uint(l),
-                  __float_as_uint(m_ex), flag ? 1u : 0u, 0u, peer_addr(bar(B_XEND + pass), peer));
+      // l < 0 carries a mark for a second pass (only the first pass marks)
+      st_async_v2(peer_addr(sbase + XEND_OFF + pass * HG * 8, peer) + hrow * 8,
+                  __float_as_uint(pass == 0 && flag ? -1.f : l), __float_as_uint(m_ex),
+                  peer_addr(bar(B_XEND + pass), peer));
       if (!warp_wait_cluster(bar(B_XEND + pass), 0)) { timed_out = true; break; }
       const volatile uint32_t *pe =
-          reinterpret_cast<const volatile uint32_t *>(sm + XEND_OFF + pass * HG * 16) + hrow * 4;
+          reinterpret_cast<const volatile uint32_t *>(sm + XEND_OFF + pass * HG * 8) + hrow * 2;
       l_peer = __uint_as_float(pe[0]);
       const float m_peer = __uint_as_float(pe[1]);
-      const bool f_peer = pe[2] != 0u;
+      const bool f_peer = pass == 0 && l_peer < 0.f;
       last_pass = pass;
       if (pass == 1) break;
       // second pass iff any head of either CTA was marked
@@ -831,6 +835,46 @@ extern "C" int hs_wait_probe(uint32_t *status, int64_t max_cycles, hs_stream_t s
   return HS_OK;
 }
 
+static int set_attn_attributes() {
+  int dev = 0;
+  HS_CUDA_TRY(cudaGetDevice(&dev));
+  static bool attr_done[64] = {false};
+  if (dev >= 64 || !attr_done[dev]) {
+    HS_CUDA_TRY(cudaFuncSetAttribute(k_attn_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_ALLOC));
+    if (dev < 64) attr_done[dev] = true;
+  }
+  return HS_OK;
+}
+
+int hs_attn_wave_rows(int32_t H, int32_t *rows) {
+  int rc = set_attn_attributes();
+  if (rc) return rc;
+  int dev = 0;
+  HS_CUDA_TRY(cudaGetDevice(&dev));
+  static int clusters[64] = {0};
+  int n = dev < 64 ? clusters[dev] : 0;
+  if (n == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    HS_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, k_attn_pair, &cfg));
+    if (n < 1) n = 1;
+    if (dev < 64) clusters[dev] = n;
+  }
+  const int per_row = (H + HG - 1) / HG;
+  *rows = n / per_row > 0 ? n / per_row : 1;
+  return HS_OK;
+}
+
 extern "C" int hs_sparse_attn_decode_mixed(const void *q, const void *kv_resident,
                                            int64_t n_resident, const void *kv_hot, int64_t n_hot,
                                            const int32_t *row_req, const int32_t *fully_resident,
@@ -838,6 +882,15 @@ extern "C" int hs_sparse_attn_decode_mixed(const void *q, const void *kv_residen
                                            int32_t H, int32_t K,
                                            float scale, void *out, float *lse, uint32_t *status,
                                            hs_stream_t stream) {
+  return hs_attn_launch(q, kv_resident, n_resident, kv_hot, n_hot, row_req, fully_resident,
+                        n_reqs, idx, R, H, K, scale, out, lse, status, true, stream);
+}
+
+int hs_attn_launch(const void *q, const void *kv_resident, int64_t n_resident, const void *kv_hot,
+                   int64_t n_hot, const int32_t *row_req, const int32_t *fully_resident,
+                   int32_t n_reqs, const int32_t *idx, int32_t R, int32_t H, int32_t K,
+                   float scale, void *out, float *lse, uint32_t *status, bool pdl,
+                   cudaStream_t stream) {
   if (R < 0 || H < 1 || H > 1024 || K < 0 || n_resident < 0 || n_hot < 0 ||
       (fully_resident && n_reqs < 0))
     return hs_set_error(HS_ERR_INVALID_ARG, "bad sizes R=%d H=%d (1..1024) K=%d n_kv=%lld/%lld",
@@ -850,14 +903,8 @@ extern "C" int hs_sparse_attn_decode_mixed(const void *q, const void *kv_residen
       ((uintptr_t)out & 15))
     return hs_set_error(HS_ERR_INVALID_ARG, "q, kv and out must be 16-byte aligned");
   if (!(scale == scale)) return hs_set_error(HS_ERR_INVALID_ARG, "scale is NaN");
-  int dev = 0;
-  HS_CUDA_TRY(cudaGetDevice(&dev));
-  static bool attr_done[64] = {false};
-  if (dev >= 64 || !attr_done[dev]) {
-    HS_CUDA_TRY(cudaFuncSetAttribute(k_attn_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_ALLOC));
-    if (dev < 64) attr_done[dev] = true;
-  }
+  int rc = set_attn_attributes();
+  if (rc) return rc;
   const int64_t blocks = (int64_t)R * ((H + HG - 1) / HG) * 2;
   if (blocks > INT32_MAX) return hs_set_error(HS_ERR_UNSUPPORTED, "R*H too large");
   // q as a [R][H][576] bf16 tensor for the prologue's tensor copies
@@ -892,7 +939,7 @@ extern "C" int hs_sparse_attn_decode_mixed(const void *q, const void *kv_residen
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   HS_CUDA_TRY(cudaLaunchKernelEx(
       &cfg, k_attn_pair, tmap, reinterpret_cast<const char *>(q),
       reinterpret_cast<const char *>(kv_resident), n_resident,

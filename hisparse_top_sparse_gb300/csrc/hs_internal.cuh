@@ -14,6 +14,8 @@
 #define HS_MAX_STEP 16
 #define HS_MAX_REQS 16384                  // requests per buffer (swap-in gather prefix in SMEM)
 #define HS_MAX_LAYERS 64                   // caches per hs_swap_apply_plan / hs_backup_pages call
+#define HS_MAX_GROUPS 8                    // request groups of one hs_swap_in_attn_decode call
+#define HS_SIDE_STREAMS 3                  // one for the gathers, two for the attention launches
 
 // Host-side state of a hot buffer. Device arrays are owned by the library.
 struct hs_buffer {
@@ -37,7 +39,12 @@ struct hs_buffer {
   int32_t *pred;         // [max_reqs*n_step] argmax per verify row
   int32_t *row_count;    // [max_reqs] verify rows done per request in a call (0 between calls)
   uint32_t *verify_claim; // [max_reqs]: low 32 bits of the clock of the last commit of a request
+  int32_t *req_group;    // [max_reqs]: group of the request's first row in the latest swap-in
   uint32_t *status;      // device status word
+
+  // streams and events of hs_swap_in_attn_decode (created with the buffer)
+  cudaStream_t side[HS_SIDE_STREAMS];
+  cudaEvent_t ev_fork, ev_gather[HS_MAX_GROUPS], ev_join[HS_SIDE_STREAMS];
 
   int64_t clock;         // LRU clock: swap-in and commit calls made so far
   int32_t copy_sms;      // SMs the copy kernels may spread over (0 = all)
@@ -122,6 +129,40 @@ __device__ __forceinline__ void hs_lru_reorder(const int32_t *order, const uint3
   }
 }
 int hs_check_buffer(const hs_buffer *buf);
+
+// ---- launchers shared by hs_swap_in and hs_swap_in_attn_decode (hs_swap.cu)
+
+// The metadata kernel over rows [0, R) of a call. Rows [group_end[g-1],
+// group_end[g]) form group g (n_groups >= 1, group_end ascending, the last
+// = R); each request's first-row group goes to buf->req_group. The caller
+// advances buf->clock first.
+int hs_swap_plan_launch(hs_buffer *buf, const int32_t *req_id_per_row,
+                        const int32_t *row_causal_len, const int32_t *kv_len, const int32_t *topk,
+                        int32_t R, int32_t K, int32_t n_groups, const int32_t *group_end,
+                        int32_t *out_slot_idx, int32_t *out_valid, int64_t *stats,
+                        cudaStream_t stream);
+// The copies of the misses of group g's requests (those whose first row lies
+// in group g) and the slot table of rows [row_lo, row_hi). ctas_per_sm
+// blocks per SM of the buffer's copy SMs; pdl: a programmatic dependent launch
+// of the kernel before it in the stream.
+int hs_swap_gather_launch(hs_buffer *buf, const int32_t *req_id_per_row,
+                          const int32_t *row_causal_len, const int32_t *kv_len,
+                          const int32_t *topk, int32_t R, int32_t K, int32_t g, int32_t row_lo,
+                          int32_t row_hi, int32_t *out_slot_idx, int32_t *out_valid,
+                          int ctas_per_sm, bool pdl, cudaStream_t stream);
+
+// ---- attention launcher (hs_attn.cu) ----------------------------------------
+
+// hs_sparse_attn_decode_mixed with the launch made a programmatic dependent
+// one (pdl) or a plain one.
+int hs_attn_launch(const void *q, const void *kv_resident, int64_t n_resident, const void *kv_hot,
+                   int64_t n_hot, const int32_t *row_req, const int32_t *fully_resident,
+                   int32_t n_reqs, const int32_t *idx, int32_t R, int32_t H, int32_t K,
+                   float scale, void *out, float *lse, uint32_t *status, bool pdl,
+                   cudaStream_t stream);
+// Rows of H heads that one wave of the attention kernel holds on the current
+// device (two-SM clusters resident at once, per row's head groups); >= 1.
+int hs_attn_wave_rows(int32_t H, int32_t *rows);
 
 // ---- argmax of one logits row (greedy verify) -------------------------------
 

@@ -1,0 +1,150 @@
+// hs_swap_in_attn_decode: the swap-in and the sparse attention of one decode
+// step in one call, with the host reads of later request groups overlapped
+// with the attention of earlier ones.
+//
+// "hiSparse-MTP", section 1 (HiSparseCoordinator.__init__): the coordinator
+// owns an asynchronous stream beside the compute stream for its copies.
+// "vllm 分析(十二) HiSparse 下篇", HiSparseCacheHandle.resolve_topk: a step's
+// rows go through swap_in, then attend over the hot cache with the indices it
+// returns. The call keeps that order per request and overlaps across them.
+//
+// Schedule, rows split into groups (row ranges; a request belongs to the group
+// of its first row, so any row order is correct):
+//   stream   k_swap_request (every row)  ->  gather of group 0 (every SM, 8
+//            blocks each)  ->  attention of group 0
+//   side 0   gather of group 1, 2, ... (one block per SM), an event after each
+//   side 1/2 attention of group g >= 1 after its gather's event, alternating
+//            between two streams so that a group's attention fills the SMs the
+//            previous group's last wave leaves idle
+// A gather block (256 threads, 51 registers, 144 + 4 * (max_reqs + 1) bytes of
+// shared memory) fits on an SM beside one attention CTA (448 threads, 93
+// registers, 229,376 bytes; the SM keeps 3 KB) for up to 448 requests, so the
+// later gathers take no SM away from the attention. The caller's stream waits
+// for every side stream before the call returns.
+
+#include <algorithm>
+
+#include "hs_internal.cuh"
+
+namespace {
+
+// Rows [ends[g-1], ends[g]) of the automatic split: the first group one
+// attention wave (its copies are the only ones not hidden), the other rows in
+// at most HS_MAX_GROUPS - 1 groups of equal size, a whole number of waves
+// (the last takes what is left). Small groups keep the copies of the next
+// group short, so the attention rarely waits for them.
+int auto_groups(int32_t R, int32_t H, int32_t *n, int32_t *ends) {
+  int32_t wave = 1;
+  int rc = hs_attn_wave_rows(H, &wave);
+  if (rc) return rc;
+  int g = 0;
+  ends[g++] = std::min(R, wave);
+  const int64_t rest = (int64_t)R - ends[0];
+  if (rest > 0) {
+    const int64_t waves = (rest + wave - 1) / wave;
+    const int64_t groups = std::min<int64_t>(HS_MAX_GROUPS - 1, waves);
+    const int64_t size = (waves + groups - 1) / groups * wave;
+    int64_t end = ends[0];
+    while (end < R) {
+      end = std::min<int64_t>(R, end + size);
+      ends[g++] = (int32_t)end;
+    }
+  }
+  *n = g;
+  return HS_OK;
+}
+
+}  // namespace
+
+extern "C" int hs_step_groups(int32_t R, int32_t H, int32_t *n_groups, int32_t *group_row_end) {
+  if (R < 0 || H < 1 || H > 1024 || !n_groups || !group_row_end)
+    return hs_set_error(HS_ERR_INVALID_ARG, "bad arguments R=%d H=%d", R, H);
+  *n_groups = 0;
+  if (R == 0) return HS_OK;
+  return auto_groups(R, H, n_groups, group_row_end);
+}
+
+extern "C" int hs_swap_in_attn_decode(hs_buffer *buf, const int32_t *req_id_per_row,
+                                      const int32_t *row_causal_len, const int32_t *kv_len,
+                                      const int32_t *topk, int32_t R, int32_t K, const void *q,
+                                      int32_t H, float scale, int32_t n_groups,
+                                      const int32_t *group_row_end, int32_t *out_slot_idx,
+                                      int32_t *out_valid, void *out, float *lse, int64_t *stats,
+                                      hs_stream_t stream) {
+  int rc = hs_check_buffer(buf);
+  if (rc) return rc;
+  if (R < 0 || K < 0 || K > (1 << 20) || H < 1 || H > 1024)
+    return hs_set_error(HS_ERR_INVALID_ARG, "bad sizes R=%d K=%d (0..2^20) H=%d (1..1024)", R,
+                        K, H);
+  if (R > 0 && (!req_id_per_row || !row_causal_len || !kv_len || !q || !out))
+    return hs_set_error(HS_ERR_INVALID_ARG, "NULL row descriptor, q or out");
+  if (R > 0 && K > 0 && (!topk || !out_slot_idx))
+    return hs_set_error(HS_ERR_INVALID_ARG, "NULL topk or out_slot_idx");
+  if (((uintptr_t)q & 15) || ((uintptr_t)out & 15))
+    return hs_set_error(HS_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  if (!(scale == scale)) return hs_set_error(HS_ERR_INVALID_ARG, "scale is NaN");
+  int32_t ends[HS_MAX_GROUPS];
+  int G = n_groups;
+  if (n_groups < 0 || n_groups > HS_MAX_GROUPS || (n_groups > 0 && !group_row_end))
+    return hs_set_error(HS_ERR_INVALID_ARG, "n_groups %d (0..%d) or group_row_end NULL",
+                        n_groups, HS_MAX_GROUPS);
+  for (int g = 0; g < n_groups; ++g) {
+    ends[g] = group_row_end[g];
+    if (ends[g] <= (g ? ends[g - 1] : 0) || (g == n_groups - 1 && ends[g] != R))
+      return hs_set_error(HS_ERR_INVALID_ARG,
+                          "group_row_end must rise strictly from above 0 to R = %d", R);
+  }
+
+  buf->clock += 1;  // one swap-in: the LRU clock advances once, as in hs_swap_in
+  if (R == 0) return HS_OK;
+  if (G == 0) {
+    rc = auto_groups(R, H, &G, ends);
+    if (rc) return rc;
+  }
+  rc = hs_swap_plan_launch(buf, req_id_per_row, row_causal_len, kv_len, topk, R, K, G, ends,
+                           out_slot_idx, out_valid, stats, stream);
+  if (rc) return rc;
+  rc = hs_swap_gather_launch(buf, req_id_per_row, row_causal_len, kv_len, topk, R, K, 0, 0,
+                             ends[0], out_slot_idx, out_valid, 8, true, stream);
+  if (rc) return rc;
+
+  const int64_t n_hot = (int64_t)buf->max_reqs * buf->S_tot;
+  auto attend = [&](int g, cudaStream_t st, bool pdl) -> int {
+    const int32_t lo = g ? ends[g - 1] : 0, n = ends[g] - lo;
+    return hs_attn_launch(static_cast<const char *>(q) + (int64_t)lo * H * HS_ROW_BYTES,
+                          buf->hot_kv, n_hot, nullptr, 0, nullptr, nullptr, 0,
+                          out_slot_idx ? out_slot_idx + (int64_t)lo * K : nullptr, n, H, K,
+                          scale, static_cast<char *>(out) + (int64_t)lo * H * 512 * 2,
+                          lse ? lse + (int64_t)lo * H : nullptr, buf->status, pdl, st);
+  };
+  if (G > 1) {
+    HS_CUDA_TRY(cudaEventRecord(buf->ev_fork, stream));
+    HS_CUDA_TRY(cudaStreamWaitEvent(buf->side[0], buf->ev_fork, 0));
+    for (int g = 1; g < G; ++g) {
+      rc = hs_swap_gather_launch(buf, req_id_per_row, row_causal_len, kv_len, topk, R, K, g,
+                                 ends[g - 1], ends[g], out_slot_idx, out_valid, 1, false,
+                                 buf->side[0]);
+      if (rc) return rc;
+      HS_CUDA_TRY(cudaEventRecord(buf->ev_gather[g], buf->side[0]));
+    }
+  }
+  // a programmatic dependent launch of the first gather: its prologue runs
+  // while that gather finishes
+  rc = attend(0, stream, true);
+  if (rc) return rc;
+  if (G == 1) return HS_OK;
+  bool used[HS_SIDE_STREAMS] = {true, false, false};
+  for (int g = 1; g < G; ++g) {
+    const int s = 1 + (g - 1) % 2;
+    used[s] = true;
+    HS_CUDA_TRY(cudaStreamWaitEvent(buf->side[s], buf->ev_gather[g], 0));
+    rc = attend(g, buf->side[s], false);
+    if (rc) return rc;
+  }
+  for (int s = 0; s < HS_SIDE_STREAMS; ++s) {
+    if (!used[s]) continue;
+    HS_CUDA_TRY(cudaEventRecord(buf->ev_join[s], buf->side[s]));
+    HS_CUDA_TRY(cudaStreamWaitEvent(stream, buf->ev_join[s], 0));
+  }
+  return HS_OK;
+}

@@ -63,6 +63,9 @@ struct SwapArgs {
   uint32_t *status;
   uint32_t epoch;
   int64_t now;
+  int32_t *req_group;                 // [max_reqs]: group of the request's first row
+  int32_t n_groups;
+  int32_t group_end[HS_MAX_GROUPS];   // rows [group_end[g-1], group_end[g]) form group g
 };
 
 // In-place ascending bitonic sort of n (a power of two) keys in shared memory.
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
   uint32_t *pbm = reinterpret_cast<uint32_t *>(rvalid + ROW_CHUNK);
   int32_t *pwp = reinterpret_cast<int32_t *>(pbm + nW);
   uint32_t *pneed = reinterpret_cast<uint32_t *>(pwp + nW);
-  __shared__ int s_need, s_miss, s_cnt, s_any, s_bad;
+  __shared__ int s_need, s_miss, s_cnt, s_any, s_bad, s_first;
   __shared__ int scan_tmp[33];
   const int lane = threadIdx.x & 31;
 
@@ -234,7 +237,10 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
     const int n = collect_rows(a, b, from, rows, &next, &s_cnt);
     from = next;
     if (n == 0) break;
-    if (threadIdx.x == 0) s_any = 1;
+    if (threadIdx.x == 0) {
+      if (!s_any) s_first = rows[0];   // rows come in ascending order
+      s_any = 1;
+    }
     if (out_valid)   // counted by the gather's table pass
       for (int i = threadIdx.x; i < n; i += SW_THREADS) out_valid[rows[i]] = 0;
     const int items = n * a.K;
@@ -298,7 +304,12 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
   }
   __syncthreads();
   if (!s_any) return;                    // no rows of this request in the call
-  if (threadIdx.x == 0 && s_bad) atomicOr(a.status, HS_STATUS_INDEX);
+  if (threadIdx.x == 0) {
+    if (s_bad) atomicOr(a.status, HS_STATUS_INDEX);
+    int g = 0;
+    while (g < a.n_groups - 1 && s_first >= a.group_end[g]) ++g;
+    a.req_group[b] = g;                  // its misses are copied with group g
+  }
 
   // ---- assign ---------------------------------------------------------------
   for (int w = threadIdx.x; w < (a.S + 31) / 32; w += SW_THREADS) {
@@ -435,7 +446,8 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
 // Arguments of the slot-table pass run inside the gather.
 struct TableArgs {
   const int32_t *req_id, *clen, *kv_len, *topk, *token_slot, *copy_cnt;
-  int32_t R, K, max_reqs, S, S_tot, max_ctx;
+  int32_t row_lo, n_rows;   // the rows whose entries this launch writes
+  int32_t K, max_reqs, S, S_tot, max_ctx;
   int32_t *out, *out_valid;
   uint32_t *status;
 };
@@ -466,53 +478,45 @@ __device__ __forceinline__ void table_entry(const TableArgs &ta, int64_t e) {
   if (v >= 0 && ta.out_valid) atomicAdd(&ta.out_valid[r], 1);
 }
 
-// Chunks of every request's misses are numbered consecutively (a prefix sum
+// The copies of the requests of group `group` (req_group, written by
+// k_swap_request) and the slot-table entries of rows [row_lo, row_lo + n_rows).
+// Chunks of those requests' misses are numbered consecutively (a prefix sum
 // over the per-request counts, computed by every block in shared memory) and
 // spread over the whole grid, four 16-byte loads in flight per thread; the
 // slot table's entries are spread the same way and worked on while the
 // loads over the host link are in flight.
 __global__ void __launch_bounds__(256) k_swap_gather(const int32_t *__restrict__ copy_cnt,
+                                                     const int32_t *__restrict__ req_group,
+                                                     int32_t group,
                                                      const uint64_t *__restrict__ copy_desc,
                                                      int32_t max_reqs, int32_t S, int32_t S_tot,
                                                      const uint4 *__restrict__ pool,
                                                      uint4 *__restrict__ hot, TableArgs ta) {
   extern __shared__ int pre[];                     // [max_reqs + 1] chunk offsets
-  __shared__ int part[256];
+  __shared__ int scan_tmp[33];
   const int tid = threadIdx.x;
   // a programmatic dependent launch of k_swap_request: resident early, it
   // waits here until that kernel has finished and its writes are visible
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int seg = (max_reqs + 255) / 256;
-  auto cnt_of = [&](int i) -> int { const int c = copy_cnt[i]; return c > 0 ? c : 0; };
+  auto cnt_of = [&](int i) -> int {
+    const int c = copy_cnt[i];
+    return c > 0 && req_group[i] == group ? c : 0;
+  };
   int sum = 0;
   for (int i = tid * seg; i < (tid + 1) * seg && i < max_reqs; ++i) sum += cnt_of(i) * HS_ROW_VEC16;
-  part[tid] = sum;
-  __syncthreads();
-  if (tid < 32) {                                  // exclusive scan of the 256 partial sums
-    int v[8], run = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) { v[k] = part[tid * 8 + k]; run += v[k]; }
-    int incl = run;
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (tid >= off) incl += o;
-    }
-    int acc = incl - run;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) { part[tid * 8 + k] = acc; acc += v[k]; }
-  }
-  __syncthreads();
   {
-    int acc = part[tid];
+    int all;
+    int acc = hs_block_exscan(sum, scan_tmp, &all);
     for (int i = tid * seg; i < (tid + 1) * seg && i < max_reqs; ++i) {
       pre[i] = acc;
       acc += cnt_of(i) * HS_ROW_VEC16;
     }
-    if (tid == 255) pre[max_reqs] = acc;
+    if (tid == 0) pre[max_reqs] = all;
   }
   __syncthreads();
   const int total = pre[max_reqs];
-  const int64_t n_entries = (int64_t)ta.R * ta.K;
+  const int64_t n_entries = (int64_t)ta.n_rows * ta.K, e0 = (int64_t)ta.row_lo * ta.K;
   const int step = gridDim.x * blockDim.x;
   constexpr int TE = 2;                            // table entries per thread per round
   const int g = blockIdx.x * blockDim.x + tid;
@@ -545,7 +549,7 @@ __global__ void __launch_bounds__(256) k_swap_gather(const int32_t *__restrict__
 #pragma unroll
     for (int u = 0; u < TE; ++u) {
       const int64_t en = te + (int64_t)u * step;
-      if (en < n_entries) table_entry(ta, en);
+      if (en < n_entries) table_entry(ta, e0 + en);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u)
@@ -638,22 +642,11 @@ __global__ void __launch_bounds__(256) k_swap_apply(const int32_t *__restrict__ 
 
 }  // namespace
 
-extern "C" int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
-                          const int32_t *row_causal_len, const int32_t *kv_len,
-                          const int32_t *topk, int32_t R, int32_t K, int32_t *out_slot_idx,
-                          int32_t *out_valid, int64_t *stats, hs_stream_t stream) {
-  int rc = hs_check_buffer(buf);
-  if (rc) return rc;
-  if (R < 0 || K < 0 || K > (1 << 20))
-    return hs_set_error(HS_ERR_INVALID_ARG, "bad sizes R=%d K=%d (0..2^20)", R, K);
-  if (R > 0 && (!req_id_per_row || !row_causal_len || !kv_len))
-    return hs_set_error(HS_ERR_INVALID_ARG, "NULL row descriptor");
-  if (R > 0 && K > 0 && (!topk || !out_slot_idx))
-    return hs_set_error(HS_ERR_INVALID_ARG, "NULL topk or out_slot_idx");
-
-  buf->clock += 1;  // the LRU clock advances once per call, even an empty one
-  if (R == 0) return HS_OK;
-
+int hs_swap_plan_launch(hs_buffer *buf, const int32_t *req_id_per_row,
+                        const int32_t *row_causal_len, const int32_t *kv_len, const int32_t *topk,
+                        int32_t R, int32_t K, int32_t n_groups, const int32_t *group_end,
+                        int32_t *out_slot_idx, int32_t *out_valid, int64_t *stats,
+                        cudaStream_t stream) {
   SwapArgs a;
   a.req_id = req_id_per_row; a.clen = row_causal_len; a.kv_len = kv_len; a.topk = topk;
   a.R = R; a.K = K;
@@ -670,6 +663,9 @@ extern "C" int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
   a.stats = stats; a.status = buf->status;
   a.epoch = (uint32_t)buf->clock;
   a.now = buf->clock;
+  a.req_group = buf->req_group;
+  a.n_groups = n_groups;
+  for (int g = 0; g < HS_MAX_GROUPS; ++g) a.group_end[g] = g < n_groups ? group_end[g] : R;
 
   const size_t smem = swap_smem_bytes(buf->S, buf->max_ctx);
   static bool attr_set[64] = {false};
@@ -678,26 +674,41 @@ extern "C" int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
                                      (int)swap_smem_bytes(HS_MAX_SLOTS, RANK_MAX_WORDS * 32)));
     HS_CUDA_TRY(cudaFuncSetAttribute(k_swap_gather, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)((HS_MAX_REQS + 1) * sizeof(int))));
+    // the gather takes an SM's leftover beside an attention CTA (one CTA of
+    // the attention kernel leaves a few KB of shared memory), so it asks for
+    // the same shared-memory carve-out as the attention
+    HS_CUDA_TRY(cudaFuncSetAttribute(k_swap_gather, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared));
     if (buf->device < 64) attr_set[buf->device] = true;
   }
   k_swap_request<<<buf->max_reqs, SW_THREADS, smem, stream>>>(a, out_slot_idx, out_valid);
   HS_LAUNCH_CHECK("k_swap_request");
+  return HS_OK;
+}
+
+int hs_swap_gather_launch(hs_buffer *buf, const int32_t *req_id_per_row,
+                          const int32_t *row_causal_len, const int32_t *kv_len,
+                          const int32_t *topk, int32_t R, int32_t K, int32_t g, int32_t row_lo,
+                          int32_t row_hi, int32_t *out_slot_idx, int32_t *out_valid,
+                          int ctas_per_sm, bool pdl, cudaStream_t stream) {
   static int sms[64] = {0};
   int nsm = (buf->device < 64) ? sms[buf->device] : 0;
   if (nsm == 0) {
     HS_CUDA_TRY(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, buf->device));
     if (buf->device < 64) sms[buf->device] = nsm;
   }
+  (void)R;
   TableArgs ta;
   ta.req_id = req_id_per_row; ta.clen = row_causal_len; ta.kv_len = kv_len; ta.topk = topk;
   ta.token_slot = buf->token_slot; ta.copy_cnt = buf->copy_cnt;
-  ta.R = R; ta.K = K; ta.max_reqs = buf->max_reqs; ta.S = buf->S; ta.S_tot = buf->S_tot;
+  ta.row_lo = row_lo; ta.n_rows = row_hi - row_lo;
+  ta.K = K; ta.max_reqs = buf->max_reqs; ta.S = buf->S; ta.S_tot = buf->S_tot;
   ta.max_ctx = buf->max_ctx;
   ta.out = out_slot_idx; ta.out_valid = out_valid; ta.status = buf->status;
   const size_t gsmem = (size_t)(buf->max_reqs + 1) * sizeof(int);
   if (buf->copy_sms > 0 && buf->copy_sms < nsm) nsm = buf->copy_sms;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(nsm * 8));
+  cfg.gridDim = dim3((unsigned)(nsm * ctas_per_sm));
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = gsmem;
   cfg.stream = stream;
@@ -705,12 +716,41 @@ extern "C" int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const uint4 *pool = reinterpret_cast<const uint4 *>(buf->host_pool);
+  uint4 *hot = reinterpret_cast<uint4 *>(buf->hot_kv);
   HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_swap_gather, (const int32_t *)buf->copy_cnt,
+                                 (const int32_t *)buf->req_group, g,
                                  (const uint64_t *)buf->copy_desc, (int32_t)buf->max_reqs,
-                                 (int32_t)buf->S, (int32_t)buf->S_tot, a.pool, a.hot, ta));
+                                 (int32_t)buf->S, (int32_t)buf->S_tot, pool, hot, ta));
   HS_LAUNCH_CHECK("k_swap_gather");
   return HS_OK;
+}
+
+extern "C" int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
+                          const int32_t *row_causal_len, const int32_t *kv_len,
+                          const int32_t *topk, int32_t R, int32_t K, int32_t *out_slot_idx,
+                          int32_t *out_valid, int64_t *stats, hs_stream_t stream) {
+  int rc = hs_check_buffer(buf);
+  if (rc) return rc;
+  if (R < 0 || K < 0 || K > (1 << 20))
+    return hs_set_error(HS_ERR_INVALID_ARG, "bad sizes R=%d K=%d (0..2^20)", R, K);
+  if (R > 0 && (!req_id_per_row || !row_causal_len || !kv_len))
+    return hs_set_error(HS_ERR_INVALID_ARG, "NULL row descriptor");
+  if (R > 0 && K > 0 && (!topk || !out_slot_idx))
+    return hs_set_error(HS_ERR_INVALID_ARG, "NULL topk or out_slot_idx");
+
+  buf->clock += 1;  // the LRU clock advances once per call, even an empty one
+  if (R == 0) return HS_OK;
+  const int32_t end = R;
+  rc = hs_swap_plan_launch(buf, req_id_per_row, row_causal_len, kv_len, topk, R, K, 1, &end,
+                           out_slot_idx, out_valid, stats, stream);
+  if (rc) return rc;
+  // a programmatic dependent launch of k_swap_request: its blocks take the
+  // SMs the metadata kernel leaves free and wait until its copy lists are
+  // complete
+  return hs_swap_gather_launch(buf, req_id_per_row, row_causal_len, kv_len, topk, R, K, 0, 0, R,
+                               out_slot_idx, out_valid, 8, true, stream);
 }
 
 extern "C" int hs_swap_apply_plan(hs_buffer *buf, int32_t n_layers, void *const *hot_kv,

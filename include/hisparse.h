@@ -259,6 +259,63 @@ int hs_sparse_attn_decode(const void *q, const void *kv, int64_t n_kv_rows,
                           hs_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* a2-a6 in one call: swap-in and attention of a decode step, with the host  */
+/*     reads of later request groups overlapped with the attention of        */
+/*     earlier ones ("hiSparse-MTP", section 1: the coordinator's            */
+/*     asynchronous copy stream beside the compute stream)                   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Gives exactly the results of
+ *   hs_swap_in(buf, req_id_per_row, row_causal_len, kv_len, topk, R, K,
+ *              out_slot_idx, out_valid, stats, stream);
+ *   hs_sparse_attn_decode(q, hot_kv, max_reqs * (S + step_slots), out_slot_idx,
+ *                         R, H, K, scale, out, lse, <buf's status>, stream);
+ * (the same slot maps, slot table, counts, hot rows and bit-identical out and
+ * lse), with one swap-in on the LRU clock. The rows are split into groups of
+ * consecutive rows; a request is swapped in with the group of its first row.
+ * The metadata kernel runs once over every row; then the first group's missed
+ * rows are copied from the host pool and its rows attended on `stream`, while
+ * the copies of the next groups run on a stream of the buffer's own, one
+ * group ahead of the attention, which for group g >= 1 runs on further
+ * streams of the buffer's own once group g is resident. The copy blocks share
+ * each SM with an attention block (a buffer of up to 448 requests; with more,
+ * the copies of later groups wait for free SMs and the call is still correct).
+ * `stream` waits for all of it before any later work on it starts, so the call
+ * is ordered like any other on `stream`, in a CUDA graph capture too. (As for
+ * every call that advances the LRU clock, a graph replays the clock value of
+ * its capture: the clock is a host counter.)
+ *   q, H, scale, out, lse   as hs_sparse_attn_decode (q [R][H][576], out
+ *                           [R][H][512]; lse may be NULL)
+ *   n_groups       0: the library picks the groups (hs_step_groups); else
+ *                  1..8 with group_row_end (host int32 [n_groups]) rising
+ *                  strictly from above 0 to R: group g is rows
+ *                  [group_row_end[g-1], group_row_end[g])
+ *   other arguments as hs_swap_in
+ * Status goes to the buffer's status word (hs_get_status): the swap-in's bits
+ * and the attention's HS_STATUS_TIMEOUT.
+ * Requirements: those of hs_swap_in and hs_sparse_attn_decode. No two calls on
+ * the same buffer may be in flight on different streams (the buffer's own
+ * streams are shared by its calls).
+ */
+int hs_swap_in_attn_decode(hs_buffer *buf, const int32_t *req_id_per_row,
+                           const int32_t *row_causal_len, const int32_t *kv_len,
+                           const int32_t *topk, int32_t R, int32_t K, const void *q, int32_t H,
+                           float scale, int32_t n_groups, const int32_t *group_row_end,
+                           int32_t *out_slot_idx, int32_t *out_valid, void *out, float *lse,
+                           int64_t *stats, hs_stream_t stream);
+
+/*
+ * The groups hs_swap_in_attn_decode picks for R rows of H heads on the
+ * current device: the first is one wave of the attention kernel (the rows
+ * its resident two-SM clusters hold at once); the other rows form at most 7
+ * groups of equal size, a whole number of waves, the last taking what is
+ * left. Writes n_groups (0 when R = 0) and group_row_end (host int32, room
+ * for 8).
+ */
+int hs_step_groups(int32_t R, int32_t H, int32_t *n_groups, int32_t *group_row_end);
+
+/* ------------------------------------------------------------------------ */
 /* next-3: a batch mixing fully-resident and host-backed requests            */
 /*         ("vllm 分析(十二) HiSparse 下篇": the HiSparseResidentSpec and      */
 /*          reclaim_resident_blocks sections, the fully_resident flag, and   */
