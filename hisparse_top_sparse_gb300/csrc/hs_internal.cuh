@@ -143,13 +143,14 @@ int hs_swap_plan_launch(hs_buffer *buf, const int32_t *req_id_per_row,
                         cudaStream_t stream);
 // The copies of the misses of group g's requests (those whose first row lies
 // in group g) and the slot table of rows [row_lo, row_hi). ctas_per_sm
-// blocks per SM of the buffer's copy SMs; pdl: a programmatic dependent launch
-// of the kernel before it in the stream.
+// blocks of `threads` (a multiple of 32, at most 512) per SM of the buffer's
+// copy SMs; pdl: a programmatic dependent launch of the kernel before it in
+// the stream.
 int hs_swap_gather_launch(hs_buffer *buf, const int32_t *req_id_per_row,
                           const int32_t *row_causal_len, const int32_t *kv_len,
                           const int32_t *topk, int32_t R, int32_t K, int32_t g, int32_t row_lo,
                           int32_t row_hi, int32_t *out_slot_idx, int32_t *out_valid,
-                          int ctas_per_sm, bool pdl, cudaStream_t stream);
+                          int ctas_per_sm, int threads, bool pdl, cudaStream_t stream);
 
 // ---- attention launcher (hs_attn.cu) ----------------------------------------
 

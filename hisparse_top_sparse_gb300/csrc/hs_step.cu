@@ -105,7 +105,7 @@ extern "C" int hs_swap_in_attn_decode(hs_buffer *buf, const int32_t *req_id_per_
                            out_slot_idx, out_valid, stats, stream);
   if (rc) return rc;
   rc = hs_swap_gather_launch(buf, req_id_per_row, row_causal_len, kv_len, topk, R, K, 0, 0,
-                             ends[0], out_slot_idx, out_valid, 8, true, stream);
+                             ends[0], out_slot_idx, out_valid, 8, 256, true, stream);
   if (rc) return rc;
 
   const int64_t n_hot = (int64_t)buf->max_reqs * buf->S_tot;
@@ -122,8 +122,8 @@ extern "C" int hs_swap_in_attn_decode(hs_buffer *buf, const int32_t *req_id_per_
     HS_CUDA_TRY(cudaStreamWaitEvent(buf->side[0], buf->ev_fork, 0));
     for (int g = 1; g < G; ++g) {
       rc = hs_swap_gather_launch(buf, req_id_per_row, row_causal_len, kv_len, topk, R, K, g,
-                                 ends[g - 1], ends[g], out_slot_idx, out_valid, 1, false,
-                                 buf->side[0]);
+                                 ends[g - 1], ends[g], out_slot_idx, out_valid, 1, 256,
+                                 false, buf->side[0]);
       if (rc) return rc;
       HS_CUDA_TRY(cudaEventRecord(buf->ev_gather[g], buf->side[0]));
     }

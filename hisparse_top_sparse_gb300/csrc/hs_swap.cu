@@ -485,7 +485,7 @@ __device__ __forceinline__ void table_entry(const TableArgs &ta, int64_t e) {
 // spread over the whole grid, four 16-byte loads in flight per thread; the
 // slot table's entries are spread the same way and worked on while the
 // loads over the host link are in flight.
-__global__ void __launch_bounds__(256) k_swap_gather(const int32_t *__restrict__ copy_cnt,
+__global__ void __launch_bounds__(512) k_swap_gather(const int32_t *__restrict__ copy_cnt,
                                                      const int32_t *__restrict__ req_group,
                                                      int32_t group,
                                                      const uint64_t *__restrict__ copy_desc,
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(256) k_swap_gather(const int32_t *__restrict__
   // a programmatic dependent launch of k_swap_request: resident early, it
   // waits here until that kernel has finished and its writes are visible
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  const int seg = (max_reqs + 255) / 256;
+  const int seg = (max_reqs + (int)blockDim.x - 1) / (int)blockDim.x;
   auto cnt_of = [&](int i) -> int {
     const int c = copy_cnt[i];
     return c > 0 && req_group[i] == group ? c : 0;
@@ -690,7 +690,7 @@ int hs_swap_gather_launch(hs_buffer *buf, const int32_t *req_id_per_row,
                           const int32_t *row_causal_len, const int32_t *kv_len,
                           const int32_t *topk, int32_t R, int32_t K, int32_t g, int32_t row_lo,
                           int32_t row_hi, int32_t *out_slot_idx, int32_t *out_valid,
-                          int ctas_per_sm, bool pdl, cudaStream_t stream) {
+                          int ctas_per_sm, int threads, bool pdl, cudaStream_t stream) {
   static int sms[64] = {0};
   int nsm = (buf->device < 64) ? sms[buf->device] : 0;
   if (nsm == 0) {
@@ -709,7 +709,7 @@ int hs_swap_gather_launch(hs_buffer *buf, const int32_t *req_id_per_row,
   if (buf->copy_sms > 0 && buf->copy_sms < nsm) nsm = buf->copy_sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(nsm * ctas_per_sm));
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3((unsigned)threads);
   cfg.dynamicSmemBytes = gsmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -750,7 +750,7 @@ extern "C" int hs_swap_in(hs_buffer *buf, const int32_t *req_id_per_row,
   // SMs the metadata kernel leaves free and wait until its copy lists are
   // complete
   return hs_swap_gather_launch(buf, req_id_per_row, row_causal_len, kv_len, topk, R, K, 0, 0, R,
-                               out_slot_idx, out_valid, 8, true, stream);
+                               out_slot_idx, out_valid, 8, 256, true, stream);
 }
 
 extern "C" int hs_swap_apply_plan(hs_buffer *buf, int32_t n_layers, void *const *hot_kv,

@@ -97,16 +97,16 @@ def test_workload4_fused_step_matches_serial_and_oracle():
                 torch.arange(cfg.B, device=DEV))
 
 
-@pytest.mark.parametrize("seed", range(4))
-def test_explicit_groups_scattered_rows(seed):
+@pytest.mark.parametrize("seed,H", [(0, 32), (1, 32), (2, 32), (3, 32), (4, 200)])
+def test_explicit_groups_scattered_rows(seed, H):
     """Rows of a request scattered over the call and over several groups (a
     request is swapped in with the group of its first row), random group
     ends, 1 to 8 groups, evictions and step positions: bit for bit the serial
     calls on a twin buffer, and the attention matches the oracle on every
-    row."""
+    row. H = 200: two head groups per row, the last ragged."""
     hs = lib()
     g = np.random.default_rng(500 + seed)
-    B, S, n_step, bs, max_ctx, H = 6, 40, 3, 4, 160, 32
+    B, S, n_step, bs, max_ctx = 6, 40, 3, 4, 160
     nblk = max_ctx // bs
     hbt = g.permutation(B * nblk).reshape(B, nblk).astype(np.int32)
     pool = W.host_pool_tensor(B * nblk * bs, 900 + seed, device=DEV)
@@ -240,6 +240,42 @@ def test_bad_groups_are_refused_before_any_work():
     hs.hs_swap_in_attn_decode(buf, req, clen, kv_len, topk, q, 0.1, idx, out, groups=[1, 3, 4])
     torch.cuda.synchronize()
     assert buf.clock == c0 + 1 and hs.hs_get_status(buf) == 0
+
+
+def test_degenerate_calls_match_the_serial_pair():
+    """K = 0 (every row without keys: out 0, lse -inf) and R = 0 (nothing but
+    the clock) give what the serial pair gives on a twin buffer."""
+    hs = lib()
+    B, S, n_step, bs, max_ctx, H = 3, 8, 2, 4, 32, 16
+    hbt = np.arange(B * 8, dtype=np.int32).reshape(B, 8)
+    pool = W.host_pool_tensor(B * 32, 6, device=DEV)
+    hots = [torch.zeros((B * (S + n_step), 576), dtype=torch.bfloat16, device=DEV)
+            for _ in range(2)]
+    bufs = [hs.HsBuffer(B, S, n_step, max_ctx, bs, h, pool, _t(hbt)) for h in hots]
+    kv_len = _t(np.array([20, 20, 20], np.int32))
+    for R, K in ((5, 0), (0, 4)):
+        req = _t(np.arange(R, dtype=np.int32) % B)
+        clen = _t(np.full(R, 21, np.int32))
+        topk = torch.zeros((R, K), dtype=torch.int32, device=DEV)
+        q = torch.ones((R, H, 576), dtype=torch.bfloat16, device=DEV)
+        res = []
+        for k, buf in enumerate(bufs):
+            idx = torch.full((R, K), 7, dtype=torch.int32, device=DEV)
+            out = torch.full((R, H, 512), 3.0, dtype=torch.bfloat16, device=DEV)
+            lse = torch.zeros((R, H), dtype=torch.float32, device=DEV)
+            if k == 0:
+                hs.hs_swap_in(buf, req, clen, kv_len, topk, idx)
+                hs.hs_sparse_attn_decode(q, hots[0], idx, 0.1, out, lse)
+            else:
+                hs.hs_swap_in_attn_decode(buf, req, clen, kv_len, topk, q, 0.1, idx, out, lse=lse)
+            torch.cuda.synchronize()
+            res.append((out, lse))
+        assert torch.equal(res[0][0].view(torch.int16), res[1][0].view(torch.int16))
+        assert torch.equal(res[0][1].view(torch.int32), res[1][1].view(torch.int32))
+        if R:
+            assert (res[1][0].float() == 0).all() and torch.isneginf(res[1][1]).all()
+        assert bufs[0].clock == bufs[1].clock
+        assert hs.hs_get_status(bufs[0]) == hs.hs_get_status(bufs[1]) == 0
 
 
 def test_library_groups():
