@@ -623,7 +623,8 @@ def run_swap_bench(hs, dev, args):
     backup = run_backup_bench(hs, dev)
     verify = run_verify_bench(hs, dev, _peaks()[0]["hbm_gbs"])
     tiny = run_tiny_bench(hs, dev)
-    overlap = run_overlap_bench(hs, dev)
+    overlap = run_overlap_bench(hs, dev, 4)
+    overlap3 = run_overlap_bench(hs, dev, 3)
     link = measure_link(hs, dev)
     steady = range(1, cfg.steps)
     bytes_ss = sum(miss[s] for s in steady) * ROW_BYTES
@@ -647,7 +648,8 @@ def run_swap_bench(hs, dev, args):
                 "frac_of_link": round(n_follow * bytes_ss / (sum(apply_ms[s] for s in steady) * 1e-3)
                                       / 1e9 / link["peak_gbs"], 4),
                 "ms_per_step": [round(x, 4) for x in apply_ms]},
-            "backup": backup, "verify": verify, "overlap_workload4": overlap, "tiny_workload1": tiny,
+            "backup": backup, "verify": verify, "overlap_workload4": overlap,
+            "overlap_workload3": overlap3, "tiny_workload1": tiny,
             "status": st, "gpu_launches_per_step": 2}
 
 
@@ -762,8 +764,9 @@ def run_verify_bench(hs, dev, peak_hbm):
             "finalize_ms": round(fin_ms, 4), "rows_committed": committed, "status": st}
 
 
-def run_overlap_bench(hs, dev, steps=8, reps=3):
-    """Workload 4 (128 requests, contexts 16K-128K, 90 % reuse): decode steps
+def run_overlap_bench(hs, dev, cfg_no=4, reps=3):
+    """Workload 4 (128 requests, contexts 16K-128K, 90 % reuse; 8 steps) or 3
+    (64 requests x 32K, 80 % reuse; 16 steps): decode steps
     of swap-in + attention, serial (hs_swap_in, then hs_sparse_attn_decode,
     on one stream) against hs_swap_in_attn_decode (the library's row groups:
     the copies of each next group run beside the attention of the groups
@@ -772,7 +775,8 @@ def run_overlap_bench(hs, dev, steps=8, reps=3):
     `reps` times; steady = mean of steps 1.. (step 0 fills the empty buffer);
     spread = range of a variant's steady times over the repetitions. The
     outputs must agree bit for bit at every step."""
-    cfg = W.get_config(4)
+    cfg = W.get_config(cfg_no)
+    steps = cfg.steps
     req, ri = W.rows_of(cfg)
     clen = W.causal_lengths(cfg.L, req, ri)
     hb = W.host_backed_case(cfg, device=dev)
@@ -799,8 +803,9 @@ def run_overlap_bench(hs, dev, steps=8, reps=3):
         hs.hs_swap_in_attn_decode(buf, t_req, t_clen, hb["kv_len"], topks[st], q, cfg.scale,
                                   idx_f, out_f, stream=s1)
 
-    # one untimed pass first: the first touch of the freshly pinned 10.9 GB
-    # host pool made the first variant's steps slow and erratic on some boxes
+    # one untimed pass first: the first touch of a freshly pinned host pool
+    # (10.9 GB for workload 4) made the first variant's steps slow and erratic
+    # on some boxes
     buf = hs.HsBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hb["hot"],
                       hb["pool"], hb["hbt"])
     for st in range(steps):
