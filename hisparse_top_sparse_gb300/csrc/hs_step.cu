@@ -117,34 +117,50 @@ extern "C" int hs_swap_in_attn_decode(hs_buffer *buf, const int32_t *req_id_per_
                           scale, static_cast<char *>(out) + (int64_t)lo * H * 512 * 2,
                           lse ? lse + (int64_t)lo * H : nullptr, buf->status, pdl, st);
   };
-  if (G > 1) {
-    HS_CUDA_TRY(cudaEventRecord(buf->ev_fork, stream));
-    HS_CUDA_TRY(cudaStreamWaitEvent(buf->side[0], buf->ev_fork, 0));
-    for (int g = 1; g < G; ++g) {
-      rc = hs_swap_gather_launch(buf, req_id_per_row, row_causal_len, kv_len, topk, R, K, g,
-                                 ends[g - 1], ends[g], out_slot_idx, out_valid, 1, 256,
-                                 false, buf->side[0]);
-      if (rc) return rc;
-      HS_CUDA_TRY(cudaEventRecord(buf->ev_gather[g], buf->side[0]));
-    }
+  if (G == 1) {
+    // a programmatic dependent launch of the gather: its prologue runs while
+    // the gather finishes
+    return attend(0, stream, true);
   }
-  // a programmatic dependent launch of the first gather: its prologue runs
-  // while that gather finishes
-  rc = attend(0, stream, true);
-  if (rc) return rc;
-  if (G == 1) return HS_OK;
+  HS_CUDA_TRY(cudaEventRecord(buf->ev_fork, stream));
+  HS_CUDA_TRY(cudaStreamWaitEvent(buf->side[0], buf->ev_fork, 0));
+  // from here on every side stream that received work joins `stream` again,
+  // also when a later launch fails, so that a stream capture stays whole
   bool used[HS_SIDE_STREAMS] = {true, false, false};
+  auto join = [&]() -> int {
+    int first = HS_OK;
+    for (int s = 0; s < HS_SIDE_STREAMS; ++s) {
+      if (!used[s]) continue;
+      cudaError_t e = cudaEventRecord(buf->ev_join[s], buf->side[s]);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, buf->ev_join[s], 0);
+      if (e != cudaSuccess && first == HS_OK)
+        first = hs_set_error(HS_ERR_CUDA, "joining the buffer's streams: %s", cudaGetErrorString(e));
+    }
+    return first;
+  };
+  auto fail = [&](int code) -> int {
+    join();
+    return code;
+  };
+  for (int g = 1; g < G; ++g) {
+    rc = hs_swap_gather_launch(buf, req_id_per_row, row_causal_len, kv_len, topk, R, K, g,
+                               ends[g - 1], ends[g], out_slot_idx, out_valid, 1, 256, false,
+                               buf->side[0]);
+    if (rc) return fail(rc);
+    const cudaError_t e = cudaEventRecord(buf->ev_gather[g], buf->side[0]);
+    if (e != cudaSuccess)
+      return fail(hs_set_error(HS_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e)));
+  }
+  rc = attend(0, stream, true);
+  if (rc) return fail(rc);
   for (int g = 1; g < G; ++g) {
     const int s = 1 + (g - 1) % 2;
     used[s] = true;
-    HS_CUDA_TRY(cudaStreamWaitEvent(buf->side[s], buf->ev_gather[g], 0));
+    const cudaError_t e = cudaStreamWaitEvent(buf->side[s], buf->ev_gather[g], 0);
+    if (e != cudaSuccess)
+      return fail(hs_set_error(HS_ERR_CUDA, "cudaStreamWaitEvent: %s", cudaGetErrorString(e)));
     rc = attend(g, buf->side[s], false);
-    if (rc) return rc;
+    if (rc) return fail(rc);
   }
-  for (int s = 0; s < HS_SIDE_STREAMS; ++s) {
-    if (!used[s]) continue;
-    HS_CUDA_TRY(cudaEventRecord(buf->ev_join[s], buf->side[s]));
-    HS_CUDA_TRY(cudaStreamWaitEvent(stream, buf->ev_join[s], 0));
-  }
-  return HS_OK;
+  return join();
 }

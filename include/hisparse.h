@@ -377,12 +377,13 @@ int hs_sparse_attn_decode_mixed(const void *q, const void *kv_resident, int64_t 
 /* ------------------------------------------------------------------------ */
 
 /*
- * Repeats the copies of buf's latest hs_swap_in (the "plan": every missed
+ * Repeats the copies of buf's latest hs_swap_in or hs_swap_in_attn_decode
+ * (the "plan": every missed
  * position's host row and the slot it went to) for n_layers follower caches,
  * e.g. the other layers of the same requests: for each copy (request b, slot
  * s, host row h) and layer l,
  *   hot_kv[l][row_offset + b * (S + step_slots) + s] = host_pools[l][h].
- * The slot table returned by that hs_swap_in indexes every follower cache
+ * The slot table returned by that swap-in indexes every follower cache
  * the same way (plus row_offset). Followers have the leader's geometry (at
  * least row_offset + max_reqs * (S + step_slots) rows in hot_kv[l], host pools
  * paged like the leader's with at least host_pool_rows rows) but their own row
@@ -395,7 +396,7 @@ int hs_sparse_attn_decode_mixed(const void *q, const void *kv_resident, int64_t 
  *   row_offset  rows added to every destination (>= 0)
  *   row_bytes   a multiple of 4 (copies are 16 bytes wide when it is a
  *               multiple of 16 and every pointer is 16-byte aligned, else 4)
- * Call it after the hs_swap_in whose plan it repeats and before the next one
+ * Call it after the swap-in whose plan it repeats and before the next one
  * (same stream, or ordered). Requirements: 0 <= n_layers <= 64, pointers
  * 4-byte aligned, max_reqs * S * (row units) < 2^31.
  */

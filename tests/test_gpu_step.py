@@ -114,6 +114,9 @@ def test_explicit_groups_scattered_rows(seed, H):
             for _ in range(2)]
     bufs = [hs.HsBuffer(B, S, n_step, max_ctx, bs, h, pool, _t(hbt)) for h in hots]
     ref = O.HotBuffer(B, S, n_step, max_ctx, bs, hbt, pool.clone())
+    # a follower layer of each buffer, filled by repeating each call's plan
+    f_pool = W.host_pool_tensor(B * nblk * bs, 950 + seed, device=DEV)
+    f_hots = [torch.zeros_like(hots[0]) for _ in range(2)]
     L = [int(x) for x in g.integers(60, 150, size=B)]
     kv_len = _t(np.asarray(L, np.int32))
     for call in range(6):
@@ -139,6 +142,7 @@ def test_explicit_groups_scattered_rows(seed, H):
             else:
                 hs.hs_swap_in_attn_decode(buf, _t(req), _t(clen), kv_len, _t(topk), q, 0.07, idx,
                                           out, groups=ends, out_valid=valid, lse=lse)
+            hs.hs_swap_apply_plan(buf, [f_hots[k]], [f_pool])
             torch.cuda.synchronize()
             res.append((idx, valid, out, lse))
         (i1, v1, o1, l1), (i2, v2, o2, l2) = res
@@ -155,6 +159,7 @@ def test_explicit_groups_scattered_rows(seed, H):
                    np.stack([r_lse[k] for k in range(R)]))
     _same_state(hs, bufs[0], bufs[1], hots[0], hots[1], S + n_step, S,
                 torch.arange(B, device=DEV))
+    assert torch.equal(f_hots[0].view(torch.int16), f_hots[1].view(torch.int16))
 
 
 def test_fused_step_in_a_cuda_graph():
