@@ -10,20 +10,21 @@
 // Two launches. k_swap_request: one 1024-thread block per request that has
 // rows in the call works through that request alone:
 //   probe   every entry of the request's rows: classify it and look up its
-//           position's slot; a hit marks the slot in a shared-memory bitmap
-//           (distinct hits = marked slots), a miss claims its position once
-//           per call (a shared-memory bitmap of the request's positions, or
-//           epoch-stamped marks when it does not fit) and the first claims
-//           are compacted with __ballot_sync / __popc into a shared-memory
-//           list (one shared atomic per warp and round)
-//   assign  capacity check; the victims are the first slots of the request's
+//           position's slot; a hit sets the slot's flag in shared memory (a
+//           plain byte store; distinct hits = flagged slots), a miss claims its
+//           position once per call (a shared-memory bitmap of the request's
+//           positions, or epoch-stamped marks when it does not fit) and the
+//           first claims are compacted with __ballot_sync / __popc into a
+//           shared-memory list (one shared atomic per warp and round)
+//   assign  the victims are the first slots of the request's
 //           LRU order (a persistent array kept in ascending (ts, slot) order)
 //           that hold no needed position; the misses, in ascending position
 //           order (their ranks in a bitmap of miss positions), take them in
 //           order; hits and victims take the current time and move to the end
 //           of the order in slot order. Victims and the new order come from
-//           warp ballots over the order with one scan of the 32 warp counts
-//           -- no sort over all S slots
+//           warp ballots over the order (held in registers from the start)
+//           with one scan of the 32 warp counts -- no sort over all S slots;
+//           the count of slots free for victims is also the capacity check
 //   publish (host pool row, hot slot) of every miss
 // k_swap_gather is a programmatic dependent launch of k_swap_request: its
 // blocks take the SMs the metadata kernel leaves free and wait
@@ -102,20 +103,17 @@ __host__ __device__ inline int rank_words(int max_ctx) {
   return w <= RANK_MAX_WORDS ? w : 0;
 }
 
-// Shared-memory layout (bytes): mkey[nS] i32 (misses) | ord[S] i32 (LRU
-// order) | vict[S] i32 (victim slots) | hit / touched bitmap [S/32] u32 |
-// rows[ROW_CHUNK] i32 | row valid counts [ROW_CHUNK] i32 | miss bitmap [W]
-// u32 | its word prefix counts [W] i32 | needed-position bitmap [W] u32
-// (W = rank_words(max_ctx); with W = 0 the claims go through pos_mark and the
-// misses are sorted)
+// Shared-memory layout (bytes): mkey[nS] i32 (misses) | vict[S] i32 (victim
+// slots) | hit / touched flags [S] u8, padded to 4 | rows[ROW_CHUNK] i32 |
+// miss bitmap [W] u32 | its word prefix counts [W] i32 | needed-position
+// bitmap [W] u32 (W = rank_words(max_ctx); with W = 0 the claims go through
+// pos_mark and the misses are sorted)
 __host__ __device__ inline size_t swap_smem_bytes(int S, int max_ctx) {
   const int nS = pow2_ceil(S);
-  return (size_t)nS * 4 + (size_t)S * 8 + (size_t)((S + 31) / 32) * 4 + ROW_CHUNK * 8 +
+  return (size_t)nS * 4 + (size_t)S * 4 + (size_t)((S + 3) / 4) * 4 + ROW_CHUNK * 4 +
          (size_t)rank_words(max_ctx) * 12;
 }
-constexpr int ORD_REGS = HS_MAX_SLOTS / SW_THREADS;   // LRU order entries a thread prefetches
-
-__device__ __forceinline__ bool bit_of(const uint32_t *bm, int s) { return (bm[s >> 5] >> (s & 31)) & 1u; }
+constexpr int ORD_REGS = HS_MAX_SLOTS / SW_THREADS;   // LRU order entries a thread holds
 
 // Exclusive scan over the block's 32 warps of one count per warp (every lane
 // passes its warp's count): the warp's offset, and the total in *total.
@@ -155,16 +153,17 @@ __device__ int collect_rows(const SwapArgs &a, int b, int from, int *rows, int *
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     if (lane == 0) warp_base[w] = __popc(m);
     __syncthreads();
-    // exclusive prefix over warps, in row order
+    // exclusive prefix over warps, in row order (one warp's shuffle scan)
     __shared__ int total;
-    if (threadIdx.x == 0) {
-      int acc = *s_cnt;
-      for (int i = 0; i < SW_THREADS / 32; ++i) {
-        const int c = warp_base[i];
-        warp_base[i] = acc;
-        acc += c;
+    if (w == 0) {
+      const int x = warp_base[lane];
+      int xi = x;
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, xi, off);
+        if (lane >= off) xi += y;
       }
-      total = acc;
+      warp_base[lane] = *s_cnt + xi - x;
+      if (lane == 31) total = *s_cnt + xi;
     }
     __syncthreads();
     if (mine) {
@@ -196,33 +195,35 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
   const int b = blockIdx.x;
   const int nS = pow2_ceil(a.S);
   int32_t *mkey = reinterpret_cast<int32_t *>(smem);
-  int32_t *ord = mkey + nS;
-  int32_t *vict = ord + a.S;
-  uint32_t *hitmap = reinterpret_cast<uint32_t *>(vict + a.S);
-  int32_t *rows = reinterpret_cast<int32_t *>(hitmap + (a.S + 31) / 32);
-  int32_t *rvalid = rows + ROW_CHUNK;
+  int32_t *vict = mkey + nS;
+  // hit / touched flag per slot: plain byte stores (every writer stores 1)
+  uint8_t *hit = reinterpret_cast<uint8_t *>(vict + a.S);
+  int32_t *rows = reinterpret_cast<int32_t *>(hit + (a.S + 3) / 4 * 4);
   const int nW = rank_words(a.max_ctx);
-  uint32_t *pbm = reinterpret_cast<uint32_t *>(rvalid + ROW_CHUNK);
+  uint32_t *pbm = reinterpret_cast<uint32_t *>(rows + ROW_CHUNK);
   int32_t *pwp = reinterpret_cast<int32_t *>(pbm + nW);
   uint32_t *pneed = reinterpret_cast<uint32_t *>(pwp + nW);
-  __shared__ int s_need, s_miss, s_cnt, s_any, s_bad, s_first;
+  __shared__ int s_miss, s_cnt, s_any, s_bad, s_first;
   __shared__ int scan_tmp[33];
-  const int lane = threadIdx.x & 31;
 
-  if (threadIdx.x == 0) { s_need = 0; s_miss = 0; s_any = 0; s_bad = 0; a.copy_cnt[b] = 0; }
-  for (int i = threadIdx.x; i < (a.S + 31) / 32; i += SW_THREADS) hitmap[i] = 0u;
+  if (threadIdx.x == 0) { s_miss = 0; s_any = 0; s_bad = 0; a.copy_cnt[b] = 0; }
+  for (int i = threadIdx.x; i < (a.S + 3) / 4; i += SW_THREADS) reinterpret_cast<uint32_t *>(hit)[i] = 0u;
   __syncthreads();
 
   const int32_t L = a.kv_len[b];
   const int64_t cbase = (int64_t)b * a.max_ctx;
   const int64_t sbase = (int64_t)b * a.S;
-  // the request's LRU order, loaded now and put in shared memory after the
-  // probe, so its latency hides behind the probe
+  // the request's LRU order, loaded now (its latency hides behind the probe)
+  // in the layout of the victim pass: order position w * CH + 32 j + lane
+  // belongs to warp w, round j < NR
+  const int lane = threadIdx.x & 31;
+  const int CH = ((a.S + 31) / 32 + 31) / 32 * 32;   // order positions per warp
+  const int NR = CH / 32;                             // rounds (at most ORD_REGS)
   int32_t ordv[ORD_REGS];
 #pragma unroll
-  for (int u = 0; u < ORD_REGS; ++u) {
-    const int i = u * SW_THREADS + (int)threadIdx.x;
-    ordv[u] = i < a.S ? a.lru_order[sbase + i] : 0;
+  for (int j = 0; j < ORD_REGS; ++j) {
+    const int i = (int)(threadIdx.x >> 5) * CH + j * 32 + lane;
+    ordv[j] = j < NR && i < a.S ? a.lru_order[sbase + i] : -1;
   }
   // a position is claimed once per call: first setter of its bit in the
   // needed-position bitmap (or of its pos_mark epoch when that does not fit)
@@ -248,17 +249,32 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
     // position's slot; a hit marks the slot (distinct hits = marked slots),
     // and only a miss claims its position, so that a position missed by
     // several rows gets one slot. The loads of a round are in flight together.
+    // Entry i = r * K + j of the chunk is row rows[r], column j; a thread
+    // starts at entry threadIdx.x and steps by SW_THREADS, carrying (r, j)
+    // instead of dividing every entry by K.
+    int r = 0, j = 0, dq = 0, dr = 0;
+    if (items > 0) {
+      r = (int)threadIdx.x / a.K;
+      j = (int)threadIdx.x % a.K;
+      dq = SW_THREADS / a.K;
+      dr = SW_THREADS % a.K;
+    }
     for (int base = 0; base < items; base += SW_THREADS * PB) {
       int32_t t[PB], clen[PB], sl[PB];
 #pragma unroll
       for (int u = 0; u < PB; ++u) {
-        const int i = base + u * SW_THREADS + (int)threadIdx.x;
         t[u] = -1;
         clen[u] = 0;
-        if (i < items) {
-          const int row = rows[i / a.K];
-          t[u] = a.topk[(int64_t)row * a.K + i % a.K];
+        if (r < n) {
+          const int row = rows[r];
+          t[u] = a.topk[(int64_t)row * a.K + j];
           clen[u] = a.clen[row];
+        }
+        r += dq;
+        j += dr;
+        if (j >= a.K) {
+          j -= a.K;
+          ++r;
         }
       }
       bool bad = false;
@@ -272,7 +288,7 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
       int my_total = 0;
 #pragma unroll
       for (int u = 0; u < PB; ++u) {
-        if (sl[u] >= 0 && sl[u] < a.S) atomicOr(&hitmap[sl[u] >> 5], 1u << (sl[u] & 31));
+        if (sl[u] >= 0 && sl[u] < a.S) hit[sl[u]] = 1;
         bool first = false;
         if (sl[u] < 0 && sl[u] != INT32_MIN) {      // a committed position not in the buffer
           if (use_bm) {
@@ -312,13 +328,25 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
   }
 
   // ---- assign ---------------------------------------------------------------
-  for (int w = threadIdx.x; w < (a.S + 31) / 32; w += SW_THREADS) {
-    const int c = __popc(hitmap[w]);
-    if (c) atomicAdd(&s_need, c);
+  // victims: the first nm slots of the LRU order (ascending (ts, slot)) that
+  // hold no position needed in this call. Order position i = w * CH + 32 j +
+  // lane belongs to warp w, round j (held in ordv since the start); ranks come
+  // from warp ballots and one scan of the warp counts, so the writes of a warp
+  // are contiguous. The count of such free slots also settles the capacity:
+  // the distinct hits are the other S - n_free slots.
+  const int nm = s_miss;
+  const int w = threadIdx.x >> 5;
+  unsigned fm[ORD_REGS];                              // free (not hit) slots, by round
+  int cnt = 0;
+#pragma unroll
+  for (int j = 0; j < ORD_REGS; ++j) {
+    const int i = w * CH + j * 32 + lane;
+    fm[j] = __ballot_sync(0xffffffffu, j < NR && i < a.S && !hit[ordv[j]]);
+    cnt += __popc(fm[j]);
   }
-  __syncthreads();
-  const int nm = s_miss, need = s_need + nm;
-  const bool failed = need > a.S;
+  int n_free;
+  int k = warp_exscan(cnt, scan_tmp, &n_free);
+  const bool failed = nm > n_free;                    // hits + misses > S
   if (failed) {
     if (threadIdx.x == 0) {
       atomicOr(a.status, HS_STATUS_CAPACITY);
@@ -326,43 +354,20 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
     }
   } else {
     if (threadIdx.x == 0 && a.stats) {
-      atomicAdd((unsigned long long *)&a.stats[0], (unsigned long long)(need - nm));
+      atomicAdd((unsigned long long *)&a.stats[0], (unsigned long long)(a.S - n_free));
       atomicAdd((unsigned long long *)&a.stats[1], (unsigned long long)nm);
     }
-    // victims: the first nm slots of the LRU order (ascending (ts, slot)) that
-    // hold no position needed in this call. Order position i = w * CH + 32 j
-    // + lane belongs to warp w, round j; ranks come from warp ballots and one
-    // scan of the warp counts, so the writes of a warp are contiguous.
     int32_t *lru = a.lru_order + sbase;
-#pragma unroll
-    for (int u = 0; u < ORD_REGS; ++u) {
-      const int i = u * SW_THREADS + (int)threadIdx.x;
-      if (i < a.S) ord[i] = ordv[u];
-    }
-    const int w = threadIdx.x >> 5;
-    const int CH = ((a.S + 31) / 32 + 31) / 32 * 32;   // order positions per warp
-    const int NR = CH / 32;                             // rounds (at most ORD_REGS)
-    __syncthreads();
-    unsigned fm[ORD_REGS];                              // free (not hit) slots, by round
-    int cnt = 0;
-#pragma unroll
-    for (int j = 0; j < ORD_REGS; ++j) {
-      const int i = w * CH + j * 32 + lane;
-      fm[j] = __ballot_sync(0xffffffffu, j < NR && i < a.S && !bit_of(hitmap, ord[i]));
-      cnt += __popc(fm[j]);
-    }
-    int n_free;
-    int k = warp_exscan(cnt, scan_tmp, &n_free);
     // the first nm free slots become victims (touched from now on); the
     // other free slots keep their order at the front of the new LRU order
 #pragma unroll
     for (int j = 0; j < ORD_REGS; ++j) {
       if ((fm[j] >> lane) & 1u) {
         const int r = k + __popc(fm[j] & ((1u << lane) - 1u));
-        const int32_t sl = ord[w * CH + j * 32 + lane];
+        const int32_t sl = ordv[j];
         if (r < nm) {
           vict[r] = sl;
-          atomicOr(&hitmap[sl >> 5], 1u << (sl & 31));
+          hit[sl] = 1;
         } else {
           lru[r - nm] = sl;
         }
@@ -376,7 +381,7 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
 #pragma unroll
     for (int j = 0; j < ORD_REGS; ++j) {
       const int sl = w * CH + j * 32 + lane;
-      tm[j] = __ballot_sync(0xffffffffu, j < NR && sl < a.S && bit_of(hitmap, sl));
+      tm[j] = __ballot_sync(0xffffffffu, j < NR && sl < a.S && hit[sl]);
       ct += __popc(tm[j]);
     }
     int n_touched;
