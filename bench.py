@@ -714,8 +714,9 @@ def run_tiny_bench(hs, dev, reps=4):
 def run_verify_bench(hs, dev, peak_hbm):
     """Workload 5: the greedy acceptance reads 256 x 4 x 129280 bf16 logits
     (264.8 MB, more than L2); its GB/s against the measured HBM peak, then
-    one full hs_verify_finalize (acceptance + commit of the accepted prefix)
-    on a warm hot buffer."""
+    the full hs_verify_finalize (acceptance + commit of the accepted prefix)
+    on warm hot buffers (median of five timed calls after three untimed
+    ones)."""
     cfg = W.get_config(5)
     logits, drafts, _ = W.planted_logits(cfg, device=dev)
     t_drafts = torch.as_tensor(drafts, device=dev)
@@ -737,31 +738,40 @@ def run_verify_bench(hs, dev, peak_hbm):
         ms.append(a.elapsed_time(b) / 10)
     best = statistics.median(ms)
     byt = logits.numel() * logits.element_size()
-    # one acceptance + commit on a buffer warmed by a swap-in of a 2048-set
+    # acceptance + commit on buffers warmed by a swap-in of a 2048-set: three
+    # untimed calls first (the first launch of the kernel in the process
+    # carries its load), then five timed ones, each on a fresh warm buffer
     req, ri = W.rows_of(cfg)
     hb = W.host_backed_case(cfg, device=dev)
-    buf = hs.HsBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hb["hot"],
-                      hb["pool"], hb["hbt"])
     sets = [W.locality_sets(cfg, cfg.L[r], r, 1) for r in range(cfg.B)]
     topk = torch.as_tensor(W.topk_shared_sets(cfg, sets, 0), device=dev)
     clen = torch.as_tensor(W.causal_lengths(cfg.L, req, ri), device=dev)
+    t_req = torch.as_tensor(req, device=dev)
     out_idx = torch.empty((cfg.R, cfg.K), dtype=torch.int32, device=dev)
-    hs.hs_swap_in(buf, torch.as_tensor(req, device=dev), clen, hb["kv_len"], topk, out_idx)
     skv = W.step_kv(cfg, 0, device=dev)
-    _lead()
-    a.record()
-    hs.hs_verify_finalize(buf, logits, t_drafts, skv, hb["kv_len"], acc, nxt)
-    b.record()
-    b.synchronize()
-    fin_ms = a.elapsed_time(b)
-    committed = int(acc.sum().item()) + cfg.B
-    st = hs.hs_get_status(buf)
-    buf.close()
+    fin, committed, st = [], 0, 0
+    for it in range(8):
+        buf = hs.HsBuffer(cfg.B, cfg.S, cfg.d + 1, hb["max_ctx"], cfg.block_size, hb["hot"],
+                          hb["pool"], hb["hbt"])
+        kv_len = hb["kv_len"].clone()
+        hs.hs_swap_in(buf, t_req, clen, kv_len, topk, out_idx)
+        _lead()
+        a.record()
+        hs.hs_verify_finalize(buf, logits, t_drafts, skv, kv_len, acc, nxt)
+        b.record()
+        b.synchronize()
+        if it >= 3:
+            fin.append(a.elapsed_time(b))
+        committed = int(acc.sum().item()) + cfg.B
+        st |= hs.hs_get_status(buf)
+        buf.close()
+    fin_ms = statistics.median(fin)
     del hb, logits
     return {"workload": cfg.name, "accept_ms": round(best, 4),
             "logits_gbs": round(byt / (best * 1e-3) / 1e9, 1),
             "frac_of_hbm": round(byt / (best * 1e-3) / 1e9 / peak_hbm, 4),
-            "finalize_ms": round(fin_ms, 4), "rows_committed": committed, "status": st}
+            "finalize_ms": round(fin_ms, 4), "finalize_ms_per_call": [round(x, 4) for x in fin],
+            "rows_committed": committed, "status": st}
 
 
 def run_overlap_bench(hs, dev, cfg_no=4, reps=3):
