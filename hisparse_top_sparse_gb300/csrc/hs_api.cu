@@ -64,7 +64,7 @@ int hs_check_buffer(const hs_buffer *buf) {
 
 static void free_buffer(hs_buffer *b) {
   if (!b) return;
-  void *ptrs[] = {b->token_slot, b->slot_token, b->slot_ts, b->lru_order, b->pos_mark,
+  void *ptrs[] = {b->token_slot, b->slot_token, b->slot_ts, b->lru_order, b->lru_head, b->pos_mark,
                   b->copy_desc,  b->copy_cnt,   b->pred,    b->row_count, b->verify_claim,
                   b->req_group,  b->status};
   for (void *p : ptrs)
@@ -146,6 +146,7 @@ extern "C" int hs_buffer_create(const hs_buffer_desc *d, hs_buffer **out) {
       {(void **)&b->slot_token, R * S * 4, 0xFF},
       {(void **)&b->slot_ts, R * S * 8, 0xFF},
       {(void **)&b->lru_order, R * S * 4, 0},
+      {(void **)&b->lru_head, R * 4, 0},
       {(void **)&b->pos_mark, R * C * 4, 0},
       {(void **)&b->copy_desc, R * S * 8, 0},
       {(void **)&b->copy_cnt, R * 4, 0},
@@ -208,7 +209,9 @@ extern "C" int hs_buffer_set_copy_sms(hs_buffer *buf, int32_t n_sms) {
 }
 
 __global__ void k_request_reset(int32_t *token_slot, int32_t *slot_token, int64_t *slot_ts,
-                                int32_t *order, int32_t S, int32_t max_ctx, int32_t req) {
+                                int32_t *order, int32_t *head, int32_t S, int32_t max_ctx,
+                                int32_t req) {
+  if (threadIdx.x == 0) head[req] = 0;
   for (int s = threadIdx.x; s < S; s += blockDim.x) {
     int64_t k = (int64_t)req * S + s;
     int32_t t = slot_token[k];
@@ -225,7 +228,8 @@ extern "C" int hs_request_reset(hs_buffer *buf, int32_t req, hs_stream_t stream)
   if (req < 0 || req >= buf->max_reqs)
     return hs_set_error(HS_ERR_INVALID_ARG, "req %d outside [0, %d)", req, buf->max_reqs);
   k_request_reset<<<1, 1024, 0, stream>>>(buf->token_slot, buf->slot_token, buf->slot_ts,
-                                          buf->lru_order, buf->S, buf->max_ctx, req);
+                                          buf->lru_order, buf->lru_head, buf->S, buf->max_ctx,
+                                          req);
   HS_LAUNCH_CHECK("k_request_reset");
   return HS_OK;
 }

@@ -30,7 +30,8 @@ struct hs_buffer {
   int32_t *token_slot;   // [max_reqs][max_ctx], -1 = not resident
   int32_t *slot_token;   // [max_reqs][S], -1 = empty
   int64_t *slot_ts;      // [max_reqs][S], -1 = empty
-  int32_t *lru_order;    // [max_reqs][S]: slots in ascending (ts, slot) order
+  int32_t *lru_order;    // [max_reqs][S]: slots in ascending (ts, slot) order, a ring
+  int32_t *lru_head;     // [max_reqs]: ring position of each request's order's first slot
 
   // per-call scratch (epoch-stamped, so nothing needs clearing per call)
   uint32_t *pos_mark;    // [max_reqs][max_ctx]: epoch at which a position was claimed
@@ -104,30 +105,6 @@ __device__ __forceinline__ int hs_block_exscan(int v, int *tmp, int *total) {
   return res;
 }
 
-// The LRU order after a call that gave every slot in `touched` the newest
-// timestamp: the untouched slots keep their order, the touched ones follow in
-// slot order -- which is again the order by ascending (ts, slot). `order` is
-// the current order (shared memory), `touched` a bitmap of S bits (shared
-// memory); the new order is written to `out` (global). Every thread calls it.
-__device__ __forceinline__ void hs_lru_reorder(const int32_t *order, const uint32_t *touched,
-                                               int S, int32_t *out, int *tmp) {
-  const int E = (S + blockDim.x - 1) / blockDim.x;
-  const int lo = threadIdx.x * E, hi = min(S, lo + E);
-  int cu = 0, ct = 0;
-  for (int i = lo; i < hi; ++i) {
-    const int s = order[i];
-    cu += !((touched[s >> 5] >> (s & 31)) & 1u);
-    ct += (touched[i >> 5] >> (i & 31)) & 1u;
-  }
-  int tot_u, tot_t;
-  int ku = hs_block_exscan(cu, tmp, &tot_u);
-  int kt = hs_block_exscan(ct, tmp, &tot_t) + tot_u;
-  for (int i = lo; i < hi; ++i) {
-    const int s = order[i];
-    if (!((touched[s >> 5] >> (s & 31)) & 1u)) out[ku++] = s;
-    if ((touched[i >> 5] >> (i & 31)) & 1u) out[kt++] = i;
-  }
-}
 int hs_check_buffer(const hs_buffer *buf);
 
 // ---- launchers shared by hs_swap_in and hs_swap_in_attn_decode (hs_swap.cu)

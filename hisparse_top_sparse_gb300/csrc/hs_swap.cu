@@ -17,7 +17,9 @@
 //           first claims are compacted with __ballot_sync / __popc into a
 //           shared-memory list (one shared atomic per warp and round)
 //   assign  the victims are the first slots of the request's
-//           LRU order (a persistent array kept in ascending (ts, slot) order)
+//           LRU order (a persistent array kept in ascending (ts, slot) order,
+//           a ring from the request's head: commits rotate it; this kernel
+//           writes the new order from position 0)
 //           that hold no needed position; the misses, in ascending position
 //           order (their ranks in a bitmap of miss positions), take them in
 //           order; hits and victims take the current time and move to the end
@@ -53,7 +55,7 @@ struct SwapArgs {
   const int32_t *hbt;
   int32_t *token_slot, *slot_token;
   int64_t *slot_ts;
-  int32_t *lru_order;
+  int32_t *lru_order, *lru_head;
   uint32_t *pos_mark;
   uint64_t *copy_desc;
   int32_t *copy_cnt;
@@ -219,11 +221,15 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
   const int lane = threadIdx.x & 31;
   const int CH = ((a.S + 31) / 32 + 31) / 32 * 32;   // order positions per warp
   const int NR = CH / 32;                             // rounds (at most ORD_REGS)
+  // (the order is a ring from position lru_head[b]: commits rotate it)
+  const int head = a.lru_head[b];
   int32_t ordv[ORD_REGS];
 #pragma unroll
   for (int j = 0; j < ORD_REGS; ++j) {
     const int i = (int)(threadIdx.x >> 5) * CH + j * 32 + lane;
-    ordv[j] = j < NR && i < a.S ? a.lru_order[sbase + i] : -1;
+    int p = head + i;
+    if (p >= a.S) p -= a.S;
+    ordv[j] = j < NR && i < a.S ? a.lru_order[sbase + p] : -1;
   }
   // a position is claimed once per call: first setter of its bit in the
   // needed-position bitmap (or of its pos_mark epoch when that does not fit)
@@ -357,7 +363,8 @@ __global__ void __launch_bounds__(SW_THREADS, 1) k_swap_request(SwapArgs a,
       atomicAdd((unsigned long long *)&a.stats[0], (unsigned long long)(a.S - n_free));
       atomicAdd((unsigned long long *)&a.stats[1], (unsigned long long)nm);
     }
-    int32_t *lru = a.lru_order + sbase;
+    int32_t *lru = a.lru_order + sbase;   // the new order is written from position 0
+    if (threadIdx.x == 0) a.lru_head[b] = 0;
     // the first nm free slots become victims (touched from now on); the
     // other free slots keep their order at the front of the new LRU order
 #pragma unroll
@@ -659,6 +666,7 @@ int hs_swap_plan_launch(hs_buffer *buf, const int32_t *req_id_per_row,
   a.block_size = buf->block_size; a.hbt_stride = buf->hbt_stride; a.hbt = buf->hbt;
   a.token_slot = buf->token_slot; a.slot_token = buf->slot_token; a.slot_ts = buf->slot_ts;
   a.lru_order = buf->lru_order;
+  a.lru_head = buf->lru_head;
   a.pos_mark = buf->pos_mark;
   a.copy_desc = buf->copy_desc;
   a.copy_cnt = buf->copy_cnt;

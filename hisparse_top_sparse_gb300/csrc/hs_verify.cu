@@ -12,8 +12,10 @@
 // argmax over the vocabulary (16-byte loads, ties to the lowest index); the
 // last of a request's rows to finish then, with the whole block, takes the
 // accepted length and next token and commits: host-pool write of the kept
-// rows through the mapped pool, LRU slot choice (the head of the request's
-// (ts, slot) order, which is then rotated), hot-slot write, kv_len update.
+// rows through the mapped pool, LRU slot choice (the first slots of the
+// request's (ts, slot) order, a ring whose head then moves past them, so the
+// commit writes as many order entries as it keeps rows), hot-slot write,
+// kv_len update.
 
 #include <float.h>
 
@@ -34,7 +36,7 @@ struct CommitArgs {
   uint4 *pool, *hot;
   int32_t *token_slot, *slot_token;
   int64_t *slot_ts;
-  int32_t *lru_order;
+  int32_t *lru_order, *lru_head;
   uint32_t *verify_claim;
   uint32_t *status;
   int64_t now;
@@ -44,8 +46,8 @@ struct CommitArgs {
 // threads): longest agreeing prefix m and next token; then the m + 1 kept step
 // rows go to the host pool and to the first m + 1 slots of the LRU order
 // (nothing protected), which take the current time and move to the order's
-// end; the maps and kv_len follow. `ord` is S int32 of dynamic shared memory.
-__device__ __forceinline__ void commit_request(const int b, const CommitArgs &ca, int32_t *ord) {
+// end; the maps and kv_len follow.
+__device__ __forceinline__ void commit_request(const int b, const CommitArgs &ca) {
   const int32_t d = ca.d;
   const int32_t *drafts = ca.drafts;
   const int32_t *pred = ca.pred;
@@ -95,15 +97,17 @@ __device__ __forceinline__ void commit_request(const int b, const CommitArgs &ca
 
   // The victims are the first n slots of the LRU order (ascending (ts, slot),
   // nothing protected). They take the current time, so the new order is the
-  // rest of the order followed by the victims in slot order.
+  // rest of the order followed by the victims in slot order. The order is a
+  // ring from lru_head[req]: the victims' ring positions take them back in
+  // slot order and the head moves past them (n entries written, not S).
   int32_t *lru = lru_order + sbase;
-  for (int i = threadIdx.x; i < S; i += blockDim.x) ord[i] = lru[i];
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int k = 0; k < n; ++k) chosen[k] = ord[k];
+  const int head = ca.lru_head[req];
+  if ((int)threadIdx.x < n) {
+    int p = head + (int)threadIdx.x;
+    if (p >= S) p -= S;
+    chosen[threadIdx.x] = lru[p];
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < S - n; i += blockDim.x) lru[i] = ord[n + i];
   if (threadIdx.x == 0) {
     int32_t sorted[HS_MAX_STEP];
     for (int k = 0; k < n; ++k) {               // insertion sort of at most 16 slots
@@ -112,7 +116,12 @@ __device__ __forceinline__ void commit_request(const int b, const CommitArgs &ca
       while (j > 0 && sorted[j - 1] > v) { sorted[j] = sorted[j - 1]; --j; }
       sorted[j] = v;
     }
-    for (int k = 0; k < n; ++k) lru[S - n + k] = sorted[k];
+    for (int k = 0; k < n; ++k) {
+      int p = head + k;
+      if (p >= S) p -= S;
+      lru[p] = sorted[k];
+    }
+    ca.lru_head[req] = head + n >= S ? head + n - S : head + n;
   }
 
   // map updates (one thread per kept position)
@@ -149,7 +158,6 @@ template <int DTYPE>
 __global__ void __launch_bounds__(HS_ARGMAX_THREADS) k_verify(const void *__restrict__ logits,
                                                              int32_t V, int32_t *row_count,
                                                              const __grid_constant__ CommitArgs ca) {
-  extern __shared__ int32_t ord[];                 // [S], for the commit
   __shared__ int s_last;
   const int64_t row = blockIdx.x;
   const int rows_per_req = ca.d + 1;
@@ -167,7 +175,7 @@ __global__ void __launch_bounds__(HS_ARGMAX_THREADS) k_verify(const void *__rest
     }
   }
   __syncthreads();
-  if (s_last) commit_request(b, ca, ord);
+  if (s_last) commit_request(b, ca);
 }
 
 }  // namespace
@@ -199,13 +207,13 @@ extern "C" int hs_verify_finalize(hs_buffer *buf, const void *logits, int32_t lo
   ca.pool = reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(buf->host_pool));
   ca.hot = reinterpret_cast<uint4 *>(buf->hot_kv);
   ca.token_slot = buf->token_slot; ca.slot_token = buf->slot_token; ca.slot_ts = buf->slot_ts;
-  ca.lru_order = buf->lru_order; ca.verify_claim = buf->verify_claim; ca.status = buf->status;
+  ca.lru_order = buf->lru_order; ca.lru_head = buf->lru_head;
+  ca.verify_claim = buf->verify_claim; ca.status = buf->status;
   ca.now = buf->clock;
-  const size_t smem = (size_t)buf->S * sizeof(int32_t);
   if (logits_dtype == HS_LOGITS_F32)
-    k_verify<HS_LOGITS_F32><<<rows, HS_ARGMAX_THREADS, smem, stream>>>(logits, V, buf->row_count, ca);
+    k_verify<HS_LOGITS_F32><<<rows, HS_ARGMAX_THREADS, 0, stream>>>(logits, V, buf->row_count, ca);
   else
-    k_verify<HS_LOGITS_BF16><<<rows, HS_ARGMAX_THREADS, smem, stream>>>(logits, V, buf->row_count, ca);
+    k_verify<HS_LOGITS_BF16><<<rows, HS_ARGMAX_THREADS, 0, stream>>>(logits, V, buf->row_count, ca);
   HS_LAUNCH_CHECK("k_verify");
   return HS_OK;
 }

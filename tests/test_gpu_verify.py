@@ -343,3 +343,56 @@ def test_verify_with_a_repeated_request_id():
         for x, y in zip(before, after):
             assert torch.equal(x[b], y[b])
     buf.close()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_swap_ins_and_commits_interleaved(seed):
+    """Random swap-in calls and verify commits in turn on a small buffer (the
+    commits move the head of each request's LRU order ring, the swap-ins read
+    the order from it and write a new one), every piece of state against the
+    oracle after every call."""
+    hs = lib()
+    g = np.random.default_rng(700 + seed)
+    B, d, V, S, bs, max_ctx = 4, 3, 300, 20, 8, 512
+    nblk = max_ctx // bs
+    hbt = g.permutation(B * nblk).reshape(B, nblk).astype(np.int32)
+    pool = W.host_pool_tensor(B * nblk * bs, 700 + seed, device=DEV)
+    hot = torch.zeros((B * (S + d + 1), 576), dtype=torch.bfloat16, device=DEV)
+    buf = hs.HsBuffer(B, S, d + 1, max_ctx, bs, hot, pool, _t(hbt))
+    ref = O.HotBuffer(B, S, d + 1, max_ctx, bs, hbt, pool.clone())
+    L = [int(x) for x in g.integers(30, 120, size=B)]
+    kv_len = _t(np.asarray(L, np.int32))
+    for call in range(10):
+        if call % 2 == 0:
+            R = int(g.integers(1, 7))
+            req = g.integers(0, B, size=R).astype(np.int32)
+            K = int(g.integers(1, 12))
+            clen = np.array([L[b] + int(g.integers(1, d + 2)) for b in req], np.int32)
+            topk = np.stack([g.integers(-1, c, size=K) for c in clen]).astype(np.int32)
+            out = torch.full((R, K), 9, dtype=torch.int32, device=DEV)
+            hs.hs_swap_in(buf, _t(req), _t(clen), kv_len, _t(topk), out)
+            e_out, _, e_st, _ = ref.swap_in(req, clen, L, topk)
+            torch.cuda.synchronize()
+            assert np.array_equal(np_(out), e_out)
+        else:
+            lg = g.standard_normal((B, d + 1, V)).astype(np.float32)
+            drafts = g.integers(0, V, size=(B, d)).astype(np.int32)
+            for b in range(B):
+                for i in range(d):
+                    if g.random() < 0.6:
+                        drafts[b, i] = int(np.argmax(lg[b, i]))
+            skv = W.bf16_normal((B, d + 1, 576), 1.0, 700 + seed, "skv_mix", call)
+            acc = torch.empty(B, dtype=torch.int32, device=DEV)
+            nxt = torch.empty_like(acc)
+            hs.hs_verify_finalize(buf, _t(lg), _t(drafts), skv.to(DEV), kv_len, acc, nxt)
+            e_acc, e_nxt, e_L, e_st = O.verify_finalize(ref, torch.as_tensor(lg), drafts, skv, L)
+            torch.cuda.synchronize()
+            assert np.array_equal(np_(acc), e_acc) and np.array_equal(np_(nxt), e_nxt)
+            assert np.array_equal(np_(kv_len), e_L)
+            L = [int(x) for x in e_L]
+        assert hs.hs_get_status(buf) == e_st
+        for b in range(B):
+            _compare_request(buf, ref, hot, b, S, S + d + 1)
+        assert np.array_equal(_u16(pool), ref.host_pool)
+        assert buf.clock == ref.now
+    buf.close()
