@@ -247,6 +247,53 @@ def test_bad_groups_are_refused_before_any_work():
     assert buf.clock == c0 + 1 and hs.hs_get_status(buf) == 0
 
 
+@pytest.mark.parametrize("max_reqs,copy_sms", [(1000, 0), (12, 3)])
+def test_large_buffer_and_held_copy_kernels(max_reqs, copy_sms):
+    """A buffer of 1000 requests (the copy kernel's per-request prefix no
+    longer fits beside an attention block, so later groups' copies wait for
+    free SMs) and a buffer whose copy kernels are held to 3 SMs: three calls
+    of scattered rows in four groups, bit for bit the serial pair."""
+    hs = lib()
+    g = np.random.default_rng(800 + max_reqs)
+    S, n_step, bs, max_ctx, H, K = 16, 2, 8, 128, 32, 12
+    nblk = max_ctx // bs
+    hbt = g.permutation(max_reqs * nblk).reshape(max_reqs, nblk).astype(np.int32)
+    pool = W.host_pool_tensor(max_reqs * nblk * bs, 801, device=DEV)
+    hots = [torch.zeros((max_reqs * (S + n_step), 576), dtype=torch.bfloat16, device=DEV)
+            for _ in range(2)]
+    bufs = [hs.HsBuffer(max_reqs, S, n_step, max_ctx, bs, h, pool, _t(hbt)) for h in hots]
+    for buf in bufs:
+        hs.hs_buffer_set_copy_sms(buf, copy_sms)
+    L = [int(x) for x in g.integers(20, 100, size=max_reqs)]
+    kv_len = _t(np.asarray(L, np.int32))
+    for call in range(3):
+        R = 40
+        req = g.choice(max_reqs, R).astype(np.int32)
+        clen = np.array([L[b] + int(g.integers(1, n_step + 1)) for b in req], np.int32)
+        topk = np.stack([g.choice(c, K, replace=False) for c in clen]).astype(np.int32)
+        q = (torch.randn((R, H, 576), generator=torch.Generator().manual_seed(call))
+             * 0.5).to(torch.bfloat16).to(DEV)
+        res = []
+        for k, buf in enumerate(bufs):
+            idx = torch.empty((R, K), dtype=torch.int32, device=DEV)
+            out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=DEV)
+            if k == 0:
+                hs.hs_swap_in(buf, _t(req), _t(clen), kv_len, _t(topk), idx)
+                hs.hs_sparse_attn_decode(q, hots[0], idx, 0.05, out)
+            else:
+                hs.hs_swap_in_attn_decode(buf, _t(req), _t(clen), kv_len, _t(topk), q, 0.05, idx,
+                                          out, groups=[5, 17, 30, R])
+            torch.cuda.synchronize()
+            res.append((idx, out))
+        assert torch.equal(res[0][0], res[1][0])
+        assert torch.equal(res[0][1].view(torch.int16), res[1][1].view(torch.int16))
+        # requests drawn more than once may overflow their slots: the same
+        # capacity bits on both sides
+        assert hs.hs_get_status(bufs[0]) == hs.hs_get_status(bufs[1])
+    _same_state(hs, bufs[0], bufs[1], hots[0], hots[1], S + n_step, S,
+                torch.arange(max_reqs, device=DEV))
+
+
 def test_degenerate_calls_match_the_serial_pair():
     """K = 0 (every row without keys: out 0, lse -inf) and R = 0 (nothing but
     the clock) give what the serial pair gives on a twin buffer."""
