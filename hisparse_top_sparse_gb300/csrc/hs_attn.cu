@@ -41,9 +41,10 @@
 //     the row, and the pair then runs the row again with the exact maximum
 //     (exchanged at the end of the first pass) as the reference. The row sum
 //     l is the sum of both CTAs' partial sums.
-// Warp roles (352 threads): warps 0-3 softmax, P exchange and epilogue (thread
-// = head = TMEM lane), warps 4-7 gather producers, warps 8-9 issue Q K^T for
-// own tiles into S buffers 0 / 1, warp 10 issues P V for every tile in order.
+// Warp roles (480 threads): warps 0-3 softmax, P exchange and epilogue (thread
+// = head = TMEM lane), warps 4-11 gather producers (eight threads per key, one
+// 16-byte chunk of each 64-dim block per thread), warps 12-13 issue Q K^T for
+// own tiles into S buffers 0 / 1, warp 14 issues P V for every tile in order.
 // The kernel is a programmatic dependent launch: its prologue (barriers, TMEM,
 // Q) overlaps the previous kernel (hs_resolve_topk releases it at entry), and
 // it reads the indices and request flags after griddepcontrol.wait.
@@ -69,8 +70,8 @@ constexpr int QS_BLOCKS = (D - QT_DIMS) / 64;   // 3 swizzle blocks of Q in SMEM
 constexpr int NSB = 2;                    // S / P buffers (own tiles)
 constexpr int VB_BLOCKS = 4;              // swizzle blocks of one value half
 constexpr int RA_SLOTS = 3, VO_SLOTS = 3, VP_SLOTS = 3, XP_SLOTS = 1;
-constexpr int THREADS = 352;
-constexpr int NPROD = 128;
+constexpr int THREADS = 480;
+constexpr int NPROD = 256;
 constexpr float REF_SLACK = 30.0f;        // P <= 2^30 on the shared reference
 
 // shared memory (offsets from a 1024-byte aligned base)
@@ -485,11 +486,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (!req_ok && status && tid == 0 && c == 0) atomicOr(status, HS_STATUS_INDEX);
 
 
-  if (warp >= 4 && warp < 8) {
+  if (warp >= 4 && warp < 12) {
     // ------------------------------------------------ gather producers ----
-    const int p = tid - 128;          // 0..127
-    const int key = p >> 2;           // 32 keys per tile, 4 threads per key
-    const int sub = p & 3;            // chunks sub, sub+4, ..., 18 per thread
+    const int p = tid - 128;          // 0..255
+    const int key = p >> 3;           // 32 keys per tile, 8 threads per key
+    const int sub = p & 7;            // chunk sub of every 64-dim block
     auto load_id = [&](int t) -> int32_t {
       const int j = t * NK + key;
       return (t < T && j < K) ? __ldg(idx_row + j) : -1;
@@ -522,9 +523,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           // copy k of this thread is chunk sub + 4k: swizzle block k / 2,
           // chunk sub + 4 (k & 1) within the block's 128-byte row
 #pragma unroll
-          for (int k = 0; k < NCH / 4; ++k) {
-            const int ch = sub + 4 * k;
-            cp_async16(kv_block(ra, rv, c, k >> 1) + sw128(key, ch & 7), v ? src + ch * 16 : q, v);
+          for (int k = 0; k < NCH / 8; ++k) {
+            const int ch = sub + 8 * k;
+            cp_async16(kv_block(ra, rv, c, k) + sw128(key, sub), v ? src + ch * 16 : q, v);
           }
           asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar(B_FULLA + sa))
                        : "memory");
@@ -538,9 +539,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t rv = sbase + VP_OFF + sp * V_SLOT_BYTES;
           // only this CTA's value half: copies k = 8c .. 8c + 7 of the 18
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int ch = sub + 4 * (8 * c + k);
-            cp_async16(rv + (k >> 1) * KV_BLOCK_BYTES + sw128(key, ch & 7), v ? src + ch * 16 : q, v);
+          for (int k = 0; k < 4; ++k) {
+            const int ch = 32 * c + sub + 8 * k;
+            cp_async16(rv + k * KV_BLOCK_BYTES + sw128(key, sub), v ? src + ch * 16 : q, v);
           }
           asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar(B_FULLVP + sp))
                        : "memory");
@@ -549,12 +550,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
     }
     cp_async_wait<0>();
-  } else if (warp >= 8 && warp < 8 + NSB) {
+  } else if (warp >= 12 && warp < 12 + NSB) {
     // ------------------------------------- Q K^T issuers (own tiles) ----
-    // warp 8 + b issues own tiles ig = b, b + 2, ... into S buffer b
+    // warp 12 + b issues own tiles ig = b, b + 2, ... into S buffer b
     {
       const uint32_t qs0 = sbase + QS_OFF;
-      const int b = warp - 8;
+      const int b = warp - 12;
       bool ok = true;
       for (int pass = 0; pass < 2 && ok; ++pass) {
         if (pass == 1) {
@@ -589,7 +590,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       timed_out = !ok;
     }
-  } else if (warp == 8 + NSB) {
+  } else if (warp == 12 + NSB) {
     // ------------------------------------ P V issuer (every tile, in order) ----
     {
       bool ok = true;

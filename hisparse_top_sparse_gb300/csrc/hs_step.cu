@@ -16,11 +16,12 @@
 //   side 1/2 attention of group g >= 1 after its gather's event, alternating
 //            between two streams so that a group's attention fills the SMs the
 //            previous group's last wave leaves idle
-// A gather block (256 threads, 51 registers, 144 + 4 * (max_reqs + 1) bytes of
-// shared memory) fits on an SM beside one attention CTA (448 threads, 93
-// registers, 229,376 bytes; the SM keeps 3 KB) for up to 448 requests, so the
-// later gathers take no SM away from the attention. The caller's stream waits
-// for every side stream before the call returns.
+// A gather block (256 threads, 54 registers, 144 + 4 * (max_reqs + 1) bytes of
+// shared memory) fits on an SM beside one attention CTA (480 threads, 93
+// registers, 229,376 bytes; the SM keeps 3 KB of shared memory and 19 K
+// registers) for up to 448 requests, so the later gathers take no SM away
+// from the attention. The caller's stream waits for every side stream before
+// the call returns.
 
 #include <algorithm>
 
