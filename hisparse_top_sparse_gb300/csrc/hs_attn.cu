@@ -121,9 +121,14 @@ enum {
   B_DECIDE = B_VOTE + 1,              // softmax -> other roles: second pass or not
   B_OFULL = B_DECIDE + 1,             // all P V of a pass done (one per pass)
   B_QLOAD = B_OFULL + 2,              // Q landed (9 x 16 KB by tensor copies)
-  B_COUNT = B_QLOAD + 1
+  B_QSTAGED = B_QLOAD + 1,            // Q dims 0..383 are in TMEM (4 softmax warps)
+  B_COUNT = B_QSTAGED + 1
 };
-static_assert(B_COUNT * 8 + 8 <= 512, "barrier area");
+static_assert(B_COUNT * 8 + 16 <= 512, "barrier area");
+// O staged for the epilogue's tensor stores: four 16 KB blocks over ring A and
+// the start of ring VO (free once the last P V is done)
+constexpr int O_STG_OFF = RA_OFF;
+static_assert(O_STG_OFF + 4 * HG * 128 <= XS_OFF, "O staging");
 
 constexpr int WAIT_LIMIT = 1 << 24;
 
@@ -135,6 +140,20 @@ __device__ __forceinline__ uint32_t kv_block(uint32_t ra, uint32_t rv, int c, in
   const int pa = (c == 0) ? a - 4 : (a == 8 ? 4 : a);
   return ra + (uint32_t)pa * KV_BLOCK_BYTES;
 }
+
+// Staging place of Q block a (dims 64a..64a+63, a < 6) before it moves into
+// TMEM: slots 1-2 of ring A (two blocks), slots 1-2 of ring VO and the two P
+// buffers (three blocks), slot 1 of ring VP (one block). Slot 0 of each ring
+// is left for the first tiles, which are gathered meanwhile.
+__host__ __device__ constexpr uint32_t q_stage_off(int a) {
+  return a < 2 ? RA_OFF + RA_SLOT_BYTES + a * (HG * 128)
+               : a < 5 ? VO_OFF + V_SLOT_BYTES + (a - 2) * (HG * 128) : VP_OFF + V_SLOT_BYTES;
+}
+static_assert(q_stage_off(1) + HG * 128 <= RA_OFF + RA_SLOTS * RA_SLOT_BYTES &&
+                  q_stage_off(4) + HG * 128 == VP_OFF && q_stage_off(0) % 1024 == 0 &&
+                  q_stage_off(1) % 1024 == 0 && q_stage_off(2) % 1024 == 0 &&
+                  q_stage_off(5) % 1024 == 0 && RA_SLOTS == 3 && VO_SLOTS == 3 && VP_SLOTS >= 2,
+              "Q staging map");
 
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
@@ -309,6 +328,10 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
+// named barrier `id` over the first `n` threads of the CTA (whole warps)
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+}
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
                    : "memory");
@@ -362,7 +385,8 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity)
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-    k_attn_pair(const __grid_constant__ CUtensorMap tmap_q, const char *__restrict__ q,
+    k_attn_pair(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_o,
+                const char *__restrict__ q,
                 const char *__restrict__ kv_res, int64_t n_res, const char *__restrict__ kv_hot,
                 int64_t n_hot, const int32_t *__restrict__ row_req,
                 const int32_t *__restrict__ fully_resident, int32_t n_reqs,
@@ -375,6 +399,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t bars = sbase + BAR_OFF;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + BAR_OFF + B_COUNT * 8);
   volatile uint32_t *s_redo = tmem_slot + 1;
+  volatile uint32_t *s_last = tmem_slot + 2;   // the last pass run (0 or 1)
+  volatile uint32_t *s_fail = tmem_slot + 3;   // a wait of warps 0-7 gave up
   auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -415,7 +441,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     bar_init(bar(B_VOTE), 4);
     bar_init(bar(B_DECIDE), 1);
     bar_init(bar(B_QLOAD), 1);
+    bar_init(bar(B_QSTAGED), 4);
     *s_redo = 0u;
+    *s_last = 0u;
+    *s_fail = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) {
@@ -427,15 +456,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // Q by nine tensor copies of 128 heads x 64 dims (16 KB, 128-byte swizzle,
   // rows past H filled with zeros), all issued by this CTA into its own
   // shared memory: dims 384..575 land in SMEM as the MMA's A operand, dims
-  // 0..383 in a staging area over the (still empty) rings A and VO and the P
-  // staging slots, from where each head's thread moves them into TMEM
-  static_assert(6 * HG * 128 <= XP_OFF - RA_OFF, "Q staging fits rings A, VO and the P staging");
+  // 0..383 in a staging area over the (still empty) slots 1 and 2 of rings
+  // A and VO, the P buffers and slot 1 of ring VP, from where each head's
+  // thread moves them into TMEM. Slot 0 of every ring stays free, so the
+  // first own and the first peer tile are gathered while Q comes in.
   if (tid == 0) {
     // the barrier was initialised by this thread; the copies need no peer
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     arrive_expect_tx(bar(B_QLOAD), 9 * HG * 128);
     for (int a = 0; a < D / 64; ++a) {
-      const uint32_t dst = a < 6 ? sbase + RA_OFF + a * (HG * 128) : sbase + QS_OFF + (a - 6) * (HG * 128);
+      const uint32_t dst = a < 6 ? sbase + q_stage_off(a) : sbase + QS_OFF + (a - 6) * (HG * 128);
       asm volatile(
           "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
           " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
@@ -448,14 +478,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   fence_after();
   const uint32_t tmem = *tmem_slot;
   bool timed_out = false;
+  int own_sent = 0;        // own tiles whose P went to the peer (softmax warps)
   if (warp < 4) {
     // staged Q dims 0..383 -> TMEM columns [256, 448): lane = head, column j
-    // holds dims 2j, 2j+1
+    // holds dims 2j, 2j+1; then the staging slots are free for KV tiles and
+    // the Q K^T issuers may start (B_QSTAGED)
     if (!warp_wait(bar(B_QLOAD), 0)) timed_out = true;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
     for (int part = 0; part < QT_DIMS / 64; ++part) {
-      const unsigned char *blk = sm + RA_OFF + part * (HG * 128) + tid * 128;
+      const unsigned char *blk = sm + q_stage_off(part) + tid * 128;
       uint32_t v[32];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -465,10 +497,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       TMEM_ST32(lane_base + COL_Q + part * 32, v);
     }
     tmem_wait_st();
+    fence_before();
+    __syncwarp();
+    if (lane == 0) bar_arrive(bar(B_QSTAGED));
   }
-  fence_before();
-  __syncthreads();         // Q is in place; the staging area is free for KV tiles
-  fence_after();
 
   // Up to here the kernel has read only q. It is launched as a programmatic
   // dependent of the kernel before it (hs_resolve_topk lets it start at once),
@@ -510,6 +542,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const char *src = kv + (v ? (int64_t)id * ROWB : 0);
         if ((t & 1) == c) {
           const int sa = ig % RA_SLOTS, so = ig % VO_SLOTS;
+          // slots 1 and 2 hold staged Q until it is in TMEM
+          if (ig == 1 && !bar_wait(bar(B_QSTAGED), 0)) {
+            timed_out = true;
+            break;
+          }
           if (ig >= RA_SLOTS && !bar_wait(bar(B_EMPTYA + sa), ((ig / RA_SLOTS) - 1) & 1)) {
             timed_out = true;
             break;
@@ -532,6 +569,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           ++ig;
         } else {
           const int sp = jg % VP_SLOTS;
+          if (jg == 1 && !bar_wait(bar(B_QSTAGED), 0)) {
+            timed_out = true;
+            break;
+          }
           if (jg >= VP_SLOTS && !bar_wait(bar(B_EMPTYVP + sp), ((jg / VP_SLOTS) - 1) & 1)) {
             timed_out = true;
             break;
@@ -556,7 +597,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     {
       const uint32_t qs0 = sbase + QS_OFF;
       const int b = warp - 12;
-      bool ok = true;
+      bool ok = warp_wait(bar(B_QSTAGED), 0);   // Q dims 0..383 in TMEM
+      fence_after();
       for (int pass = 0; pass < 2 && ok; ++pass) {
         if (pass == 1) {
           ok = warp_wait(bar(B_DECIDE), 0);
@@ -763,42 +805,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
     if (!decided && tid == 0) bar_arrive(bar(B_DECIDE));   // lets the other roles wind down
 
-    // ---------------------------------------------------------- epilogue --
+    // 1 / l of the head for the epilogue (the first-tile maxima's slot is
+    // free: the reference was agreed in the first pass)
     const int h = h0 + hrow;
     const float lt = l + l_peer;
-    if (!timed_out && T > 0 && !warp_wait(bar(B_OFULL + last_pass), 0)) timed_out = true;
+    reinterpret_cast<volatile float *>(sm + XMAX_OFF)[hrow] = lt > 0.f ? 1.0f / lt : 0.f;
+    if (lse && c == 0 && h < H)
+      lse[(int64_t)r * H + h] = lt > 0.f ? (ref + log2f(lt)) * 0.69314718055994530942f : -INFINITY;
+    if (tid == 0) *s_last = (uint32_t)last_pass;
+    own_sent = ig;
+  }
+
+  // ------------------------------------------------------------ epilogue ----
+  // Warps 0-7 (two per TMEM lane quarter, 128 columns each) read O once the
+  // last P V is done, scale it by 1 / l, write it as bf16 into four 128-byte
+  // swizzled 16 KB blocks over the free ring A, and one thread stores the
+  // blocks with tensor copies (heads past H are clipped by the copy).
+  if (warp < 8) {
+    if (timed_out) atomicOr((uint32_t *)s_fail, 1u);
+    named_bar_sync(1, 256);             // 1 / l, the pass count and failures are in place
+    bool ok = *s_fail == 0u && T > 0;
+    if (ok) {
+      ok = warp_wait(bar(B_OFULL + *s_last), 0);
+      if (!ok) timed_out = true;
+    }
     fence_after();
-    const float inv = lt > 0.f ? 1.0f / lt : 0.f;
-    __nv_bfloat16 *orow = out + ((int64_t)r * H + (h < H ? h : 0)) * DV + 256 * c;
+    const int q4 = warp & 3, half = warp >> 2;
+    const int row = q4 * 32 + lane;
+    const float inv = ok ? reinterpret_cast<volatile float *>(sm + XMAX_OFF)[row] : 0.f;
+    const uint32_t lane_q = tmem + ((uint32_t)(q4 * 32) << 16);
 #pragma unroll 1
-    for (int part = 0; part < 256 / 32; ++part) {
-      uint32_t o[32];
-      if (T > 0 && !timed_out) {
-        TMEM_LD32(lane_base + COL_O + part * 32, o);
+    for (int pp = 0; pp < 4; pp += 2) {
+      const int p0 = half * 4 + pp;
+      uint32_t o[2][32];
+      if (ok) {
+        TMEM_LD32(lane_q + COL_O + p0 * 32, o[0]);
+        TMEM_LD32(lane_q + COL_O + (p0 + 1) * 32, o[1]);
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) o[k] = 0u;
+        for (int k = 0; k < 32; ++k) o[0][k] = o[1][k] = 0u;
       }
-      if (h < H) {
-        uint4 *dst = reinterpret_cast<uint4 *>(orow + part * 32);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          dst[k] = make_uint4(pack_bf16(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv),
-                              pack_bf16(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv),
-                              pack_bf16(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
-                              pack_bf16(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
+      for (int u = 0; u < 2; ++u) {
+        const int part = p0 + u;
+        unsigned char *blk = sm + O_STG_OFF + (part >> 1) * (HG * 128) + row * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j = (part & 1) * 4 + k;
+          *reinterpret_cast<uint4 *>(blk + ((j ^ (row & 7)) << 4)) =
+              make_uint4(pack_bf16(__uint_as_float(o[u][8 * k]) * inv, __uint_as_float(o[u][8 * k + 1]) * inv),
+                         pack_bf16(__uint_as_float(o[u][8 * k + 2]) * inv, __uint_as_float(o[u][8 * k + 3]) * inv),
+                         pack_bf16(__uint_as_float(o[u][8 * k + 4]) * inv, __uint_as_float(o[u][8 * k + 5]) * inv),
+                         pack_bf16(__uint_as_float(o[u][8 * k + 6]) * inv, __uint_as_float(o[u][8 * k + 7]) * inv));
+        }
       }
     }
-    if (lse && c == 0 && h < H)
-      lse[(int64_t)r * H + h] = lt > 0.f ? (ref + log2f(lt)) * 0.69314718055994530942f : -INFINITY;
-
-    // every P sent must have been consumed by the peer (its multicast commit
-    // arrives here) before this CTA's shared memory goes away
-    if (tid == 0 && !timed_out) {
-      for (int xs = 0; xs < XP_SLOTS; ++xs) {
-        const int uses = ig > xs ? (ig - xs + XP_SLOTS - 1) / XP_SLOTS : 0;
-        if (uses > 0 && !bar_wait_cluster(bar(B_XPFREE + xs), (uses - 1) & 1)) timed_out = true;
+    fence_proxy_async();                // the tensor stores read through the async proxy
+    named_bar_sync(1, 256);
+    if (tid == 0) {
+#pragma unroll 1
+      for (int b = 0; b < 4; ++b)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];\n" ::"l"(
+                reinterpret_cast<uint64_t>(&tmap_o)),
+            "r"(256 * c + 64 * b), "r"(h0), "r"(r), "r"(sbase + O_STG_OFF + b * (HG * 128))
+            : "memory");
+      asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+      // every P sent must have been consumed by the peer (its multicast
+      // commit arrives here) before this CTA's shared memory goes away
+      if (!timed_out) {
+        for (int xs = 0; xs < XP_SLOTS; ++xs) {
+          const int uses = own_sent > xs ? (own_sent - xs + XP_SLOTS - 1) / XP_SLOTS : 0;
+          if (uses > 0 && !bar_wait_cluster(bar(B_XPFREE + xs), (uses - 1) & 1)) timed_out = true;
+        }
       }
     }
   }
@@ -929,6 +1010,14 @@ int hs_attn_launch(const void *q, const void *kv_resident, int64_t n_resident, c
                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (er != CUDA_SUCCESS) return hs_set_error(HS_ERR_CUDA, "tensor map of q failed (%d)", (int)er);
+  // out as a [R][H][512] bf16 tensor for the epilogue's tensor stores
+  alignas(64) CUtensorMap tmap_o;
+  const cuuint64_t odim[3] = {(cuuint64_t)DV, (cuuint64_t)H, (cuuint64_t)R};
+  const cuuint64_t ostride[2] = {(cuuint64_t)DV * 2, (cuuint64_t)H * DV * 2};
+  const CUresult eo = encode(&tmap_o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, odim, ostride, box,
+                             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (eo != CUDA_SUCCESS) return hs_set_error(HS_ERR_CUDA, "tensor map of out failed (%d)", (int)eo);
   // a programmatic dependent launch: the prologue (barriers, TMEM, Q) may
   // run while the previous kernel in the stream finishes
   cudaLaunchConfig_t cfg = {};
@@ -942,7 +1031,7 @@ int hs_attn_launch(const void *q, const void *kv_resident, int64_t n_resident, c
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   HS_CUDA_TRY(cudaLaunchKernelEx(
-      &cfg, k_attn_pair, tmap, reinterpret_cast<const char *>(q),
+      &cfg, k_attn_pair, tmap, tmap_o, reinterpret_cast<const char *>(q),
       reinterpret_cast<const char *>(kv_resident), n_resident,
       reinterpret_cast<const char *>(kv_hot), n_hot, row_req, fully_resident, n_reqs, idx, H, K,
       scale * 1.4426950408889634f, reinterpret_cast<__nv_bfloat16 *>(out), lse, status));
