@@ -332,6 +332,14 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
 }
+// the cluster barrier in two halves: arrive (this thread's earlier writes
+// released) and wait (the other CTA's writes before its arrival acquired)
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
                    : "memory");
@@ -473,9 +481,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           : "memory");
     }
   }
+  // This CTA's barriers and TMEM exist: the CTA proceeds at once, and it
+  // arrives on the cluster barrier, whose wait the warps that write into the
+  // peer CTA (softmax and P V issuer) take before their first remote write.
+  // The other warps take it just before the closing cluster barrier.
   fence_before();
-  cluster_sync();          // both CTAs' barriers exist before any remote operation
+  __syncthreads();
   fence_after();
+  cluster_arrive();
   const uint32_t tmem = *tmem_slot;
   bool timed_out = false;
   int own_sent = 0;        // own tiles whose P went to the peer (softmax warps)
@@ -634,6 +647,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 12 + NSB) {
     // ------------------------------------ P V issuer (every tile, in order) ----
+    cluster_wait();                                // the peer's barriers exist
     {
       bool ok = true;
       int ig = 0, jg = 0;
@@ -683,6 +697,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else if (warp < 4) {
     // -------------------------------- softmax + P exchange (warps 0-3) ----
+    cluster_wait();                                // the peer's barriers exist
     const int hrow = tid;                          // head row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const uint32_t peer_xp = peer_addr(sbase + XP_OFF, peer) + (uint32_t)warp * 32 * 64;
@@ -885,6 +900,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 
   if (timed_out && status) atomicOr(status, HS_STATUS_TIMEOUT);
+  __syncwarp();
+  if (warp >= 4 && warp < 12 + NSB) cluster_wait();   // the opening barrier's wait
   fence_before();
   cluster_sync();          // the peer writes into this CTA's shared memory until here
   if (warp == 0) {
