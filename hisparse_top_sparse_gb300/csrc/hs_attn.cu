@@ -412,6 +412,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == 12 + NSB && lane == 0)
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
   const int c = (int)cluster_rank();                // value half; own tiles t = c mod 2
   const uint32_t peer = (uint32_t)(c ^ 1);
   const int n_hg = (H + HG - 1) / HG;
@@ -461,6 +463,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
 
+  // This CTA's barriers and TMEM exist: the CTA proceeds at once, and it
+  // arrives on the cluster barrier, whose wait the warps that write into the
+  // peer CTA (softmax and P V issuer) take before their first remote write.
+  // The other warps take it just before the closing cluster barrier.
+  fence_before();
+  __syncthreads();
+  fence_after();
+  cluster_arrive();
+  const uint32_t tmem = *tmem_slot;
   // Q by nine tensor copies of 128 heads x 64 dims (16 KB, 128-byte swizzle,
   // rows past H filled with zeros), all issued by this CTA into its own
   // shared memory: dims 384..575 land in SMEM as the MMA's A operand, dims
@@ -468,8 +479,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // A and VO, the P buffers and slot 1 of ring VP, from where each head's
   // thread moves them into TMEM. Slot 0 of every ring stays free, so the
   // first own and the first peer tile are gathered while Q comes in.
-  if (tid == 0) {
-    // the barrier was initialised by this thread; the copies need no peer
+  // The copies are issued by the P V issuer warp, whose first MMA waits for
+  // the first P anyway: issuing them can stall the issuing thread for
+  // microseconds while the other CTAs of the wave load their Q.
+  if (warp == 12 + NSB && lane == 0) {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     arrive_expect_tx(bar(B_QLOAD), 9 * HG * 128);
     for (int a = 0; a < D / 64; ++a) {
@@ -481,15 +494,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           : "memory");
     }
   }
-  // This CTA's barriers and TMEM exist: the CTA proceeds at once, and it
-  // arrives on the cluster barrier, whose wait the warps that write into the
-  // peer CTA (softmax and P V issuer) take before their first remote write.
-  // The other warps take it just before the closing cluster barrier.
-  fence_before();
-  __syncthreads();
-  fence_after();
-  cluster_arrive();
-  const uint32_t tmem = *tmem_slot;
   bool timed_out = false;
   int own_sent = 0;        // own tiles whose P went to the peer (softmax warps)
   if (warp < 4) {
@@ -647,6 +651,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 12 + NSB) {
     // ------------------------------------ P V issuer (every tile, in order) ----
+    __syncwarp();
     cluster_wait();                                // the peer's barriers exist
     {
       bool ok = true;
@@ -697,6 +702,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else if (warp < 4) {
     // -------------------------------- softmax + P exchange (warps 0-3) ----
+    __syncwarp();
     cluster_wait();                                // the peer's barriers exist
     const int hrow = tid;                          // head row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
