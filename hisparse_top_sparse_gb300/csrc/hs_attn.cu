@@ -893,7 +893,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             "r"(256 * c + 64 * b), "r"(h0), "r"(r), "r"(sbase + O_STG_OFF + b * (HG * 128))
             : "memory");
       asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
-      asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
       // every P sent must have been consumed by the peer (its multicast
       // commit arrives here) before this CTA's shared memory goes away
       if (!timed_out) {
