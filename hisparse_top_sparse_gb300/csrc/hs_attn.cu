@@ -184,36 +184,41 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
 constexpr uint32_t IDESC_QK = idesc_bf16(128, NK, 0);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, 1);
 
-// MMA issue helpers: called by a whole converged warp with warp-uniform
-// operands; one elected lane issues. (A warp-uniform issue runs ~3x faster
-// than one issued from a single-lane branch.)
+// MMA issue: a warp elects one lane once (elect_one), and that lane issues a
+// whole group of MMAs and commits with the single-thread helpers below. One
+// lane issuing a straight run keeps the tensor pipe fed (~16 cycles per
+// M=128, N=32, K=16 MMA); an elect.sync around every MMA costs ~80 cycles
+// each, which then bounds Q K^T.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile("{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\nselp.u32 %0, 1, 0, e;\n}\n" : "=r"(e));
+  return e != 0;
+}
 __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t acc) {
   asm volatile(
-      "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                        uint32_t acc) {
   asm volatile(
-      "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
 }
-// commits (whole warp, one elected lane); the multicast form's arrival lands
-// at the same offset in the CTAs of `mask`
+// commits (the issuing lane); the multicast form's arrival lands at the same
+// offset in the CTAs of `mask`
 __device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
   asm volatile(
-      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;\n}\n" ::"r"(bar), "h"(mask)
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n" ::"r"(bar), "h"(mask)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
-      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void fence_before() {
@@ -633,18 +638,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t ra = sbase + RA_OFF + sa * RA_SLOT_BYTES;
           const uint32_t rv = sbase + VO_OFF + (ig % VO_SLOTS) * V_SLOT_BYTES;
           const uint32_t sd = tmem + COL_S + b * NK;
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < QT_DIMS / 16; ++kk)
-            mma_ts(sd, tmem + COL_Q + kk * 8,
-                   sdesc(kv_block(ra, rv, c, kk >> 2) + (kk & 3) * 32, 16, 1024), IDESC_QK, kk > 0);
+            for (int kk = 0; kk < QT_DIMS / 16; ++kk)
+              mma_ts(sd, tmem + COL_Q + kk * 8,
+                     sdesc(kv_block(ra, rv, c, kk >> 2) + (kk & 3) * 32, 16, 1024), IDESC_QK, kk > 0);
 #pragma unroll
-          for (int kk = QT_DIMS / 16; kk < D / 16; ++kk) {
-            const int qk = kk - QT_DIMS / 16;
-            mma_ss(sd, sdesc(qs0 + (qk >> 2) * (HG * 128) + (qk & 3) * 32, 16, 1024),
-                   sdesc(kv_block(ra, rv, c, kk >> 2) + (kk & 3) * 32, 16, 1024), IDESC_QK, 1);
+            for (int kk = QT_DIMS / 16; kk < D / 16; ++kk) {
+              const int qk = kk - QT_DIMS / 16;
+              mma_ss(sd, sdesc(qs0 + (qk >> 2) * (HG * 128) + (qk & 3) * 32, 16, 1024),
+                     sdesc(kv_block(ra, rv, c, kk >> 2) + (kk & 3) * 32, 16, 1024), IDESC_QK, 1);
+            }
+            mma_commit(bar(B_SFULL + b));
+            mma_commit(bar(B_EMPTYA + sa));   // ring A slot: Q K^T was its last reader
           }
-          mma_commit(bar(B_SFULL + b));
-          mma_commit(bar(B_EMPTYA + sa));   // ring A slot: Q K^T was its last reader
+          __syncwarp();
         }
       }
       timed_out = !ok;
@@ -668,12 +676,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             if (!ok) break;
             fence_after();
             const uint32_t vb = sbase + VO_OFF + so * V_SLOT_BYTES;
+            if (elect_one()) {
 #pragma unroll
-            for (int ks = 0; ks < NK / 16; ++ks)
-              mma_ts(tmem + COL_O, tmem + COL_S + sb * NK + ks * 8,
-                     sdesc(vb + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (t > 0 || ks > 0));
-            mma_commit(bar(B_SFREE + sb));    // S / P buffer may take own tile ig + 2
-            mma_commit(bar(B_EMPTYVO + so));
+              for (int ks = 0; ks < NK / 16; ++ks)
+                mma_ts(tmem + COL_O, tmem + COL_S + sb * NK + ks * 8,
+                       sdesc(vb + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (t > 0 || ks > 0));
+              mma_commit(bar(B_SFREE + sb));    // S / P buffer may take own tile ig + 2
+              mma_commit(bar(B_EMPTYVO + so));
+            }
+            __syncwarp();
             ++ig;
           } else {
             const int sp = jg % VP_SLOTS, xs = jg % XP_SLOTS;
@@ -687,16 +698,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             fence_after();
             fence_proxy_async();   // V by cp.async, P by a bulk copy
             const uint32_t vb = sbase + VP_OFF + sp * V_SLOT_BYTES;
+            if (elect_one()) {
 #pragma unroll
-            for (int ks = 0; ks < NK / 16; ++ks)
-              mma_ss(tmem + COL_O, sdesc64(sbase + XP_OFF + xs * P_SLOT_BYTES + ks * 32),
-                     sdesc(vb + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (t > 0 || ks > 0));
-            mma_commit(bar(B_EMPTYVP + sp));
-            mma_commit_multicast(bar(B_XPFREE + xs), (uint16_t)(1u << peer));   // the peer may refill
+              for (int ks = 0; ks < NK / 16; ++ks)
+                mma_ss(tmem + COL_O, sdesc64(sbase + XP_OFF + xs * P_SLOT_BYTES + ks * 32),
+                       sdesc(vb + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (t > 0 || ks > 0));
+              mma_commit(bar(B_EMPTYVP + sp));
+              mma_commit_multicast(bar(B_XPFREE + xs), (uint16_t)(1u << peer));   // the peer may refill
+            }
+            __syncwarp();
             ++jg;
           }
         }
-        if (ok && T > 0) mma_commit(bar(B_OFULL + pass));
+        if (ok && T > 0) {
+          if (elect_one()) mma_commit(bar(B_OFULL + pass));
+          __syncwarp();
+        }
       }
       timed_out = !ok;
     }
