@@ -429,38 +429,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int n_own = T > c ? (T - c + 1) / 2 : 0;
   const int32_t *idx_row = idx + (int64_t)r * K;
 
-  if (tid == 0) {
-    for (int s = 0; s < RA_SLOTS; ++s) {
-      bar_init(bar(B_FULLA + s), NPROD);
-      bar_init(bar(B_EMPTYA + s), 1);
+  if (warp == 1) {
+    // one barrier per lane: its arrival count
+    static_assert(B_COUNT <= 32, "one lane per barrier");
+    if (lane < B_COUNT) {
+      const int i = lane;
+      const bool prod = (i >= B_FULLA && i < B_FULLA + RA_SLOTS) || (i >= B_FULLVP && i < B_FULLVP + VP_SLOTS);
+      const bool four = (i >= B_PFULL && i < B_PFULL + NSB) || i == B_VOTE || i == B_QSTAGED;
+      bar_init(bar(i), prod ? NPROD : four ? 4 : 1);
+      asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
-    for (int s = 0; s < VO_SLOTS; ++s) bar_init(bar(B_EMPTYVO + s), 1);
-    for (int s = 0; s < VP_SLOTS; ++s) {
-      bar_init(bar(B_FULLVP + s), NPROD);
-      bar_init(bar(B_EMPTYVP + s), 1);
+    if (lane == 0) {
+      *s_redo = 0u;
+      *s_last = 0u;
+      *s_fail = 0u;
     }
-    for (int b = 0; b < NSB; ++b) {
-      bar_init(bar(B_SFULL + b), 1);
-      bar_init(bar(B_SFREE + b), 1);
-      bar_init(bar(B_PFULL + b), 4);
-    }
-    for (int s = 0; s < XP_SLOTS; ++s) {
-      bar_init(bar(B_XPFULL + s), 1);
-      bar_init(bar(B_XPFREE + s), 1);
-    }
-    bar_init(bar(B_XMAX), 1);
-    for (int p = 0; p < 2; ++p) {
-      bar_init(bar(B_XEND + p), 1);
-      bar_init(bar(B_OFULL + p), 1);
-    }
-    bar_init(bar(B_VOTE), 4);
-    bar_init(bar(B_DECIDE), 1);
-    bar_init(bar(B_QLOAD), 1);
-    bar_init(bar(B_QSTAGED), 4);
-    *s_redo = 0u;
-    *s_last = 0u;
-    *s_fail = 0u;
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(
@@ -857,8 +840,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // ------------------------------------------------------------ epilogue ----
   // Warps 0-7 (two per TMEM lane quarter, 128 columns each) read O once the
   // last P V is done, scale it by 1 / l, write it as bf16 into four 128-byte
-  // swizzled 16 KB blocks over the free ring A, and one thread stores the
-  // blocks with tensor copies (heads past H are clipped by the copy).
+  // swizzled 16 KB blocks over the free ring A, and one thread of each half
+  // stores its two blocks with tensor copies (heads past H are clipped by
+  // the copy).
   if (warp < 8) {
     if (timed_out) atomicOr((uint32_t *)s_fail, 1u);
     named_bar_sync(1, 256);             // 1 / l, the pass count and failures are in place
@@ -900,10 +884,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
     }
     fence_proxy_async();                // the tensor stores read through the async proxy
-    named_bar_sync(1, 256);
-    if (tid == 0) {
+    // each half (four warps) stores its two blocks as soon as it has
+    // written them
+    if (half == 0)
+      named_bar_sync(2, 128);
+    else
+      named_bar_sync(3, 128);
+    if ((warp & 3) == 0 && lane == 0) {
 #pragma unroll 1
-      for (int b = 0; b < 4; ++b)
+      for (int b = 2 * half; b < 2 * half + 2; ++b)
         asm volatile(
             "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];\n" ::"l"(
                 reinterpret_cast<uint64_t>(&tmap_o)),
@@ -911,6 +900,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             : "memory");
       asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
       asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+    }
+    if (tid == 0) {
       // every P sent must have been consumed by the peer (its multicast
       // commit arrives here) before this CTA's shared memory goes away
       if (!timed_out) {
