@@ -435,7 +435,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (lane < B_COUNT) {
       const int i = lane;
       const bool prod = (i >= B_FULLA && i < B_FULLA + RA_SLOTS) || (i >= B_FULLVP && i < B_FULLVP + VP_SLOTS);
-      const bool four = (i >= B_PFULL && i < B_PFULL + NSB) || i == B_VOTE || i == B_QSTAGED;
+      const bool four = (i >= B_PFULL && i < B_PFULL + NSB) || i == B_VOTE;
       bar_init(bar(i), prod ? NPROD : four ? 4 : 1);
       asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -484,27 +484,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
   bool timed_out = false;
   int own_sent = 0;        // own tiles whose P went to the peer (softmax warps)
-  if (warp < 4) {
-    // staged Q dims 0..383 -> TMEM columns [256, 448): lane = head, column j
-    // holds dims 2j, 2j+1; then the staging slots are free for KV tiles and
-    // the Q K^T issuers may start (B_QSTAGED)
+  if (warp == 0) {
+    // staged Q dims 0..383 -> TMEM columns [256, 448), the layout the Q K^T
+    // MMAs read their A operand in: one 128-row x 32-byte tensor-memory copy
+    // per 16-dim slice (the slice the MMA would read from shared memory),
+    // issued by one lane; their completion (B_QSTAGED) frees the staging
+    // slots for KV tiles and lets the Q K^T issuers start
     if (!warp_wait(bar(B_QLOAD), 0)) timed_out = true;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    fence_after();
+    if (elect_one()) {
 #pragma unroll 1
-    for (int part = 0; part < QT_DIMS / 64; ++part) {
-      const unsigned char *blk = sm + q_stage_off(part) + tid * 128;
-      uint32_t v[32];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(blk + ((k ^ (tid & 7)) << 4));
-        v[4 * k] = w.x; v[4 * k + 1] = w.y; v[4 * k + 2] = w.z; v[4 * k + 3] = w.w;
-      }
-      TMEM_ST32(lane_base + COL_Q + part * 32, v);
+      for (int kk = 0; kk < QT_DIMS / 16; ++kk)
+        asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;\n" ::"r"(tmem + COL_Q + kk * 8),
+                     "l"(sdesc(sbase + q_stage_off(kk >> 2) + (kk & 3) * 32, 16, 1024))
+                     : "memory");
+      mma_commit(bar(B_QSTAGED));
     }
-    tmem_wait_st();
-    fence_before();
     __syncwarp();
-    if (lane == 0) bar_arrive(bar(B_QSTAGED));
   }
 
   // Up to here the kernel has read only q. It is launched as a programmatic
