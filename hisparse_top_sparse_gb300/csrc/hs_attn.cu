@@ -44,7 +44,12 @@
 // Warp roles (480 threads): warps 0-3 softmax, P exchange and epilogue (thread
 // = head = TMEM lane), warps 4-11 gather producers (eight threads per key, one
 // 16-byte chunk of each 64-dim block per thread), warps 12-13 issue Q K^T for
-// own tiles into S buffers 0 / 1, warp 14 issues P V for every tile in order.
+// own tiles into S buffers 0 / 1, warp 14 issues P V for every tile. The
+// gathers and the P V walk the tiles pair by pair with the CTA's own tile
+// first (CTA 1 takes tile 2k + 1 before 2k): the peer's P comes through
+// distributed shared memory about half a microsecond after the CTA's own P
+// of the same pair, and an own tile queued behind it would hold its ring
+// slots that much longer.
 // The kernel is a programmatic dependent launch: its prologue (barriers, TMEM,
 // Q) overlaps the previous kernel (hs_resolve_topk releases it at entry), and
 // it reads the indices and request flags after griddepcontrol.wait.
@@ -264,10 +269,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, bar_wait(bar, parity));
 }
 
-// a hint: `bytes` (a multiple of 16) from p into L2
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                "r"(valid ? 16 : 0)
@@ -408,7 +409,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 int64_t n_hot, const int32_t *__restrict__ row_req,
                 const int32_t *__restrict__ fully_resident, int32_t n_reqs,
                 const int32_t *__restrict__ idx, int32_t H, int32_t K, float scale_log2,
-                int32_t wave,
                 __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, uint32_t *status) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm =
@@ -433,6 +433,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int T = (K + NK - 1) / NK;
   const int n_own = T > c ? (T - c + 1) / 2 : 0;
   const int32_t *idx_row = idx + (int64_t)r * K;
+  // Position i of the tile sequence that the gathers and the P V issuer walk:
+  // every pair of tiles with this CTA's own tile first (CTA 1 swaps the
+  // pairs), so that an own tile's P V never waits behind the peer's P.
+  auto tile_at = [&](int i) -> int {
+    return (c == 1 && i < T && (i ^ 1) < T) ? (i ^ 1) : i;
+  };
 
   if (warp == 1) {
     // one barrier per lane: its arrival count
@@ -539,11 +545,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (!bar_wait(bar(B_DECIDE), 0)) { timed_out = true; break; }
         if (!*s_redo) break;
       }
-      int32_t id0 = load_id(0), id1 = load_id(1);
-      for (int t = 0; t < T; ++t) {
+      int32_t id0 = load_id(tile_at(0)), id1 = load_id(tile_at(1));
+      for (int i = 0; i < T; ++i) {
+        const int t = tile_at(i);
         const int32_t id = id0;
         id0 = id1;
-        id1 = load_id(t + 2);
+        id1 = load_id(tile_at(i + 2));
         const bool v = id >= 0 && id < n_kv;
         const char *src = kv + (v ? (int64_t)id * ROWB : 0);
         if ((t & 1) == c) {
@@ -597,34 +604,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
     }
     cp_async_wait<0>();
-    // While this CTA drains: the row group that will start in the next wave
-    // (wave = the clusters resident at once) gets its Q (this CTA's half)
-    // and the rows of its first four tiles (tiles c and c + 2 here) brought
-    // into L2, so that its first tiles do not wait on DRAM. Warp 8 has
-    // nothing else to do and takes no part in the epilogue.
-    if (warp == 8 && !timed_out && wave > 0 && rg + wave < (int)(gridDim.x >> 1)) {
-      const int rg2 = rg + wave, r2 = rg2 / n_hg, h2 = (rg2 % n_hg) * HG;
-      const uint32_t qbytes = (uint32_t)((H - h2 < HG ? H - h2 : HG) * ROWB);
-      const uint32_t mid = (qbytes / 2 + 15u) & ~15u;
-      const uint32_t lo = c ? mid : 0u, hi = c ? qbytes : mid;
-      const char *q2 = q + ((int64_t)r2 * H + h2) * ROWB;
-      for (uint32_t off = lo + (uint32_t)lane * 16384u; off < hi; off += 32u * 16384u)
-        prefetch_l2(q2 + off, hi - off < 16384u ? hi - off : 16384u);
-      const int32_t req2 = fully_resident ? (row_req ? __ldg(row_req + r2) : r2) : 0;
-      const bool ok2 = !fully_resident || (req2 >= 0 && req2 < n_reqs);
-      const bool hot2 = ok2 && fully_resident && __ldg(fully_resident + req2) == 0;
-      const char *kv2 = hot2 ? kv_hot : kv_res;
-      const int64_t nkv2 = !ok2 ? 0 : hot2 ? n_hot : n_res;
-      int32_t ids[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int jj = (c + 2 * j) * NK + lane;
-        ids[j] = (c + 2 * j < T && jj < K) ? __ldg(idx + (int64_t)r2 * K + jj) : -1;
-      }
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-        if (ids[j] >= 0 && ids[j] < nkv2) prefetch_l2(kv2 + (int64_t)ids[j] * ROWB, ROWB);
-    }
   } else if (warp >= 12 && warp < 12 + NSB) {
     // ------------------------------------- Q K^T issuers (own tiles) ----
     // warp 12 + b issues own tiles ig = b, b + 2, ... into S buffer b
@@ -670,7 +649,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       timed_out = !ok;
     }
   } else if (warp == 12 + NSB) {
-    // ------------------------------------ P V issuer (every tile, in order) ----
+    // ------------------------- P V issuer (every tile, own tile of a pair first) ----
     __syncwarp();
     cluster_wait();                                // the peer's barriers exist
     {
@@ -681,7 +660,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           ok = warp_wait(bar(B_DECIDE), 0);
           if (!ok || !*s_redo) break;
         }
-        for (int t = 0; t < T && ok; ++t) {
+        for (int i = 0; i < T && ok; ++i) {
+          const int t = tile_at(i);
           if ((t & 1) == c) {
             const int sb = ig % NSB, so = ig % VO_SLOTS;
             ok = warp_wait(bar(B_PFULL + sb), (ig / NSB) & 1);
@@ -692,7 +672,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int ks = 0; ks < NK / 16; ++ks)
                 mma_ts(tmem + COL_O, tmem + COL_S + sb * NK + ks * 8,
-                       sdesc(vb + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (t > 0 || ks > 0));
+                       sdesc(vb + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (i > 0 || ks > 0));
               mma_commit(bar(B_SFREE + sb));    // S / P buffer may take own tile ig + 2
               mma_commit(bar(B_EMPTYVO + so));
             }
@@ -714,7 +694,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int ks = 0; ks < NK / 16; ++ks)
                 mma_ss(tmem + COL_O, sdesc64(sbase + XP_OFF + xs * P_SLOT_BYTES + ks * 32),
-                       sdesc(vb + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (t > 0 || ks > 0));
+                       sdesc(vb + ks * 2048, KV_BLOCK_BYTES, 1024), IDESC_PV, (i > 0 || ks > 0));
               mma_commit(bar(B_EMPTYVP + sp));
               mma_commit_multicast(bar(B_XPFREE + xs), (uint16_t)(1u << peer));   // the peer may refill
             }
@@ -1049,10 +1029,6 @@ int hs_attn_launch(const void *q, const void *kv_resident, int64_t n_resident, c
   if (rc) return rc;
   const int64_t blocks = (int64_t)R * ((H + HG - 1) / HG) * 2;
   if (blocks > INT32_MAX) return hs_set_error(HS_ERR_UNSUPPORTED, "R*H too large");
-  int32_t wave_rows = 0;
-  rc = hs_attn_wave_rows(H, &wave_rows);
-  if (rc) return rc;
-  const int32_t wave = wave_rows * ((H + HG - 1) / HG);   // clusters resident at once
   // q as a [R][H][576] bf16 tensor for the prologue's tensor copies
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
@@ -1098,7 +1074,7 @@ int hs_attn_launch(const void *q, const void *kv_resident, int64_t n_resident, c
       &cfg, k_attn_pair, tmap, tmap_o, reinterpret_cast<const char *>(q),
       reinterpret_cast<const char *>(kv_resident), n_resident,
       reinterpret_cast<const char *>(kv_hot), n_hot, row_req, fully_resident, n_reqs, idx, H, K,
-      scale * 1.4426950408889634f, wave, reinterpret_cast<__nv_bfloat16 *>(out), lse, status));
+      scale * 1.4426950408889634f, reinterpret_cast<__nv_bfloat16 *>(out), lse, status));
   HS_LAUNCH_CHECK("k_attn_pair");
   return HS_OK;
 }
