@@ -31,9 +31,11 @@
 //   * the KV rows of an own tile are gathered whole (16-byte cp.async, each
 //     producer thread's copies arriving on the tile's mbarrier as they land):
 //     the four 64-dim swizzle blocks of this CTA's value half into ring VO
-//     (3 slots), the other five into ring A (3 slots, each freed once its
-//     Q K^T is done); of a peer tile
-//     only this CTA's value half is gathered, into ring VP;
+//     (4 slots), the other five into ring A (3 slots, each freed once its
+//     Q K^T is done); of a peer tile only this CTA's value half is
+//     gathered, into ring VP (2 slots), and two own tiles later than it
+//     would be in tile order: its rows are read only once the peer's P has
+//     come, so a VP slot is held about 1.3 us instead of 3;
 //   * both CTAs use one softmax reference per head: the larger of their first
 //     tiles' maxima, agreed through distributed shared memory before any P is
 //     made, so every P of the row is on one scale and O is never rescaled. A
@@ -74,7 +76,8 @@ constexpr int QT_DIMS = 384;              // Q dims held in TMEM
 constexpr int QS_BLOCKS = (D - QT_DIMS) / 64;   // 3 swizzle blocks of Q in SMEM
 constexpr int NSB = 2;                    // S / P buffers (own tiles)
 constexpr int VB_BLOCKS = 4;              // swizzle blocks of one value half
-constexpr int RA_SLOTS = 3, VO_SLOTS = 3, VP_SLOTS = 3, XP_SLOTS = 1;
+constexpr int RA_SLOTS = 3, VO_SLOTS = 4, VP_SLOTS = 2, XP_SLOTS = 1;
+constexpr int PEER_LAG = 2;               // own tiles gathered ahead of the peer tiles
 constexpr int THREADS = 480;
 constexpr int NPROD = 256;
 constexpr float REF_SLACK = 30.0f;        // P <= 2^30 on the shared reference
@@ -147,17 +150,18 @@ __device__ __forceinline__ uint32_t kv_block(uint32_t ra, uint32_t rv, int c, in
 }
 
 // Staging place of Q block a (dims 64a..64a+63, a < 6) before it moves into
-// TMEM: slots 1-2 of ring A (two blocks), slots 1-2 of ring VO and the two P
-// buffers (three blocks), slot 1 of ring VP (one block). Slot 0 of each ring
-// is left for the first tiles, which are gathered meanwhile.
+// TMEM: slots 1-2 of ring A (two blocks), slots 1-3 of ring VO (three
+// blocks), the two P buffers (one block). Slot 0 of rings A and VO and all of
+// ring VP are left for the first tiles, which are gathered meanwhile.
 __host__ __device__ constexpr uint32_t q_stage_off(int a) {
   return a < 2 ? RA_OFF + RA_SLOT_BYTES + a * (HG * 128)
-               : a < 5 ? VO_OFF + V_SLOT_BYTES + (a - 2) * (HG * 128) : VP_OFF + V_SLOT_BYTES;
+               : a < 5 ? VO_OFF + V_SLOT_BYTES + (a - 2) * (HG * 128) : XS_OFF;
 }
 static_assert(q_stage_off(1) + HG * 128 <= RA_OFF + RA_SLOTS * RA_SLOT_BYTES &&
-                  q_stage_off(4) + HG * 128 == VP_OFF && q_stage_off(0) % 1024 == 0 &&
-                  q_stage_off(1) % 1024 == 0 && q_stage_off(2) % 1024 == 0 &&
-                  q_stage_off(5) % 1024 == 0 && RA_SLOTS == 3 && VO_SLOTS == 3 && VP_SLOTS >= 2,
+                  q_stage_off(4) + HG * 128 == XS_OFF && XS_OFF + HG * 128 == VP_OFF &&
+                  q_stage_off(0) % 1024 == 0 && q_stage_off(1) % 1024 == 0 &&
+                  q_stage_off(2) % 1024 == 0 && q_stage_off(5) % 1024 == 0 && RA_SLOTS == 3 &&
+                  VO_SLOTS == 4 && XP_SLOTS == 1,
               "Q staging map");
 
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
@@ -432,6 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int h0 = (rg % n_hg) * HG;
   const int T = (K + NK - 1) / NK;
   const int n_own = T > c ? (T - c + 1) / 2 : 0;
+  const int n_peer = T - n_own;
   const int32_t *idx_row = idx + (int64_t)r * K;
   // Position i of the tile sequence that the gathers and the P V issuer walk:
   // every pair of tiles with this CTA's own tile first (CTA 1 swaps the
@@ -474,10 +479,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // Q by nine tensor copies of 128 heads x 64 dims (16 KB, 128-byte swizzle,
   // rows past H filled with zeros), all issued by this CTA into its own
   // shared memory: dims 384..575 land in SMEM as the MMA's A operand, dims
-  // 0..383 in a staging area over the (still empty) slots 1 and 2 of rings
-  // A and VO, the P buffers and slot 1 of ring VP, from where each head's
-  // thread moves them into TMEM. Slot 0 of every ring stays free, so the
-  // first own and the first peer tile are gathered while Q comes in.
+  // 0..383 in a staging area over the (still empty) slots 1 and 2 of ring
+  // A, 1 to 3 of ring VO and the P buffers, from where one lane moves them
+  // into TMEM. Slot 0 of rings A and VO and ring VP stay free, so the first
+  // own and the first peer tiles are gathered while Q comes in.
   // The copies are issued by the P V issuer warp, whose first MMA waits for
   // the first P anyway: issuing them can stall the issuing thread for
   // microseconds while the other CTAs of the wave load their Q.
@@ -545,12 +550,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (!bar_wait(bar(B_DECIDE), 0)) { timed_out = true; break; }
         if (!*s_redo) break;
       }
-      int32_t id0 = load_id(tile_at(0)), id1 = load_id(tile_at(1));
+      // gather order: the own tiles run up to PEER_LAG + 1 ahead of the
+      // peer tiles, whose value halves are read only once the peer's P has
+      // come, so that a ring VP slot is taken only shortly before its use
+      int na = 0, nb = 0;             // own / peer tiles of this pass taken
+      int la = 0, lb = 0;             // the same two steps ahead (index prefetch)
+      auto step = [&](int &a, int &b) -> int {
+        if (a < n_own && (b >= n_peer || a < b + PEER_LAG + 1)) return 2 * (a++) + c;
+        if (b < n_peer) return 2 * (b++) + (1 - c);
+        return T;
+      };
+      const int t0 = step(la, lb);
+      const int t1 = step(la, lb);
+      int32_t id0 = load_id(t0), id1 = load_id(t1);
       for (int i = 0; i < T; ++i) {
-        const int t = tile_at(i);
+        const int t = step(na, nb);
         const int32_t id = id0;
         id0 = id1;
-        id1 = load_id(tile_at(i + 2));
+        id1 = load_id(step(la, lb));
         const bool v = id >= 0 && id < n_kv;
         const char *src = kv + (v ? (int64_t)id * ROWB : 0);
         if ((t & 1) == c) {
@@ -582,10 +599,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           ++ig;
         } else {
           const int sp = jg % VP_SLOTS;
-          if (jg == 1 && !bar_wait(bar(B_QSTAGED), 0)) {
-            timed_out = true;
-            break;
-          }
           if (jg >= VP_SLOTS && !bar_wait(bar(B_EMPTYVP + sp), ((jg / VP_SLOTS) - 1) & 1)) {
             timed_out = true;
             break;
