@@ -79,6 +79,14 @@ constexpr int VB_BLOCKS = 4;              // swizzle blocks of one value half
 constexpr int RA_SLOTS = 3, VO_SLOTS = 4, VP_SLOTS = 2, XP_SLOTS = 1;
 constexpr int PEER_LAG = 2;               // own tiles gathered ahead of the peer tiles
 constexpr int THREADS = 480;
+// Registers per thread, at most: a swap-in gather block (256 threads, 56
+// registers each) must fit beside one attention CTA in each of the SM's four
+// register-file quarters (16 K registers; four attention warps and two gather
+// warps share one) so that the one-call step overlaps its copies with the
+// attention. 4 x 96 x 32 + 2 x 56 x 32 = 15,872; at 98 (rounded to 104) it
+// no longer fits and the copies wait for whole SMs.
+#define ATTN_MAX_REGS 96
+static_assert(THREADS * ATTN_MAX_REGS <= 65536, "register budget");
 constexpr int NPROD = 256;
 constexpr float REF_SLACK = 30.0f;        // P <= 2^30 on the shared reference
 
@@ -406,7 +414,7 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity)
   return __all_sync(0xffffffffu, bar_wait_cluster(bar, parity));
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(ATTN_MAX_REGS)
     k_attn_pair(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_o,
                 const char *__restrict__ q,
                 const char *__restrict__ kv_res, int64_t n_res, const char *__restrict__ kv_hot,

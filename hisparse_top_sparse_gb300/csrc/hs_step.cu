@@ -17,11 +17,12 @@
 //            between two streams so that a group's attention fills the SMs the
 //            previous group's last wave leaves idle
 // A gather block (256 threads, 54 registers, 144 + 4 * (max_reqs + 1) bytes of
-// shared memory) fits on an SM beside one attention CTA (480 threads, 93
-// registers, 229,376 bytes; the SM keeps 3 KB of shared memory and 19 K
-// registers) for up to 448 requests, so the later gathers take no SM away
-// from the attention. The caller's stream waits for every side stream before
-// the call returns.
+// shared memory) fits on an SM beside one attention CTA (480 threads, at most
+// 96 registers, 229,376 bytes; the SM keeps 3 KB of shared memory, and each of
+// its four register-file quarters holds four attention warps and two gather
+// warps) for up to 448 requests, so the later gathers take no SM away from
+// the attention. The caller's stream waits for every side stream before the
+// call returns.
 
 #include <algorithm>
 
