@@ -40,6 +40,7 @@ EXPORTS = (
     "hs_verify_accept_noalloc", "hs_swap_apply_plan", "hs_backup_pages", "hs_reclaim_resident",
     "hs_sparse_attn_decode_mixed", "hs_backup_rows", "hs_backup_indexer",
     "hs_buffer_set_copy_sms", "hs_swap_in_attn_decode", "hs_step_groups",
+    "hs_step_overlap_fits",
 )
 
 
@@ -92,6 +93,7 @@ def lib() -> ctypes.CDLL:
             "hs_swap_in_attn_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _I, ctypes.c_float,
                                             _I, _P, _P, _P, _P, _P, _P, _P]),
             "hs_step_groups": (_I, [_I, _I, _P, _P]),
+            "hs_step_overlap_fits": (_I, [_I, _P]),
             "hs_reclaim_resident": (_I, [_P, _I, _I, _P, _I, _P, _P, _P, _P]),
             "hs_verify_finalize": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
             "hs_read_probe": (_I, [_P, ctypes.c_size_t, _P, _I, _P]),
@@ -303,6 +305,14 @@ def hs_step_groups(R: int, H: int) -> list:
     ends = (ctypes.c_int32 * 8)()
     _check(lib().hs_step_groups(int(R), int(H), ctypes.byref(n), ends), "hs_step_groups")
     return [int(ends[i]) for i in range(n.value)]
+
+
+def hs_step_overlap_fits(max_reqs: int) -> bool:
+    """Whether a copy block of hs_swap_in_attn_decode fits on an SM beside an
+    attention CTA on the current device (for a buffer of max_reqs requests)."""
+    f = ctypes.c_int32(0)
+    _check(lib().hs_step_overlap_fits(int(max_reqs), ctypes.byref(f)), "hs_step_overlap_fits")
+    return bool(f.value)
 
 
 def hs_sparse_attn_decode_mixed(q, kv_resident, kv_hot, row_req, fully_resident, idx,

@@ -990,6 +990,15 @@ static int set_attn_attributes() {
   return HS_OK;
 }
 
+int hs_attn_block_attrs(cudaFuncAttributes *attr, int *threads, size_t *dyn_smem) {
+  int rc = set_attn_attributes();
+  if (rc) return rc;
+  HS_CUDA_TRY(cudaFuncGetAttributes(attr, k_attn_pair));
+  *threads = THREADS;
+  *dyn_smem = SMEM_ALLOC;
+  return HS_OK;
+}
+
 int hs_attn_wave_rows(int32_t H, int32_t *rows) {
   int rc = set_attn_attributes();
   if (rc) return rc;

@@ -141,6 +141,12 @@ int hs_attn_launch(const void *q, const void *kv_resident, int64_t n_resident, c
 // Rows of H heads that one wave of the attention kernel holds on the current
 // device (two-SM clusters resident at once, per row's head groups); >= 1.
 int hs_attn_wave_rows(int32_t H, int32_t *rows);
+// The attention kernel's attributes (registers, static shared memory) and the
+// threads and dynamic shared memory of one CTA.
+int hs_attn_block_attrs(cudaFuncAttributes *attr, int *threads, size_t *dyn_smem);
+// The same for the swap-in gather kernel (its dynamic shared memory depends
+// on the launch: 4 * (max_reqs + 1) bytes).
+int hs_gather_func_attrs(cudaFuncAttributes *attr);
 
 // ---- argmax of one logits row (greedy verify) -------------------------------
 

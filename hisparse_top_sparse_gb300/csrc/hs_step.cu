@@ -30,6 +30,8 @@
 
 namespace {
 
+constexpr int STEP_GATHER_THREADS = 256;   // a later group's gather block, one per SM
+
 // Rows [ends[g-1], ends[g]) of the automatic split: the first group one
 // attention wave (its copies are the only ones not hidden), the other rows in
 // at most HS_MAX_GROUPS - 1 groups of equal size, a whole number of waves
@@ -64,6 +66,39 @@ extern "C" int hs_step_groups(int32_t R, int32_t H, int32_t *n_groups, int32_t *
   *n_groups = 0;
   if (R == 0) return HS_OK;
   return auto_groups(R, H, n_groups, group_row_end);
+}
+
+extern "C" int hs_step_overlap_fits(int32_t max_reqs, int32_t *fits) {
+  if (max_reqs < 1 || max_reqs > HS_MAX_REQS || !fits)
+    return hs_set_error(HS_ERR_INVALID_ARG, "max_reqs %d not in 1..%d or NULL fits", max_reqs,
+                        HS_MAX_REQS);
+  *fits = 0;
+  cudaFuncAttributes fa, fg;
+  int attn_threads = 0;
+  size_t attn_dyn = 0;
+  int rc = hs_attn_block_attrs(&fa, &attn_threads, &attn_dyn);
+  if (rc) return rc;
+  rc = hs_gather_func_attrs(&fg);
+  if (rc) return rc;
+  int dev = 0, regs_sm = 0, smem_sm = 0, smem_rsv = 0, threads_sm = 0;
+  HS_CUDA_TRY(cudaGetDevice(&dev));
+  HS_CUDA_TRY(cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev));
+  HS_CUDA_TRY(cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
+  HS_CUDA_TRY(cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev));
+  HS_CUDA_TRY(cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev));
+  // registers: a warp holds its threads' count rounded up to 8, times 32;
+  // a CTA's warps spread over the SM's four schedulers, each with a quarter
+  // of the register file, so the fullest quarter holds ceil(warps / 4) of
+  // each block
+  auto warp_regs = [](int per_thread) { return ((per_thread + 7) / 8) * 8 * 32; };
+  const int attn_warps = (attn_threads + 31) / 32, gather_warps = STEP_GATHER_THREADS / 32;
+  const long long quarter = (long long)((attn_warps + 3) / 4) * warp_regs(fa.numRegs) +
+                            (long long)((gather_warps + 3) / 4) * warp_regs(fg.numRegs);
+  const long long smem = (long long)attn_dyn + fa.sharedSizeBytes + smem_rsv +
+                         (long long)(max_reqs + 1) * 4 + fg.sharedSizeBytes + smem_rsv;
+  *fits = quarter <= regs_sm / 4 && smem <= smem_sm &&
+          attn_threads + STEP_GATHER_THREADS <= threads_sm;
+  return HS_OK;
 }
 
 extern "C" int hs_swap_in_attn_decode(hs_buffer *buf, const int32_t *req_id_per_row,
@@ -146,7 +181,7 @@ extern "C" int hs_swap_in_attn_decode(hs_buffer *buf, const int32_t *req_id_per_
   };
   for (int g = 1; g < G; ++g) {
     rc = hs_swap_gather_launch(buf, req_id_per_row, row_causal_len, kv_len, topk, R, K, g,
-                               ends[g - 1], ends[g], out_slot_idx, out_valid, 1, 256, false,
+                               ends[g - 1], ends[g], out_slot_idx, out_valid, 1, STEP_GATHER_THREADS, false,
                                buf->side[0]);
     if (rc) return fail(rc);
     const cudaError_t e = cudaEventRecord(buf->ev_gather[g], buf->side[0]);

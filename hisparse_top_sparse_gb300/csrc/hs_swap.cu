@@ -699,6 +699,11 @@ int hs_swap_plan_launch(hs_buffer *buf, const int32_t *req_id_per_row,
   return HS_OK;
 }
 
+int hs_gather_func_attrs(cudaFuncAttributes *attr) {
+  HS_CUDA_TRY(cudaFuncGetAttributes(attr, k_swap_gather));
+  return HS_OK;
+}
+
 int hs_swap_gather_launch(hs_buffer *buf, const int32_t *req_id_per_row,
                           const int32_t *row_causal_len, const int32_t *kv_len,
                           const int32_t *topk, int32_t R, int32_t K, int32_t g, int32_t row_lo,

@@ -315,6 +315,20 @@ int hs_swap_in_attn_decode(hs_buffer *buf, const int32_t *req_id_per_row,
  */
 int hs_step_groups(int32_t R, int32_t H, int32_t *n_groups, int32_t *group_row_end);
 
+/*
+ * Whether, on the current device, one copy block of hs_swap_in_attn_decode's
+ * later groups (256 threads) fits on an SM beside one attention CTA: the
+ * fullest quarter of the SM's register file (registers are allocated per warp
+ * in units of 8 per thread, and a block's warps spread over the SM's four
+ * schedulers), the shared memory of both (the copy block's grows with the
+ * buffer's max_reqs) and the threads. When it does not, those copies wait
+ * for whole SMs and the call runs no faster than hs_swap_in followed by
+ * hs_sparse_attn_decode (the overlap that "hiSparse-MTP", section 1, gives
+ * the coordinator's asynchronous stream is then lost). Writes *fits (1 or 0);
+ * HS_ERR_INVALID_ARG for max_reqs outside 1..16384 or a NULL fits.
+ */
+int hs_step_overlap_fits(int32_t max_reqs, int32_t *fits);
+
 /* ------------------------------------------------------------------------ */
 /* next-3: a batch mixing fully-resident and host-backed requests            */
 /*         ("vllm 分析(十二) HiSparse 下篇": the HiSparseResidentSpec and      */

@@ -38,6 +38,10 @@ def test_argument_errors_return_without_a_gpu():
     assert L.hs_sparse_attn_decode(None, None, 0, None, 1, 0, 1, ctypes.c_float(1.0), None,
                                    None, None, None) == hs.HS_ERR_INVALID_ARG
     assert L.hs_buffer_create(None, None) == hs.HS_ERR_INVALID_ARG
+    fits = ctypes.c_int32(7)
+    assert L.hs_step_overlap_fits(0, ctypes.byref(fits)) == hs.HS_ERR_INVALID_ARG
+    assert L.hs_step_overlap_fits(16385, ctypes.byref(fits)) == hs.HS_ERR_INVALID_ARG
+    assert L.hs_step_overlap_fits(64, None) == hs.HS_ERR_INVALID_ARG
     assert L.hs_swap_in(None, None, None, None, None, 0, 0, None, None, None,
                         None) == hs.HS_ERR_INVALID_ARG
     # mixed batch: negative cache sizes, a negative request count with flags

@@ -350,3 +350,15 @@ def test_library_groups():
             mid = sizes[1:-1]
             assert (mid == mid[0]).all() and mid[0] % w == 0 and 0 < sizes[-1] <= mid[0]
     assert hs.hs_step_groups(0, 128) == []
+
+
+def test_copy_block_fits_beside_attention():
+    """The later groups' copies overlap the attention only when a copy block
+    fits on an SM beside an attention CTA (register-file quarters, shared
+    memory, threads). A kernel change that breaks this still passes every
+    bit-exactness test, so it is checked here: it holds for buffers of up to
+    448 requests and fails for 16384 (a 64 KB copy-prefix table)."""
+    hs = lib()
+    for max_reqs in (1, 64, 128, 448):
+        assert hs.hs_step_overlap_fits(max_reqs), max_reqs
+    assert not hs.hs_step_overlap_fits(16384)
