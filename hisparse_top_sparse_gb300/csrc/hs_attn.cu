@@ -275,7 +275,7 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
   return bar_wait_n(bar, parity, 1ll << 31);
 }
 
-// The same wait taken by a whole warp, with one verdict for every lane (the
+// The same wait taken by a whole warp, with one answer for every lane (the
 // warp then issues warp-collective tcgen05 loads and stores).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, bar_wait(bar, parity));
