@@ -141,8 +141,8 @@ enum {
   B_COUNT = B_QSTAGED + 1
 };
 static_assert(B_COUNT * 8 + 16 <= 512, "barrier area");
-// O staged for the epilogue's tensor stores: four 16 KB blocks over ring A and
-// the start of ring VO (free once the last P V is done)
+// O staged for the epilogue's stores: four 16 KB blocks over ring A and the
+// start of ring VO (free once the last P V is done)
 constexpr int O_STG_OFF = RA_OFF;
 static_assert(O_STG_OFF + 4 * HG * 128 <= XS_OFF, "O staging");
 
@@ -415,7 +415,7 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity)
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(ATTN_MAX_REGS)
-    k_attn_pair(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_o,
+    k_attn_pair(const __grid_constant__ CUtensorMap tmap_q,
                 const char *__restrict__ q,
                 const char *__restrict__ kv_res, int64_t n_res, const char *__restrict__ kv_hot,
                 int64_t n_hot, const int32_t *__restrict__ row_req,
@@ -870,9 +870,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(ATTN_MAX_REGS)
   // ------------------------------------------------------------ epilogue ----
   // Warps 0-7 (two per TMEM lane quarter, 128 columns each) read O once the
   // last P V is done, scale it by 1 / l, write it as bf16 into four 128-byte
-  // swizzled 16 KB blocks over the free ring A, and one thread of each half
-  // stores its two blocks with tensor copies (heads past H are clipped by
-  // the copy).
+  // swizzled 16 KB blocks over the free ring A, and each half (four warps)
+  // copies its two blocks to the output with coalesced 16-byte stores (rows
+  // past H skipped). A tensor store instead kept the CTA ~1 us waiting for
+  // the copy to read shared memory; these stores drain after the CTA.
   if (warp < 8) {
     if (timed_out) atomicOr((uint32_t *)s_fail, 1u);
     named_bar_sync(1, 256);             // 1 / l, the pass count and failures are in place
@@ -913,23 +914,25 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(ATTN_MAX_REGS)
         }
       }
     }
-    fence_proxy_async();                // the tensor stores read through the async proxy
-    // each half (four warps) stores its two blocks as soon as it has
-    // written them
+    // each half (four warps) copies its two blocks out as soon as it has
+    // written them: lane l of a warp takes 16-byte chunk l & 7 of block
+    // 2 half + ((l >> 3) & 1) of row 8 it + 2 w + (l >> 4), so one warp
+    // store writes two whole 256-byte row segments; nothing waits for the
+    // stores, and the shared memory is free once it has been read
     if (half == 0)
       named_bar_sync(2, 128);
     else
       named_bar_sync(3, 128);
-    if ((warp & 3) == 0 && lane == 0) {
-#pragma unroll 1
-      for (int b = 2 * half; b < 2 * half + 2; ++b)
-        asm volatile(
-            "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];\n" ::"l"(
-                reinterpret_cast<uint64_t>(&tmap_o)),
-            "r"(256 * c + 64 * b), "r"(h0), "r"(r), "r"(sbase + O_STG_OFF + b * (HG * 128))
-            : "memory");
-      asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
-      asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+    {
+      const int wq = warp & 3, b = 2 * half + ((lane >> 3) & 1), j = lane & 7;
+      const unsigned char *src = sm + O_STG_OFF + b * (HG * 128);
+      __nv_bfloat16 *dst_row = out + ((int64_t)r * H + h0) * DV + 256 * c + 64 * b + 8 * j;
+#pragma unroll 4
+      for (int it = 0; it < HG / 8; ++it) {
+        const int row = 8 * it + 2 * wq + (lane >> 4);
+        const uint4 v = *reinterpret_cast<const uint4 *>(src + row * 128 + ((j ^ (row & 7)) << 4));
+        if (h0 + row < H) *reinterpret_cast<uint4 *>(dst_row + (int64_t)row * DV) = v;
+      }
     }
     if (tid == 0) {
       // every P sent must have been consumed by the peer (its multicast
@@ -1080,14 +1083,6 @@ int hs_attn_launch(const void *q, const void *kv_resident, int64_t n_resident, c
                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (er != CUDA_SUCCESS) return hs_set_error(HS_ERR_CUDA, "tensor map of q failed (%d)", (int)er);
-  // out as a [R][H][512] bf16 tensor for the epilogue's tensor stores
-  alignas(64) CUtensorMap tmap_o;
-  const cuuint64_t odim[3] = {(cuuint64_t)DV, (cuuint64_t)H, (cuuint64_t)R};
-  const cuuint64_t ostride[2] = {(cuuint64_t)DV * 2, (cuuint64_t)H * DV * 2};
-  const CUresult eo = encode(&tmap_o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, odim, ostride, box,
-                             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (eo != CUDA_SUCCESS) return hs_set_error(HS_ERR_CUDA, "tensor map of out failed (%d)", (int)eo);
   // a programmatic dependent launch: the prologue (barriers, TMEM, Q) may
   // run while the previous kernel in the stream finishes
   cudaLaunchConfig_t cfg = {};
@@ -1101,7 +1096,7 @@ int hs_attn_launch(const void *q, const void *kv_resident, int64_t n_resident, c
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   HS_CUDA_TRY(cudaLaunchKernelEx(
-      &cfg, k_attn_pair, tmap, tmap_o, reinterpret_cast<const char *>(q),
+      &cfg, k_attn_pair, tmap, reinterpret_cast<const char *>(q),
       reinterpret_cast<const char *>(kv_resident), n_resident,
       reinterpret_cast<const char *>(kv_hot), n_hot, row_req, fully_resident, n_reqs, idx, H, K,
       scale * 1.4426950408889634f, reinterpret_cast<__nv_bfloat16 *>(out), lse, status));
